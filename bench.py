@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""Throughput of the paged-KV hot path on one GB300 (or N, one process each).
+
+A step is one pass of the whole hot path over one batch: the slot mapping
+of the step's new tokens, and per layer the KV write, paged decode
+attention (plan + persistent split kernel + merge) and chunked-prefill
+attention.  The default workload is one layer of a LLaMA-2-70B-shaped
+(GQA-8) mixed step: 256 decode sequences with log-normal lengths
+(median 1024, clipped to 16..8192) plus 4 prefill sequences each with a
+512-token causal chunk over 0..4096 tokens of paged history, in a pool of
+65,536 16-token blocks.  Inputs are seeded synthetic data (workloads/).
+
+Reported (one JSON line from rank 0):
+  value      algorithmic HBM bytes of the step / device time (GB/s), inputs
+             resident in HBM; every step reads ~1.7 GB of KV, more than the
+             129 MB L2, so no flush is needed between steps
+  e2e        the same metric with the step's inputs copied from pinned host
+             memory and its outputs copied back inside the timed region
+  roofline   the decode kernels (the dominant launches) against the measured
+             HBM copy bandwidth; prefill_roofline against the measured bf16
+             tensor peak
+  cpu_baseline  the float64 CPU oracle on a bounded sample of the workload
+
+--impl reference times the CPU oracle (the reference implementation of
+this build) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle's BLAS calls run single-threaded so the baseline's core
+# count is exact (set before numpy is imported).
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("paged decode attn: KV GB/s read (% of GB300 HBM peak), decode tokens/s per step")
+WORKLOAD = "llama2-70b-mixed"
+WORKLOAD_LABEL = "llama2-70b-gqa8-mixed-decode256-prefill4x512"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit -> name
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+    0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------ accounting
+
+
+def step_accounting(plan):
+    """Algorithmic bytes and FLOPs of one layer of the step.
+
+    decode:  each decode sequence's KV (K and V, every token once, shared
+             blocks once), its query and output rows, the table entries it
+             uses and its length;
+    prefill: the same for the prefill sequences' full history + chunk;
+    write:   the new K/V rows read and written into the pool, their slots.
+    prefill FLOPs: 4 * head_dim * n_heads * sum over queries of visible keys.
+    """
+    sh = plan.shape
+    e = sh.itemsize
+    row = sh.n_kv * sh.head_dim * e              # one token's K (or V)
+    qrow = sh.n_heads * sh.head_dim * e
+    nd = plan.n_decode
+    bs = sh.block_size
+
+    def kv_bytes(rows):
+        held = set()
+        tokens = 0
+        for b in rows:
+            L = int(plan.seq_lens[b])
+            nb = -(-L // bs)
+            for j in range(nb):
+                blk = int(plan.block_tables[b, j])
+                if blk in held:
+                    continue  # a shared block is read once
+                held.add(blk)
+                tokens += min(bs, L - j * bs)
+        return tokens * row * 2
+
+    dec_rows = range(nd)
+    pre_rows = range(nd, plan.num_seqs)
+    dec = kv_bytes(dec_rows) + 2 * nd * qrow + sum(4 * (-(-int(plan.seq_lens[b]) // bs)) + 4
+                                                    for b in dec_rows)
+    tq = int(plan.new_lens[nd:].sum())
+    pre = kv_bytes(pre_rows) + 2 * tq * qrow + sum(4 * (-(-int(plan.seq_lens[b]) // bs)) + 8
+                                                    for b in pre_rows)
+    T = plan.num_new_tokens
+    write = T * row * 2 * 2 + T * 8
+    flops = 0
+    for b in pre_rows:
+        L, c = int(plan.seq_lens[b]), int(plan.new_lens[b])
+        vis = sum(L - c + i + 1 for i in range(c))
+        flops += 4 * sh.head_dim * sh.n_heads * vis
+    return dict(decode_bytes=dec, prefill_bytes=pre, write_bytes=write, prefill_flops=flops,
+                decode_kv_bytes=kv_bytes(dec_rows))
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", f"--id={index}",
+                    "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                    "--format=csv,noheader,nounits", f"-lms={period_ms}"]
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 4:
+                continue
+            try:
+                sm, smax = float(parts[0]), float(parts[1])
+                reasons = int(parts[3], 16) if parts[3].startswith("0x") else int(parts[3])
+            except ValueError:
+                continue
+            self.samples.append((sm, smax, reasons))
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [s for s in self.samples if not (s[2] & 0x1)] or self.samples
+        names = set()
+        for _, _, r in busy:
+            for bit, name in THROTTLE_BITS.items():
+                if r & bit and name != "gpu_idle":
+                    names.add(name)
+        return {"sm_mhz": float(np.median([s[0] for s in busy])),
+                "sm_max_mhz": float(max(s[1] for s in busy)), "reasons": sorted(names),
+                "samples": len(busy)}
+
+
+# ----------------------------------------------------------- distributed
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ CPU oracle
+
+
+def oracle_sample(plan, layer, n_decode: int, n_prefill_queries: int, offset: int = 0):
+    """Time the float64 oracle on a bounded sample of the step: n_decode
+    decode sequences and n_prefill_queries prefill queries (spread over the
+    prefill chunks).  Returns (seconds, algorithmic bytes of the sample)."""
+    import torch
+    import oracle
+
+    def raw(t):
+        t = t.contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    sh = plan.shape
+    dt = sh.dtype
+    row = sh.n_kv * sh.head_dim * sh.itemsize
+    qrow = sh.n_heads * sh.head_dim * sh.itemsize
+    kp, vp = raw(layer["k_pool"]), raw(layer["v_pool"])
+    q = raw(layer["q"])
+    nd = plan.n_decode
+    rows = [(offset + i) % nd for i in range(min(n_decode, nd))] if nd else []
+    pre = []
+    npre = plan.num_seqs - nd
+    for j in range(n_prefill_queries if npre else 0):
+        b = nd + j % npre
+        c = int(plan.new_lens[b])
+        pre.append((b, ((offset + j) * 97) % c))
+    t0 = time.perf_counter()
+    if rows:
+        oracle.paged_attention_decode(q[:nd], kp, vp, plan.block_tables[:nd], plan.seq_lens[:nd],
+                                      sh.scale, dt, rows=rows)
+    for b, i in pre:
+        c = int(plan.new_lens[b])
+        Li = int(plan.seq_lens[b]) - c + i + 1
+        t = int(plan.cu_new_lens[b]) + i
+        oracle.paged_attention_decode(q[t:t + 1], kp, vp, plan.block_tables[b:b + 1],
+                                      np.array([Li]), sh.scale, dt)
+    secs = time.perf_counter() - t0
+    nbytes = sum(int(plan.seq_lens[b]) * row * 2 + 2 * qrow for b in rows)
+    nbytes += sum((int(plan.seq_lens[b]) - int(plan.new_lens[b]) + i + 1) * row * 2 + 2 * qrow
+                  for b, i in pre)
+    return secs, nbytes, len(rows), len(pre)
+
+
+# --------------------------------------------------------------- arms
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from workloads import draw_plan, make_layer
+    plan = draw_plan(args.workload)
+    layer = make_layer(plan, 0)
+    n_dec, n_pre = 8, 4
+    for w in range(args.warmup):
+        oracle_sample(plan, layer, n_dec, n_pre, offset=w)
+    total_s, total_b = 0.0, 0
+    for k in range(args.steps):
+        s, b, nr, npq = oracle_sample(plan, layer, n_dec, n_pre, offset=(args.warmup + k) * n_dec)
+        total_s += s
+        total_b += b
+    gbs = total_b / total_s / 1e9
+    sample = (f"per step: {n_dec} decode sequences (rotating) and {n_pre} prefill queries of one "
+              f"layer of the {WORKLOAD_LABEL} step, float64 numpy oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(plan),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(plan):
+    sh = plan.shape
+    from workloads import TIMED_LAYERS
+    return {"workload": WORKLOAD_LABEL if plan.shape.name == WORKLOAD else plan.shape.name,
+            "layers_timed": TIMED_LAYERS[sh.name], "layers_model": sh.layers,
+            "decode_seqs": int(plan.n_decode), "prefill_seqs": int(plan.num_seqs - plan.n_decode),
+            "prefill_chunk_tokens": int(plan.new_lens[plan.n_decode:].max()) if plan.num_seqs > plan.n_decode else 0,
+            "n_heads": sh.n_heads, "n_kv": sh.n_kv, "head_dim": sh.head_dim,
+            "block_size": sh.block_size, "num_blocks": sh.num_blocks, "dtype": sh.dtype,
+            "sum_seq_len": int(plan.seq_lens.sum()),
+            "l2": "inputs larger than L2 (each step reads >1 GB of KV), no flush"}
+
+
+def run_gb300(args, rank, world, local):
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from paged_kv_cache_write_gb300 import build as _b
+    _b.build()
+    import paged_kv_cache_write_gb300 as pkv
+    from workloads import TIMED_LAYERS, draw_plan, make_layer
+
+    plan = draw_plan(args.workload)
+    sh = plan.shape
+    n_layers = TIMED_LAYERS[sh.name]
+    acc = step_accounting(plan)
+    layers_cpu = [make_layer(plan, l) for l in range(n_layers)]
+    L = [{n: t.to(dev) for n, t in lay.items()} for lay in layers_cpu]
+    if rank != 0 or args.no_cpu_baseline:
+        layers_cpu = layers_cpu[:1] if rank == 0 else []
+    nd = plan.n_decode
+    has_pre = plan.num_seqs > nd
+    bt = torch.from_numpy(plan.block_tables).to(dev)
+    seq_lens = torch.from_numpy(plan.seq_lens).to(dev)
+    cu_new = torch.from_numpy(plan.cu_new_lens).to(dev)
+    T = plan.num_new_tokens
+    max_dec = int(plan.seq_lens[:nd].max()) if nd else 0
+    if has_pre:
+        cu_q = torch.from_numpy((plan.cu_new_lens[nd:] - plan.cu_new_lens[nd]).astype(np.int32)).to(dev)
+        max_q = int(plan.new_lens[nd:].max())
+        max_pre = int(plan.seq_lens[nd:].max())
+    slots = torch.empty(T, dtype=torch.int64, device=dev)
+    ws = torch.empty(pkv.decode_workspace_bytes(nd, sh.n_heads, sh.head_dim, max_dec), dtype=torch.uint8,
+                     device=dev)
+    dec_out = [torch.empty((nd, sh.n_heads, sh.head_dim), dtype=sh.torch_dtype, device=dev) for _ in L]
+    pre_out = [torch.empty((T - nd, sh.n_heads, sh.head_dim), dtype=sh.torch_dtype, device=dev)
+               for _ in L] if has_pre else None
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev_dec, ev_pre = [], []
+
+    def step(timed=False, inputs=None):
+        src_bt, src_sl, src_cu = (bt, seq_lens, cu_new) if inputs is None else inputs[:3]
+        pkv.slot_mapping(src_bt, src_sl, src_cu, T, sh.block_size, sh.num_blocks, out=slots, err=err)
+        for li, lay in enumerate(L):
+            q, k, v = (lay["q"], lay["k"], lay["v"]) if inputs is None else inputs[3][li]
+            pkv.kv_write(k, v, slots, lay["k_pool"], lay["v_pool"], err=err)
+            if nd:
+                if timed:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                pkv.paged_attention_decode(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd],
+                                           src_sl[:nd], sh.scale, max_dec, out=dec_out[li],
+                                           workspace=ws, err=err)
+                if timed:
+                    e1.record(stream)
+                    ev_dec.append((e0, e1))
+            if has_pre:
+                if timed:
+                    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e2.record(stream)
+                pkv.paged_attention_prefill(q[nd:], cu_q, lay["k_pool"], lay["v_pool"], src_bt[nd:],
+                                            src_sl[nd:], sh.scale, max_q, max_pre, out=pre_out[li],
+                                            err=err)
+                if timed:
+                    e3.record(stream)
+                    ev_pre.append((e2, e3))
+
+    launches_per_step = 1 + n_layers * (1 + (3 if nd else 0) + (1 if has_pre else 0))
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
+
+    # ---- device-resident timing
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step(timed=True)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(stop)
+    ms_max = max_over_ranks(ms, world, dev)
+    ms_step = ms_max / args.steps
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_dec])) if ev_dec else None
+    pre_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_pre])) if ev_pre else None
+
+    per_layer = acc["decode_bytes"] + acc["prefill_bytes"] + acc["write_bytes"]
+    step_bytes = per_layer * n_layers
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end: step inputs from pinned host memory, outputs back
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (bt, seq_lens, cu_new)]
+        host_layers = [[lay[n].cpu().pin_memory() for n in ("q", "k", "v")] for lay in L]
+        dev_in = [torch.empty_like(t) for t in (bt, seq_lens, cu_new)]
+        dev_layers = [[torch.empty_like(lay[n]) for n in ("q", "k", "v")] for lay in L]
+        host_out = [o.cpu().pin_memory() for o in dec_out] + ([o.cpu().pin_memory() for o in pre_out]
+                                                              if has_pre else [])
+        h2d = sum(t.numel() * t.element_size() for t in host_in) + sum(
+            t.numel() * t.element_size() for lay in host_layers for t in lay)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        dev_outs = dec_out + (pre_out if has_pre else [])
+
+        def e2e_step():
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            for dl, hl in zip(dev_layers, host_layers):
+                for d, h in zip(dl, hl):
+                    d.copy_(h, non_blocking=True)
+            step(inputs=(dev_in[0], dev_in[1], dev_in[2], dev_layers))
+            for h, d in zip(host_out, dev_outs):
+                h.copy_(d, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e_steps = max(3, args.steps // 3)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev) / e_steps
+        e2e = {"value": world * step_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} in the timed region")
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tc = float(peaks["bf16_tflops"])
+    roof = None
+    if dec_ms:
+        ach = acc["decode_bytes"] / (dec_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "paged_attention_decode (plan + split + merge)",
+                "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_source": f"hbm_gbs of {src}", "traffic": None,
+                "algorithmic_bytes_per_launch": acc["decode_bytes"], "ms_per_launch": dec_ms}
+    pre_roof = None
+    if pre_ms:
+        tf = acc["prefill_flops"] / (pre_ms * 1e-3) / 1e12
+        pre_roof = {"bound": "tensor", "kernel": "paged_attention_prefill", "achieved": tf,
+                    "peak": tc, "unit": "TFLOP/s", "frac": tf / tc,
+                    "peak_source": f"bf16_tflops of {src}", "flops_per_launch": acc["prefill_flops"],
+                    "ms_per_launch": pre_ms}
+    cpu = None
+    if not args.no_cpu_baseline and layers_cpu:
+        secs, nbytes, nr, npq = oracle_sample(plan, layers_cpu[0], 48 if nd >= 48 else nd, 16)
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nr} decode sequences + {npq} prefill queries of layer 0 "
+                         f"({nbytes / 1e6:.0f} MB of KV), float64 numpy oracle, {secs:.1f} s"}
+    dec_tok_s = world * nd / (ms_step * 1e-3 * (sh.layers / n_layers)) if nd else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if sh.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; workloads/)", "config": workload_config(plan),
+        "decode_tokens_per_s": dec_tok_s,
+        "decode_tokens_per_s_note": f"{nd} decode tokens per step of {sh.layers} layers, "
+                                    f"{n_layers} timed layer(s) scaled by {sh.layers / n_layers:g}",
+        "percent_of_hbm_peak_step": 100.0 * value / world / hbm,
+        "roofline": roof, "prefill_roofline": pre_roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "bytes_per_step": step_bytes,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gb300(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

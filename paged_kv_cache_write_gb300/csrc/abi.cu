@@ -1,0 +1,219 @@
+// extern "C" entry points declared in include/pkv.h: host-side argument
+// checks, then the kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+#include "launch.h"
+
+namespace {
+
+using pkv::PoolShape;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status check_pool(const pkv_pool_desc* pool, PoolShape* out) {
+  if (pool == nullptr) return PKV_ERR_NULL;
+  if (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (pool->num_blocks <= 0 || pool->block_size <= 0 || pool->n_kv <= 0 || pool->head_dim <= 0)
+    return PKV_ERR_SHAPE;
+  *out = PoolShape{pool->num_blocks, pool->block_size, pool->n_kv, pool->head_dim, pool->dtype};
+  if (out->row_bytes() % 16 != 0) return PKV_ERR_ALIGN;
+  if ((int64_t)pool->num_blocks * pool->block_size > INT32_MAX) return PKV_ERR_RANGE;
+  return PKV_OK;
+}
+
+pkv_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  cudaGetLastError();  // clear a sticky launch-configuration error
+  return PKV_ERR_CUDA;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+pkv_status check_attention(const void* q, int32_t num_seqs, int32_t n_heads, const void* k_pool,
+                           const void* v_pool, const pkv_pool_desc* pool,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                           const void* out, PoolShape* shape) {
+  pkv_status st = check_pool(pool, shape);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || n_heads <= 0 || max_blocks_per_seq < 0 || max_seq_len < 0)
+    return PKV_ERR_SHAPE;
+  if (n_heads % shape->n_kv != 0) return PKV_ERR_SHAPE;
+  if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
+    return PKV_ERR_RANGE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return PKV_ERR_ALIGN;
+  if (max_blocks_per_seq == 0 && max_seq_len > 0) return PKV_ERR_SHAPE;
+  if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * shape->block_size) return PKV_ERR_SHAPE;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int32_t status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL: return "a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "invalid or inconsistent sizes";
+    case PKV_ERR_DTYPE: return "unknown dtype";
+    case PKV_ERR_ALIGN: return "pointer or row size not 16-byte aligned";
+    case PKV_ERR_RANGE: return "value out of range";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_UNSUPPORTED: return "unsupported head_dim / block_size / head grouping";
+    case PKV_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+int32_t pkv_abi_version(void) { return 1; }
+
+pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, const int32_t* cu_new_lens, int32_t num_seqs,
+                            int32_t num_tokens, int32_t block_size, int32_t num_blocks,
+                            int64_t* slot_mapping, int32_t* err_word, void* stream) {
+  if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0) return PKV_ERR_SHAPE;
+  if (block_size <= 0 || num_blocks <= 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (num_seqs == 0) return PKV_ERR_SHAPE;
+  if (!block_tables || !seq_lens || !cu_new_lens || !slot_mapping) return PKV_ERR_NULL;
+  if (max_blocks_per_seq == 0) return PKV_ERR_SHAPE;
+  return from_cuda(pkv::launch_slot_mapping(block_tables, max_blocks_per_seq, seq_lens,
+                                            cu_new_lens, num_seqs, num_tokens, block_size,
+                                            num_blocks, slot_mapping, err_word, as_stream(stream)));
+}
+
+pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
+                        int32_t num_tokens, void* k_pool, void* v_pool, const pkv_pool_desc* pool,
+                        int32_t* err_word, void* stream) {
+  PoolShape shape;
+  pkv_status st = check_pool(pool, &shape);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_pool || !v_pool) return PKV_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))
+    return PKV_ERR_ALIGN;
+  return from_cuda(pkv::launch_kv_write(k, v, slot_mapping, num_tokens, k_pool, v_pool, shape,
+                                        err_word, as_stream(stream)));
+}
+
+pkv_status pkv_kv_gather(const void* k_pool, const void* v_pool, const pkv_pool_desc* pool,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* seq_lens, const int32_t* cu_seq_lens, int32_t num_seqs,
+                         int32_t total_tokens, void* k_out, void* v_out, int32_t* err_word,
+                         void* stream) {
+  PoolShape shape;
+  pkv_status st = check_pool(pool, &shape);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || total_tokens < 0 || max_blocks_per_seq < 0) return PKV_ERR_SHAPE;
+  if (total_tokens == 0) return PKV_OK;
+  if (num_seqs == 0 || max_blocks_per_seq == 0) return PKV_ERR_SHAPE;
+  if (!k_pool || !v_pool || !block_tables || !seq_lens || !cu_seq_lens || !k_out || !v_out)
+    return PKV_ERR_NULL;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_out) || !aligned16(v_out))
+    return PKV_ERR_ALIGN;
+  return from_cuda(pkv::launch_kv_gather(k_pool, v_pool, shape, block_tables, max_blocks_per_seq,
+                                         seq_lens, cu_seq_lens, num_seqs, total_tokens, k_out,
+                                         v_out, err_word, as_stream(stream)));
+}
+
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim,
+                                  int32_t max_seq_len, int32_t max_ctas,
+                                  int32_t block_size) {
+  (void)block_size;
+  if (num_seqs < 0) num_seqs = 0;
+  if (n_heads < 1) n_heads = 1;
+  if (head_dim < 1) head_dim = 1;
+  return pkv::decode_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len, max_ctas);
+}
+
+pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n_heads,
+                                      const void* k_pool, const void* v_pool,
+                                      const pkv_pool_desc* pool, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                      int32_t max_seq_len, float scale, int32_t max_ctas,
+                                      void* out, void* workspace, size_t workspace_bytes,
+                                      int32_t* err_word, void* stream) {
+  PoolShape shape;
+  pkv_status st = check_attention(q, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
+                                  max_blocks_per_seq, seq_lens, max_seq_len, scale, out, &shape);
+  if (st != PKV_OK) return st;
+  if (max_ctas < 0) return PKV_ERR_RANGE;
+  if (!pkv::decode_supported(shape, n_heads)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!workspace) return PKV_ERR_WORKSPACE;
+  if (workspace_bytes < pkv::decode_workspace_bytes(num_seqs, n_heads, shape.head_dim,
+                                                    max_seq_len, max_ctas))
+    return PKV_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return PKV_ERR_ALIGN;
+  pkv::AttnArgs a{};
+  a.q = q;
+  a.out = out;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.cu_q_lens = nullptr;
+  a.num_seqs = num_seqs;
+  a.n_heads = n_heads;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_seq_len = max_seq_len;
+  a.max_q_len = 1;
+  a.total_q = num_seqs;
+  a.pool = shape;
+  a.scale = scale;
+  a.max_ctas = max_ctas;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err = err_word;
+  return from_cuda(pkv::launch_decode(a, as_stream(stream)));
+}
+
+size_t pkv_prefill_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
+
+pkv_status pkv_paged_attention_prefill(const void* q, const int32_t* cu_q_lens, int32_t num_seqs,
+                                       int32_t total_q, int32_t max_q_len, int32_t n_heads,
+                                       const void* k_pool, const void* v_pool,
+                                       const pkv_pool_desc* pool, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                       int32_t max_seq_len, float scale, void* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* err_word, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  PoolShape shape;
+  pkv_status st = check_attention(q, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
+                                  max_blocks_per_seq, seq_lens, max_seq_len, scale, out, &shape);
+  if (st != PKV_OK) return st;
+  if (total_q < 0 || max_q_len < 0) return PKV_ERR_SHAPE;
+  if (!pkv::prefill_supported(shape, n_heads)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;
+  if (!cu_q_lens) return PKV_ERR_NULL;
+  if (max_q_len == 0 || max_q_len > total_q || max_q_len > max_seq_len) return PKV_ERR_SHAPE;
+  pkv::AttnArgs a{};
+  a.q = q;
+  a.out = out;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.cu_q_lens = cu_q_lens;
+  a.num_seqs = num_seqs;
+  a.n_heads = n_heads;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_seq_len = max_seq_len;
+  a.max_q_len = max_q_len;
+  a.total_q = total_q;
+  a.pool = shape;
+  a.scale = scale;
+  a.err = err_word;
+  return from_cuda(pkv::launch_prefill(a, as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,1075 @@
+// Paged attention over the block pool: decode (one query per sequence,
+// split over the whole machine and merged by log-sum-exp weights) and
+// chunked prefill (a causal query chunk over paged history).
+//
+// What is computed ("Build a Mini vLLM" section 3, paged_attention, and
+// section 4, prefill / decode_step):  for a query row of head h the output
+// is softmax_j(scale * q . K_j) V_j over the keys j the row may see, with
+// K_j, V_j read from block table[j / 16], offset j % 16, of KV head
+// h / (n_heads / n_kv) ("nano-vLLM", How it works: query heads grouped onto
+// their shared K/V head).  Softmax is evaluated online (running maximum,
+// rescaled running sum) in fp32; scores are kept in log2 units
+// (scale * log2(e) folded into one multiply) so exp2 can be used.
+//
+// GB300 design.
+//  * Data movement: a producer warp copies each 16-token block's K and V
+//    rows for the CTA's KV heads into a shared-memory ring with bulk
+//    asynchronous copies (cp.async.bulk, the TMA engine), one copy per
+//    token row (HG heads x head_dim contiguous elements, up to 1 KB), with
+//    completion counted on an mbarrier per stage.  Rows past a sequence's
+//    length are zero-filled instead of copied, so pool slots past the
+//    length are never read.  Token rows are padded by 16 bytes in shared
+//    memory so the MMA fragment loads are bank-conflict free.
+//  * Math: bf16 pools use warp-level tensor-core MMA (m16n8k16, fp32
+//    accumulate) with the GQA group's query heads as the 16 MMA rows, so
+//    one K/V tile serves every head of the group (the group-8 shapes need
+//    8 multiply-adds per KV byte, more than the CUDA cores issue at HBM
+//    rate).  fp32 pools use a CUDA-core path with fp32 FMAs.
+//  * Decode work balance: a persistent grid sized to the SMs divides the
+//    total work - every (sequence, KV-head group, 16-token block) unit - into
+//    equal contiguous ranges, one per CTA (stream-K style).  A sequence
+//    whose blocks fall in one CTA's range is finished there; one that spans
+//    several CTAs leaves a partial (normalised output, max, exp-sum) per
+//    CTA, which a merge kernel combines.  Split points depend only on
+//    logical block positions and lengths, never on physical block ids, so
+//    results are bit-identical under any placement or sharing of blocks.
+//  * Every mbarrier wait is bounded; a wait that runs out sets
+//    PKV_DEVERR_TIMEOUT, and the producer drains its copies before exit.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <type_traits>
+
+#include "device.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kBS = 16;          // tokens per block handled by these kernels
+constexpr int kMaxRep = 16;      // query heads per KV head (MMA rows)
+constexpr int kBarrierBytes = 1024;
+constexpr int kMaxStages = 32;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------ rows
+
+// Per-warp softmax state over up to 16 query rows, tensor-core version
+// (bf16).  Thread `lane` owns rows g = lane/4 and g + 8 of every m16n8
+// accumulator tile and the columns 2*(lane%4) + {0,1} of it.
+template <int HD>
+struct MmaRows {
+  static_assert(HD % 16 == 0, "head_dim must be a multiple of 16");
+  uint32_t qa[HD / 16][4];
+  float o[HD / 8][4];
+  float m[2], l[2];
+  int last[2];
+
+  // q_row(r) -> pointer to row r's query (nullptr = inactive row),
+  // last_key(r) -> last key position the row may see.
+  template <typename QRow, typename LastKey>
+  __device__ __forceinline__ void begin(QRow q_row, LastKey last_key) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __nv_bfloat16* qp = q_row(g + 8 * h);
+      last[h] = qp ? last_key(g + 8 * h) : -1;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        uint32_t lo = 0, hi = 0;
+        if (qp) {
+          lo = *reinterpret_cast<const uint32_t*>(qp + kk * 16 + 2 * c);
+          hi = *reinterpret_cast<const uint32_t*>(qp + kk * 16 + 8 + 2 * c);
+        }
+        qa[kk][h] = lo;      // a0 (row g) / a1 (row g+8): k = 2c, 2c+1
+        qa[kk][2 + h] = hi;  // a2 (row g) / a3 (row g+8): k = 2c+8, 2c+9
+      }
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  }
+
+  // One 16-token block.  k_tile / v_tile point at token 0 of this warp's KV
+  // head; consecutive tokens are `stride` bytes apart.  j0 = position of
+  // token 0 of the block.
+  __device__ __forceinline__ void block(const uint8_t* k_tile, const uint8_t* v_tile, int stride,
+                                        int j0, float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int c = lane & 3;
+    const int mi = lane >> 3, ri = lane & 7;
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    // S = Q K^T: the four 8x8 matrices are (tokens 0-7 | 8-15) x (dims lo | hi).
+    const uint8_t* kaddr = k_tile + ((mi >> 1) * 8 + ri) * stride + (mi & 1) * 16;
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      uint32_t kb[4];
+      ldsm_x4(kb, kaddr + kk * 32);
+      mma_bf16_16816(s[0], qa[kk], kb[0], kb[1]);
+      mma_bf16_16816(s[1], qa[kk], kb[2], kb[3]);
+    }
+    // scale, causal / length mask, online softmax
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = e >> 1;
+        const int pos = j0 + nt * 8 + 2 * c + (e & 1);
+        const float x = s[nt][e] * scale_log2;
+        s[nt][e] = (pos <= last[h]) ? x : -INFINITY;
+        mx[h] = fmaxf(mx[h], s[nt][e]);
+      }
+    float alpha[2], mref[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+      const float mn = fmaxf(m[h], mx[h]);
+      mref[h] = (mn == -INFINITY) ? 0.f : mn;  // a row with nothing visible yet
+      alpha[h] = fast_exp2(m[h] - mref[h]);
+      m[h] = mn;
+    }
+    uint32_t pa[4];
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float p0 = fast_exp2(s[nt][2 * h] - mref[h]);
+        const float p1 = fast_exp2(s[nt][2 * h + 1] - mref[h]);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        const float2 pr = __bfloat1622float2(pb);
+        rs[h] += pr.x + pr.y;  // the sum uses the same rounded weights as P V
+        pa[nt * 2 + h] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) l[h] = l[h] * alpha[h] + rs[h];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[0];
+      o[i][2] *= alpha[1];
+      o[i][3] *= alpha[1];
+    }
+    // O += P V: matrices (tokens 0-7 | 8-15) x (dims lo | hi), transposed.
+    const uint8_t* vaddr = v_tile + ((mi & 1) * 8 + ri) * stride + (mi >> 1) * 16;
+#pragma unroll
+    for (int dp = 0; dp < HD / 16; ++dp) {
+      uint32_t vb[4];
+      ldsm_x4_trans(vb, vaddr + dp * 32);
+      mma_bf16_16816(o[2 * dp], pa, vb[0], vb[1]);
+      mma_bf16_16816(o[2 * dp + 1], pa, vb[2], vb[3]);
+    }
+  }
+
+  __device__ __forceinline__ void reduce_sums() {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+    }
+  }
+
+  // Final output of every active row: out_row(r) -> T* (nullptr = skip).
+  template <typename OutRow>
+  __device__ __forceinline__ void store(OutRow out_row) {
+    reduce_sums();
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      __nv_bfloat16* op = out_row(g + 8 * h);
+      if (!op) continue;
+      const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        *reinterpret_cast<__nv_bfloat162*>(op + i * 8 + 2 * c) =
+            __floats2bfloat162_rn(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+      }
+    }
+  }
+
+  // Partial result of every active row: normalised output (fp32), max
+  // (log2 units) and exp-sum.  part_row(r) -> float* (nullptr = skip),
+  // ml_row(r) -> float* of two floats.
+  template <typename PartRow, typename MlRow>
+  __device__ __forceinline__ void store_partial(PartRow part_row, MlRow ml_row) {
+    reduce_sums();
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float* pp = part_row(g + 8 * h);
+      if (!pp) continue;
+      const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i)
+        *reinterpret_cast<float2*>(pp + i * 8 + 2 * c) =
+            make_float2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+      if (c == 0) {
+        float* ml = ml_row(g + 8 * h);
+        ml[0] = m[h];
+        ml[1] = l[h];
+      }
+    }
+  }
+};
+
+// CUDA-core version (any element type).  Half-warp hw = lane/16 owns rows
+// hw, hw+2, ...; within a half-warp lane t = lane%16 owns token t of a
+// block for scores and head dims t, t+16, ... for the output.  The warp's
+// query rows (fp32) and block weights live in shared scratch.
+template <typename T, int HD, int MAXR>
+struct SimtRows {
+  static_assert(HD % 16 == 0, "head_dim must be a multiple of 16");
+  static constexpr int RPH = MAXR / 2;  // rows per half-warp
+  static constexpr int SCRATCH_FLOATS = MAXR * HD + MAXR * kBS;
+  float o[RPH][HD / 16];
+  float m[RPH], l[RPH];
+  int last[RPH];
+  float* qs;  // [MAXR][HD]
+  float* ps;  // [MAXR][16]
+
+  __device__ __forceinline__ void bind(float* scratch) {
+    qs = scratch;
+    ps = scratch + MAXR * HD;
+  }
+
+  template <typename QRow, typename LastKey>
+  __device__ __forceinline__ void begin(QRow q_row, LastKey last_key) {
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+    for (int i = lane; i < MAXR * HD; i += 32) {
+      const T* qp = q_row(i / HD);
+      qs[i] = qp ? Elem<T>::to_f(qp[i % HD]) : 0.f;
+    }
+    const int hw = lane >> 4;
+#pragma unroll
+    for (int k = 0; k < RPH; ++k) {
+      const int r = hw + 2 * k;
+      last[k] = q_row(r) ? last_key(r) : -1;
+      m[k] = -INFINITY;
+      l[k] = 0.f;
+#pragma unroll
+      for (int i = 0; i < HD / 16; ++i) o[k][i] = 0.f;
+    }
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ void block(const uint8_t* k_tile, const uint8_t* v_tile, int stride,
+                                        int j0, float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 15, hw = lane >> 4;
+    const unsigned half_mask = 0xffffffffu;
+    const T* krow = reinterpret_cast<const T*>(k_tile + t * stride);
+    const int pos = j0 + t;
+#pragma unroll
+    for (int k = 0; k < RPH; ++k) {
+      const int r = hw + 2 * k;
+      float s = 0.f;
+      const float* q = qs + r * HD;
+#pragma unroll 8
+      for (int d = 0; d < HD; ++d) s = fmaf(q[d], Elem<T>::to_f(krow[d]), s);
+      s = (pos <= last[k]) ? s * scale_log2 : -INFINITY;
+      float mx = s;
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(half_mask, mx, off));
+      const float mn = fmaxf(m[k], mx);
+      const float mref = (mn == -INFINITY) ? 0.f : mn;
+      const float alpha = fast_exp2(m[k] - mref);
+      m[k] = mn;
+      const float p = fast_exp2(s - mref);
+      float sum = p;
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) sum += __shfl_xor_sync(half_mask, sum, off);
+      l[k] = l[k] * alpha + sum;
+#pragma unroll
+      for (int i = 0; i < HD / 16; ++i) o[k][i] *= alpha;
+      ps[r * kBS + t] = p;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < RPH; ++k) {
+      const int r = hw + 2 * k;
+      const float* p = ps + r * kBS;
+#pragma unroll
+      for (int i = 0; i < HD / 16; ++i) {
+        const int d = t + 16 * i;
+        float acc = 0.f;
+#pragma unroll
+        for (int tt = 0; tt < kBS; ++tt)
+          acc = fmaf(p[tt], Elem<T>::to_f(reinterpret_cast<const T*>(v_tile + tt * stride)[d]), acc);
+        o[k][i] += acc;
+      }
+    }
+    __syncwarp();
+  }
+
+  template <typename OutRow>
+  __device__ __forceinline__ void store(OutRow out_row) {
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 15, hw = lane >> 4;
+#pragma unroll
+    for (int k = 0; k < RPH; ++k) {
+      T* op = out_row(hw + 2 * k);
+      if (!op) continue;
+      const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
+#pragma unroll
+      for (int i = 0; i < HD / 16; ++i) op[t + 16 * i] = Elem<T>::from_f(o[k][i] * inv);
+    }
+  }
+
+  template <typename PartRow, typename MlRow>
+  __device__ __forceinline__ void store_partial(PartRow part_row, MlRow ml_row) {
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 15, hw = lane >> 4;
+#pragma unroll
+    for (int k = 0; k < RPH; ++k) {
+      const int r = hw + 2 * k;
+      float* pp = part_row(r);
+      if (!pp) continue;
+      const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
+#pragma unroll
+      for (int i = 0; i < HD / 16; ++i) pp[t + 16 * i] = o[k][i] * inv;
+      if (t == 0) {
+        float* ml = ml_row(r);
+        ml[0] = m[k];
+        ml[1] = l[k];
+      }
+    }
+  }
+};
+
+template <typename T, int HD, int MAXR, bool MMA>
+struct RowsOf {
+  using type = SimtRows<T, HD, MAXR>;
+  static constexpr int kScratch = SimtRows<T, HD, MAXR>::SCRATCH_FLOATS;
+};
+template <int HD, int MAXR>
+struct RowsOf<__nv_bfloat16, HD, MAXR, true> {
+  using type = MmaRows<HD>;
+  static constexpr int kScratch = 0;
+};
+
+// ------------------------------------------------------------ pipeline
+
+struct Ring {
+  uint64_t* full;   // [nstages] producer -> consumers (1 arrival + bytes)
+  uint64_t* empty;  // [nstages] consumers -> producer (one arrival per consumer warp)
+  volatile int* abort_flag;
+  uint8_t* stages;
+  int nstages, stage_bytes, tile_bytes, row_stride, row_bytes;
+
+  __device__ __forceinline__ uint8_t* k_tile(int st) const { return stages + st * stage_bytes; }
+  __device__ __forceinline__ uint8_t* v_tile(int st) const {
+    return stages + st * stage_bytes + tile_bytes;
+  }
+};
+
+__device__ __forceinline__ Ring make_ring(uint8_t* smem, int nstages, int row_bytes) {
+  Ring r;
+  r.full = reinterpret_cast<uint64_t*>(smem);
+  r.empty = r.full + kMaxStages;
+  r.abort_flag = reinterpret_cast<volatile int*>(r.empty + kMaxStages);
+  r.stages = smem + kBarrierBytes;
+  r.nstages = nstages;
+  r.row_bytes = row_bytes;
+  r.row_stride = row_bytes + 16;
+  r.tile_bytes = kBS * r.row_stride;
+  r.stage_bytes = 2 * r.tile_bytes;
+  return r;
+}
+
+__device__ __forceinline__ void ring_init(const Ring& r, int consumer_warps) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < r.nstages; ++i) {
+      mbar_init(r.full + i, 1);
+      mbar_init(r.empty + i, consumer_warps);
+    }
+    *r.abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+}
+
+// Producer side, executed by all 32 lanes of the producer warp: fill the
+// next stage with rows [0, valid) of block `blk` (lane l < 16: K row l,
+// lane l >= 16: V row l-16), zero rows [valid, 16).  `k_src`/`v_src` point
+// at the first element of this CTA's heads in token row 0 of the block
+// (ignored when valid == 0).  Returns false if the wait timed out.
+__device__ __forceinline__ bool ring_fill(const Ring& r, uint32_t it, const uint8_t* k_src,
+                                          const uint8_t* v_src, int64_t src_row_pitch, int valid,
+                                          int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int st = static_cast<int>(it % r.nstages);
+  const uint32_t use = it / r.nstages;
+  if (use > 0 && !mbar_wait(r.empty + st, (use - 1) & 1)) {
+    if (lane == 0) report(err, PKV_DEVERR_TIMEOUT);
+    return false;
+  }
+  const int row = lane & 15;
+  const bool is_v = lane >= 16;
+  uint8_t* dst = (is_v ? r.v_tile(st) : r.k_tile(st)) + row * r.row_stride;
+  if (row >= valid) {
+    for (int off = 0; off < r.row_bytes; off += 16)
+      *reinterpret_cast<uint4*>(dst + off) = make_uint4(0, 0, 0, 0);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive_expect_tx(r.full + st, static_cast<uint32_t>(2 * valid * r.row_bytes));
+  if (row < valid) {
+    fence_proxy_async_smem();
+    const uint8_t* src = (is_v ? v_src : k_src) + row * src_row_pitch;
+    bulk_copy_g2s(dst, src, static_cast<uint32_t>(r.row_bytes), r.full + st);
+  }
+  return true;
+}
+
+// Producer after an abort: wait (bounded) for every stage it may still
+// have copies in flight to, so no copy lands after the CTA exits.
+__device__ __forceinline__ void ring_drain(const Ring& r, uint32_t issued) {
+  const uint32_t first = issued > static_cast<uint32_t>(r.nstages) ? issued - r.nstages : 0;
+  for (uint32_t it = first; it < issued; ++it)
+    mbar_wait(r.full + (it % r.nstages), (it / r.nstages) & 1);
+}
+
+__device__ __forceinline__ bool ring_wait_full(const Ring& r, uint32_t it, int32_t* err) {
+  const int st = static_cast<int>(it % r.nstages);
+  if (!mbar_wait(r.full + st, (it / r.nstages) & 1)) {
+    if ((threadIdx.x & 31) == 0) report(err, PKV_DEVERR_TIMEOUT);
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void ring_release(const Ring& r, uint32_t it) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(r.empty + (it % r.nstages));
+}
+
+// ------------------------------------------------------------- decode
+
+struct DecodeParams {
+  const void* q;
+  void* out;
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  int32_t* err;
+  int32_t* cu_units;  // [B+1] units (16-token blocks x head groups) before each sequence
+  float* ws_o;        // [2 * grid][HG * rep][HD]
+  float* ws_ml;       // [2 * grid][HG * rep][2]
+  int B, n_heads, n_kv, rep, hg_size, n_groups, W, num_blocks, max_len, head_dim;
+  int elem_bytes, nstages;
+  float scale_log2;
+};
+
+// Length used for sequence b: seq_lens[b] clamped to [0, max_len]
+// (max_len = min(max_seq_len, table width * 16)).
+__device__ __forceinline__ int used_len(const DecodeParams& p, int b) {
+  const int L = __ldg(p.seq_lens + b);
+  return L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+}
+
+// Largest b with cu[b] <= u (cu nondecreasing, u < cu[B]).
+__device__ __forceinline__ int seq_of_unit(const int32_t* cu, int B, int u) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu + mid) <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int range_begin(int64_t c, int64_t U, int64_t G) {
+  return static_cast<int>((c * U) / G);
+}
+
+// Exclusive scan of units per sequence; reports bad lengths once.
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p, int max_seq_len) {
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x;
+  const int chunk = (p.B + blockDim.x - 1) / blockDim.x;
+  const int b0 = tid * chunk;
+  const int b1 = min(p.B, b0 + chunk);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int L = __ldg(p.seq_lens + b);
+    if (L < 0 || L > max_seq_len) report(p.err, PKV_DEVERR_LENGTH);
+    else if (L > p.W * kBS) report(p.err, PKV_DEVERR_TABLE_WIDTH);
+    local += p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
+  }
+  // block-wide exclusive scan of `local`
+  const int lane = tid & 31, wid = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int t = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += y;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - local + (wid > 0 ? warp_tot[wid - 1] : 0);
+  for (int b = b0; b < b1; ++b) {
+    p.cu_units[b] = run;
+    run += p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
+  }
+  if (tid == blockDim.x - 1) p.cu_units[p.B] = run;
+}
+
+// A contiguous run of units of one (sequence, head group) inside this
+// CTA's range.
+struct Segment {
+  int b, grp, L, j_first, n_blocks;  // blocks j_first .. j_first+n_blocks-1
+  bool whole;                        // the run is the sequence's entire group
+  bool first_in_range;               // the run starts at this CTA's range start
+};
+
+__device__ __forceinline__ Segment segment_at(const DecodeParams& p, int u, int range_start,
+                                              int range_end) {
+  Segment s;
+  s.b = seq_of_unit(p.cu_units, p.B, u);
+  const int base = __ldg(p.cu_units + s.b);
+  s.L = used_len(p, s.b);
+  const int nblk = (s.L + kBS - 1) / kBS;
+  s.grp = (u - base) / nblk;
+  s.j_first = (u - base) - s.grp * nblk;
+  const int grp_end = base + (s.grp + 1) * nblk;
+  const int end = min(range_end, grp_end);
+  s.n_blocks = end - u;
+  s.whole = (s.j_first == 0) && (end == grp_end);
+  s.first_in_range = (u == range_start);
+  return s;
+}
+
+template <typename T, int HD, int MAXR, bool MMA>
+__global__ void __launch_bounds__(288) decode_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using Rows = typename RowsOf<T, HD, MAXR, MMA>::type;
+  const int consumers = p.hg_size;
+  const int row_bytes = p.hg_size * HD * p.elem_bytes;
+  Ring ring = make_ring(smem, p.nstages, row_bytes);
+  ring_init(ring, consumers);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int U = __ldg(p.cu_units + p.B);
+  const int G = gridDim.x;
+  const int r0 = range_begin(blockIdx.x, U, G);
+  const int r1 = range_begin(blockIdx.x + 1, U, G);
+  const int64_t token_pitch = int64_t(p.n_kv) * HD * p.elem_bytes;  // bytes per pool slot
+  const int rows_per_group = p.hg_size * p.rep;
+
+  if (warp == consumers) {
+    // ------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = r0; u < r1 && ok;) {
+      const Segment s = segment_at(p, u, r0, r1);
+      const int32_t* row = p.bt + int64_t(s.b) * p.W;
+      const int64_t head_off = int64_t(s.grp) * p.hg_size * HD * p.elem_bytes;
+      for (int jj = 0; jj < s.n_blocks && ok; jj += 32) {
+        const int j_lane = s.j_first + jj + lane;
+        int id = (jj + lane < s.n_blocks) ? __ldg(row + j_lane) : 0;
+        const int n_here = min(32, s.n_blocks - jj);
+        for (int k = 0; k < n_here; ++k) {
+          if (*ring.abort_flag) { ok = false; break; }
+          const int blk = __shfl_sync(0xffffffffu, id, k);
+          const int j = s.j_first + jj + k;
+          int valid = min(kBS, s.L - j * kBS);
+          if (blk < 0 || blk >= p.num_blocks) {
+            if (lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
+            valid = 0;
+          }
+          const int64_t off = int64_t(valid > 0 ? blk : 0) * kBS * token_pitch + head_off;
+          if (!ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err)) {
+            *ring.abort_flag = 1;
+            ok = false;
+            break;
+          }
+          ++it;
+        }
+      }
+      u += s.n_blocks;
+    }
+    if (!ok) ring_drain(ring, it);
+  } else if (warp < consumers) {
+    // ------------------------------------------------------ consumers
+    Rows rows;
+    if constexpr (!MMA) {
+      float* scratch = reinterpret_cast<float*>(ring.stages + p.nstages * ring.stage_bytes);
+      rows.bind(scratch + warp * RowsOf<T, HD, MAXR, MMA>::kScratch);
+    }
+    uint32_t it = 0;
+    bool ok = true;
+    const T* q = static_cast<const T*>(p.q);
+    for (int u = r0; u < r1 && ok;) {
+      const Segment s = segment_at(p, u, r0, r1);
+      const int kv_head = s.grp * p.hg_size + warp;
+      const int head0 = kv_head * p.rep;
+      const int last = s.L - 1;
+      rows.begin(
+          [&](int r) -> const T* {
+            return r < p.rep ? q + (int64_t(s.b) * p.n_heads + head0 + r) * HD : nullptr;
+          },
+          [&](int) { return last; });
+      for (int k = 0; k < s.n_blocks; ++k) {
+        if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
+          *ring.abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const int st = static_cast<int>(it % ring.nstages);
+        const int hoff = warp * HD * p.elem_bytes;
+        rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride,
+                   (s.j_first + k) * kBS, p.scale_log2);
+        ring_release(ring, it);
+        ++it;
+      }
+      if (!ok) break;
+      if (s.whole) {
+        T* out = static_cast<T*>(p.out);
+        rows.store([&](int r) -> T* {
+          return r < p.rep ? out + (int64_t(s.b) * p.n_heads + head0 + r) * HD : nullptr;
+        });
+      } else {
+        const int slot = 2 * blockIdx.x + (s.first_in_range ? 0 : 1);
+        const int64_t base_row = int64_t(slot) * rows_per_group + warp * p.rep;
+        rows.store_partial(
+            [&](int r) -> float* { return r < p.rep ? p.ws_o + (base_row + r) * HD : nullptr; },
+            [&](int r) -> float* { return p.ws_ml + (base_row + r) * 2; });
+      }
+      u += s.n_blocks;
+    }
+  }
+}
+
+// Owner CTA of unit u: the largest c with range_begin(c) <= u.
+__device__ __forceinline__ int owner_of(int u, int U, int G) {
+  int lo = 0, hi = G;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (range_begin(mid, U, G) <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Combine the partials of every (sequence, head group) that was split over
+// several CTAs; write zeros for empty sequences.  One warp per (sequence,
+// query head).
+template <typename T, int HD>
+__global__ void decode_merge_kernel(DecodeParams p, int G) {
+  const int warps_per_cta = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t total = int64_t(p.B) * p.n_heads;
+  const int U = __ldg(p.cu_units + p.B);
+  const int rows_per_group = p.hg_size * p.rep;
+  for (int64_t wi = int64_t(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5); wi < total;
+       wi += int64_t(gridDim.x) * warps_per_cta) {
+    const int b = static_cast<int>(wi / p.n_heads);
+    const int h = static_cast<int>(wi - int64_t(b) * p.n_heads);
+    T* out = static_cast<T*>(p.out) + wi * HD;
+    const int L = used_len(p, b);
+    if (L == 0) {
+      for (int d = lane; d < HD; d += 32) out[d] = Elem<T>::from_f(0.f);
+      continue;
+    }
+    const int nblk = (L + kBS - 1) / kBS;
+    const int kv_head = h / p.rep;
+    const int grp = kv_head / p.hg_size;
+    const int row_in_group = (kv_head - grp * p.hg_size) * p.rep + (h - kv_head * p.rep);
+    const int a = __ldg(p.cu_units + b) + grp * nblk;  // first unit of (b, grp)
+    const int e = a + nblk;                            // one past the last
+    const int c0 = owner_of(a, U, G);
+    const int c1 = owner_of(e - 1, U, G);
+    if (c0 == c1) continue;  // finished inside one CTA
+    // pass 1: common maximum
+    float M = -INFINITY;
+    for (int c = c0; c <= c1; ++c) {
+      if (range_begin(c + 1, U, G) == range_begin(c, U, G)) continue;  // empty range
+      const int slot = (c == c0 && range_begin(c, U, G) != a) ? 2 * c + 1 : 2 * c;
+      M = fmaxf(M, p.ws_ml[(int64_t(slot) * rows_per_group + row_in_group) * 2]);
+    }
+    float acc[(HD + 31) / 32];
+#pragma unroll
+    for (int i = 0; i < (HD + 31) / 32; ++i) acc[i] = 0.f;
+    float den = 0.f;
+    for (int c = c0; c <= c1; ++c) {
+      if (range_begin(c + 1, U, G) == range_begin(c, U, G)) continue;  // empty range
+      const int slot = (c == c0 && range_begin(c, U, G) != a) ? 2 * c + 1 : 2 * c;
+      const int64_t row = int64_t(slot) * rows_per_group + row_in_group;
+      const float w = fast_exp2(p.ws_ml[row * 2] - M) * p.ws_ml[row * 2 + 1];
+      den += w;
+      const float* po = p.ws_o + row * HD;
+#pragma unroll
+      for (int i = 0; i < (HD + 31) / 32; ++i) {
+        const int d = lane + 32 * i;
+        if (d < HD) acc[i] = fmaf(w, po[d], acc[i]);
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+    for (int i = 0; i < (HD + 31) / 32; ++i) {
+      const int d = lane + 32 * i;
+      if (d < HD) out[d] = Elem<T>::from_f(acc[i] * inv);
+    }
+  }
+}
+
+// ------------------------------------------------------------ prefill
+
+struct PrefillParams {
+  const void* q;
+  void* out;
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  const int32_t* cu_q;
+  int32_t* err;
+  int B, n_heads, n_kv, rep, W, num_blocks, max_len, queries_per_warp, consumer_warps, total_q;
+  int elem_bytes, nstages;
+  float scale_log2;
+};
+
+// CTA = (query tile, KV head, sequence).  Consumer warps each own
+// `queries_per_warp` consecutive queries x all `rep` heads of the group
+// (rows r -> query r / rep, head r % rep); the ring holds the KV head's
+// rows of each block up to the tile's last visible key.
+template <typename T, int HD, int MAXR, bool MMA>
+__global__ void __launch_bounds__(288) prefill_kernel(PrefillParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using Rows = typename RowsOf<T, HD, MAXR, MMA>::type;
+  const int b = blockIdx.z;
+  const int g = blockIdx.y;
+  const int q0 = __ldg(p.cu_q + b);
+  const int c = __ldg(p.cu_q + b + 1) - q0;
+  const int tile_q = p.consumer_warps * p.queries_per_warp;
+  const int i0 = blockIdx.x * tile_q;
+  if (i0 >= c) return;  // whole CTA idle: exit before touching barriers
+  if (q0 < 0 || q0 + c > p.total_q) {  // offsets disagree with the query count
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.err, PKV_DEVERR_LENGTH);
+    return;
+  }
+  int L = __ldg(p.seq_lens + b);
+  if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) {
+    if (L < c || L < 0) report(p.err, PKV_DEVERR_LENGTH);
+    else if (L > p.max_len) report(p.err, L > p.W * kBS ? PKV_DEVERR_TABLE_WIDTH : PKV_DEVERR_LENGTH);
+  }
+  if (L > p.max_len) L = p.max_len;
+  if (L < c) return;  // inconsistent chunk: reported above, nothing computed
+  const int i_end = min(c, i0 + tile_q);
+  const int last_needed = L - c + i_end - 1;  // last key any row of the tile sees
+  const int n_blocks = last_needed / kBS + 1;
+
+  const int row_bytes = HD * p.elem_bytes;
+  Ring ring = make_ring(smem, p.nstages, row_bytes);
+  ring_init(ring, p.consumer_warps);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t token_pitch = int64_t(p.n_kv) * HD * p.elem_bytes;
+
+  if (warp == p.consumer_warps) {
+    const int32_t* row = p.bt + int64_t(b) * p.W;
+    const int64_t head_off = int64_t(g) * HD * p.elem_bytes;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int jj = 0; jj < n_blocks && ok; jj += 32) {
+      int id = (jj + lane < n_blocks) ? __ldg(row + jj + lane) : 0;
+      const int n_here = min(32, n_blocks - jj);
+      for (int k = 0; k < n_here; ++k) {
+        if (*ring.abort_flag) { ok = false; break; }
+        const int blk = __shfl_sync(0xffffffffu, id, k);
+        const int j = jj + k;
+        int valid = min(kBS, L - j * kBS);
+        if (blk < 0 || blk >= p.num_blocks) {
+          if (lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
+          valid = 0;
+        }
+        const int64_t off = int64_t(valid > 0 ? blk : 0) * kBS * token_pitch + head_off;
+        if (!ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err)) {
+          *ring.abort_flag = 1;
+          ok = false;
+          break;
+        }
+        ++it;
+      }
+    }
+    if (!ok) ring_drain(ring, it);
+  } else if (warp < p.consumer_warps) {
+    Rows rows;
+    if constexpr (!MMA) {
+      float* scratch = reinterpret_cast<float*>(ring.stages + p.nstages * ring.stage_bytes);
+      rows.bind(scratch + warp * RowsOf<T, HD, MAXR, MMA>::kScratch);
+    }
+    const T* q = static_cast<const T*>(p.q);
+    const int qw = i0 + warp * p.queries_per_warp;  // first query of this warp
+    const int nrows = p.queries_per_warp * p.rep;
+    auto query_of = [&](int r) { return qw + r / p.rep; };
+    rows.begin(
+        [&](int r) -> const T* {
+          if (r >= nrows || query_of(r) >= c) return nullptr;
+          return q + (int64_t(q0 + query_of(r)) * p.n_heads + g * p.rep + r % p.rep) * HD;
+        },
+        [&](int r) { return L - c + query_of(r); });
+    // this warp's last visible key (its rows beyond it are masked anyway)
+    const int my_last = L - c + min(c, qw + p.queries_per_warp) - 1;
+    for (int k = 0; k < n_blocks; ++k) {
+      if (*ring.abort_flag || !ring_wait_full(ring, k, p.err)) {
+        *ring.abort_flag = 1;
+        return;
+      }
+      if (qw < c && k * kBS <= my_last) {
+        const int st = k % ring.nstages;
+        rows.block(ring.k_tile(st), ring.v_tile(st), ring.row_stride, k * kBS, p.scale_log2);
+      }
+      ring_release(ring, k);
+    }
+    T* out = static_cast<T*>(p.out);
+    rows.store([&](int r) -> T* {
+      if (r >= nrows || query_of(r) >= c) return nullptr;
+      return out + (int64_t(q0 + query_of(r)) * p.n_heads + g * p.rep + r % p.rep) * HD;
+    });
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+int sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  return sms;
+}
+
+bool use_mma(const PoolShape& pool) { return pool.dtype == PKV_BF16 && (pool.head_dim == 64 || pool.head_dim == 128); }
+
+// Heads per CTA for decode: the largest divisor of n_kv, at most 8, whose
+// rows (heads x head_dim elements) fit in 1 KB.
+int decode_group(const PoolShape& pool) {
+  const int per_head = pool.head_dim * pool.elem_bytes();
+  int best = 1;
+  for (int h = 1; h <= 8 && h <= pool.n_kv; ++h)
+    if (pool.n_kv % h == 0 && h * per_head <= 1024) best = h;
+  return best;
+}
+
+int stages_for(int stage_bytes, int scratch_bytes, int target_bytes) {
+  int ns = (target_bytes - kBarrierBytes - scratch_bytes) / stage_bytes;
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns < 2) ns = 2;
+  return ns;
+}
+
+template <typename T, int HD, int MAXR, bool MMA>
+struct DecodeLaunch {
+  static size_t scratch_bytes(int warps) {
+    return MMA ? 0 : size_t(warps) * RowsOf<T, HD, MAXR, MMA>::kScratch * sizeof(float);
+  }
+  static cudaError_t run(const AttnArgs& a, int hg, cudaStream_t stream) {
+    const PoolShape& pool = a.pool;
+    DecodeParams p{};
+    p.q = a.q;
+    p.out = a.out;
+    p.k_pool = static_cast<const uint8_t*>(a.k_pool);
+    p.v_pool = static_cast<const uint8_t*>(a.v_pool);
+    p.bt = a.block_tables;
+    p.seq_lens = a.seq_lens;
+    p.err = a.err;
+    p.B = a.num_seqs;
+    p.n_heads = a.n_heads;
+    p.n_kv = pool.n_kv;
+    p.rep = a.n_heads / pool.n_kv;
+    p.hg_size = hg;
+    p.n_groups = pool.n_kv / hg;
+    p.W = a.max_blocks_per_seq;
+    p.num_blocks = pool.num_blocks;
+    p.max_len = min(a.max_seq_len, a.max_blocks_per_seq * kBS);
+    p.head_dim = HD;
+    p.elem_bytes = pool.elem_bytes();
+    p.scale_log2 = a.scale * kLog2e;
+    const int row_bytes = hg * HD * p.elem_bytes;
+    const int stage_bytes = 2 * kBS * (row_bytes + 16);
+    const int threads = (hg + 1) * 32;
+    const size_t scratch = scratch_bytes(hg);
+    p.nstages = stages_for(stage_bytes, static_cast<int>(scratch), 110 * 1024);
+    const size_t smem = kBarrierBytes + size_t(p.nstages) * stage_bytes + scratch;
+    auto kern = decode_kernel<T, HD, MAXR, MMA>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int G = sm_count() * per_sm;
+    if (a.max_ctas > 0 && a.max_ctas < G) G = a.max_ctas;
+    // workspace: cu_units | ml | o
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    const int rows_per_group = hg * p.rep;
+    const size_t cu_bytes = (size_t(a.num_seqs + 1) * 4 + 255) / 256 * 256;
+    const size_t ml_bytes = (size_t(2) * G * rows_per_group * 2 * 4 + 255) / 256 * 256;
+    const size_t o_bytes = size_t(2) * G * rows_per_group * HD * 4;
+    if (cu_bytes + ml_bytes + o_bytes > a.workspace_bytes) return cudaErrorInvalidValue;
+    p.cu_units = reinterpret_cast<int32_t*>(ws);
+    p.ws_ml = reinterpret_cast<float*>(ws + cu_bytes);
+    p.ws_o = reinterpret_cast<float*>(ws + cu_bytes + ml_bytes);
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(p, a.max_seq_len);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kern<<<G, threads, smem, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t warps = int64_t(a.num_seqs) * a.n_heads;
+    int mgrid = static_cast<int>((warps + 7) / 8);
+    if (mgrid > sm_count() * 16) mgrid = sm_count() * 16;
+    if (mgrid < 1) mgrid = 1;
+    decode_merge_kernel<T, HD><<<mgrid, 256, 0, stream>>>(p, G);
+    return cudaGetLastError();
+  }
+};
+
+template <typename T, int HD, int MAXR, bool MMA>
+struct PrefillLaunch {
+  static cudaError_t run(const AttnArgs& a, cudaStream_t stream) {
+    const PoolShape& pool = a.pool;
+    PrefillParams p{};
+    p.q = a.q;
+    p.out = a.out;
+    p.k_pool = static_cast<const uint8_t*>(a.k_pool);
+    p.v_pool = static_cast<const uint8_t*>(a.v_pool);
+    p.bt = a.block_tables;
+    p.seq_lens = a.seq_lens;
+    p.cu_q = a.cu_q_lens;
+    p.err = a.err;
+    p.B = a.num_seqs;
+    p.n_heads = a.n_heads;
+    p.n_kv = pool.n_kv;
+    p.rep = a.n_heads / pool.n_kv;
+    p.W = a.max_blocks_per_seq;
+    p.num_blocks = pool.num_blocks;
+    p.max_len = min(a.max_seq_len, a.max_blocks_per_seq * kBS);
+    p.total_q = a.total_q;
+    p.elem_bytes = pool.elem_bytes();
+    p.scale_log2 = a.scale * kLog2e;
+    p.consumer_warps = 8;
+    p.queries_per_warp = MMA ? (kMaxRep / p.rep) : 1;
+    const int row_bytes = HD * p.elem_bytes;
+    const int stage_bytes = 2 * kBS * (row_bytes + 16);
+    const size_t scratch =
+        MMA ? 0 : size_t(p.consumer_warps) * RowsOf<T, HD, MAXR, MMA>::kScratch * sizeof(float);
+    p.nstages = stages_for(stage_bytes, static_cast<int>(scratch), 100 * 1024);
+    const size_t smem = kBarrierBytes + size_t(p.nstages) * stage_bytes + scratch;
+    auto kern = prefill_kernel<T, HD, MAXR, MMA>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int tile_q = p.consumer_warps * p.queries_per_warp;
+    const int tiles = (a.max_q_len + tile_q - 1) / tile_q;
+    if (tiles == 0 || a.num_seqs == 0) return cudaSuccess;
+    dim3 grid(tiles, pool.n_kv, a.num_seqs);
+    kern<<<grid, (p.consumer_warps + 1) * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+};
+
+template <template <typename, int, int, bool> class Launch, typename T, int HD>
+cudaError_t by_rep_simt(int rep, const AttnArgs& a, cudaStream_t s, int hg) {
+  if constexpr (std::is_same<Launch<T, HD, 4, false>, DecodeLaunch<T, HD, 4, false>>::value) {
+    if (rep <= 4) return DecodeLaunch<T, HD, 4, false>::run(a, hg, s);
+    return DecodeLaunch<T, HD, 16, false>::run(a, hg, s);
+  } else {
+    if (rep <= 4) return PrefillLaunch<T, HD, 4, false>::run(a, s);
+    return PrefillLaunch<T, HD, 16, false>::run(a, s);
+  }
+}
+
+bool simt_head_dim(int hd) { return hd == 16 || hd == 32 || hd == 64 || hd == 128; }
+
+}  // namespace
+
+bool decode_supported(const PoolShape& pool, int32_t n_heads) {
+  if (pool.block_size != kBS || pool.n_kv <= 0 || n_heads % pool.n_kv != 0) return false;
+  if (n_heads / pool.n_kv > kMaxRep) return false;
+  if (pool.dtype == PKV_BF16) return use_mma(pool) || simt_head_dim(pool.head_dim);
+  return pool.dtype == PKV_F32 && simt_head_dim(pool.head_dim);
+}
+
+bool prefill_supported(const PoolShape& pool, int32_t n_heads) { return decode_supported(pool, n_heads); }
+
+int32_t decode_default_partition(int32_t, int32_t, int32_t, int32_t) { return 0; }
+
+// Upper bound of the decode workspace: cu_units plus two partial slots per
+// CTA of the largest grid this device can run (every SM full of the
+// smallest CTA).
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim, int32_t, int32_t) {
+  const size_t G = size_t(sm_count()) * 16;
+  const size_t rows = size_t(n_heads);  // rows per group <= n_heads
+  const size_t cu = (size_t(num_seqs + 1) * 4 + 255) / 256 * 256;
+  const size_t ml = (2 * G * rows * 2 * 4 + 255) / 256 * 256;
+  const size_t o = 2 * G * rows * size_t(head_dim) * 4;
+  return cu + ml + o;
+}
+
+cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s) {
+  const PoolShape& pool = a.pool;
+  const int rep = a.n_heads / pool.n_kv;
+  const int hg = decode_group(pool);
+  if (use_mma(pool)) {
+    if (pool.head_dim == 64) return DecodeLaunch<__nv_bfloat16, 64, 16, true>::run(a, hg, s);
+    return DecodeLaunch<__nv_bfloat16, 128, 16, true>::run(a, hg, s);
+  }
+  if (pool.dtype == PKV_F32) {
+    switch (pool.head_dim) {
+      case 16: return by_rep_simt<DecodeLaunch, float, 16>(rep, a, s, hg);
+      case 32: return by_rep_simt<DecodeLaunch, float, 32>(rep, a, s, hg);
+      case 64: return by_rep_simt<DecodeLaunch, float, 64>(rep, a, s, hg);
+      default: return by_rep_simt<DecodeLaunch, float, 128>(rep, a, s, hg);
+    }
+  }
+  switch (pool.head_dim) {
+    case 16: return by_rep_simt<DecodeLaunch, __nv_bfloat16, 16>(rep, a, s, hg);
+    default: return by_rep_simt<DecodeLaunch, __nv_bfloat16, 32>(rep, a, s, hg);
+  }
+}
+
+cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t s) {
+  const PoolShape& pool = a.pool;
+  const int rep = a.n_heads / pool.n_kv;
+  if (use_mma(pool)) {
+    if (pool.head_dim == 64) return PrefillLaunch<__nv_bfloat16, 64, 16, true>::run(a, s);
+    return PrefillLaunch<__nv_bfloat16, 128, 16, true>::run(a, s);
+  }
+  if (pool.dtype == PKV_F32) {
+    switch (pool.head_dim) {
+      case 16: return by_rep_simt<PrefillLaunch, float, 16>(rep, a, s, 0);
+      case 32: return by_rep_simt<PrefillLaunch, float, 32>(rep, a, s, 0);
+      case 64: return by_rep_simt<PrefillLaunch, float, 64>(rep, a, s, 0);
+      default: return by_rep_simt<PrefillLaunch, float, 128>(rep, a, s, 0);
+    }
+  }
+  switch (pool.head_dim) {
+    case 16: return by_rep_simt<PrefillLaunch, __nv_bfloat16, 16>(rep, a, s, 0);
+    default: return by_rep_simt<PrefillLaunch, __nv_bfloat16, 32>(rep, a, s, 0);
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,62 @@
+// Internal launcher interface between the C ABI (abi.cu) and the kernels.
+// Arguments here are already validated by the ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct PoolShape {
+  int32_t num_blocks, block_size, n_kv, head_dim, dtype;
+  int32_t elem_bytes() const { return dtype == 0 ? 4 : 2; }
+  int64_t row_bytes() const { return int64_t(n_kv) * head_dim * elem_bytes(); }
+};
+
+cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens, const int32_t* cu_new_lens,
+                                int32_t num_seqs, int32_t num_tokens, int32_t block_size,
+                                int32_t num_blocks, int64_t* slot_mapping, int32_t* err,
+                                cudaStream_t stream);
+
+cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
+                            int32_t num_tokens, void* k_pool, void* v_pool, const PoolShape& pool,
+                            int32_t* err, cudaStream_t stream);
+
+cudaError_t launch_kv_gather(const void* k_pool, const void* v_pool, const PoolShape& pool,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, const int32_t* cu_seq_lens, int32_t num_seqs,
+                             int32_t total_tokens, void* k_out, void* v_out, int32_t* err,
+                             cudaStream_t stream);
+
+// Attention problem shared by decode and prefill.
+struct AttnArgs {
+  const void* q;
+  void* out;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* cu_q_lens;  // prefill only
+  int32_t num_seqs, n_heads, max_blocks_per_seq, max_seq_len, max_q_len, total_q;
+  PoolShape pool;
+  float scale;
+  int32_t max_ctas;  // decode: persistent grid cap (0 = one full wave)
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* err;
+};
+
+// Decode support / sizing.
+bool decode_supported(const PoolShape& pool, int32_t n_heads);
+int32_t decode_default_partition(int32_t num_seqs, int32_t n_kv, int32_t max_seq_len,
+                                 int32_t block_size);
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim,
+                              int32_t max_seq_len, int32_t partition_tokens);
+cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream);
+
+bool prefill_supported(const PoolShape& pool, int32_t n_heads);
+cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,127 @@
+"""The C-ABI library loads, exports every entry point that include/pkv.h
+declares, and rejects bad arguments on the host before any launch (these
+calls never touch a GPU, so they run on CPU-only machines)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_write_gb300 import build
+    build.build()
+    import paged_kv_cache_write_gb300 as m
+    return m
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for need in ("pkv_slot_mapping", "pkv_kv_write", "pkv_kv_gather", "pkv_paged_attention_decode",
+                 "pkv_paged_attention_prefill", "pkv_decode_workspace_bytes", "pkv_status_string"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(pkv):
+    lib = ctypes.CDLL(pkv.library_path)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(pkv):
+    assert pkv.status_string(0) == "ok"
+    for s in range(1, 9):
+        assert pkv.status_string(s) not in ("ok", "unknown status")
+    assert pkv.status_string(1234) == "unknown status"
+    assert pkv.abi_version() == 1
+
+
+def _desc(pkv, **kw):
+    d = dict(num_blocks=8, block_size=16, n_kv=2, head_dim=64, dtype=1)
+    d.update(kw)
+    return pkv.PoolDesc(**d)
+
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address; never dereferenced
+
+
+def test_kv_write_host_checks(pkv):
+    lib = pkv.lib
+    d = _desc(pkv)
+    by = ctypes.byref
+    assert lib.pkv_kv_write(FAKE, FAKE, FAKE, 4, FAKE, FAKE, None, None, None) == 1
+    assert lib.pkv_kv_write(FAKE, FAKE, FAKE, 4, FAKE, FAKE, by(_desc(pkv, dtype=7)), None, None) == 3
+    assert lib.pkv_kv_write(FAKE, FAKE, FAKE, -1, FAKE, FAKE, by(d), None, None) == 2
+    assert lib.pkv_kv_write(None, FAKE, FAKE, 4, FAKE, FAKE, by(d), None, None) == 1
+    assert lib.pkv_kv_write(FAKE + 4, FAKE, FAKE, 4, FAKE, FAKE, by(d), None, None) == 4
+    # row of 1 x 6 fp32 = 24 bytes is not a multiple of 16
+    assert lib.pkv_kv_write(FAKE, FAKE, FAKE, 4, FAKE, FAKE,
+                            by(_desc(pkv, n_kv=1, head_dim=6, dtype=0)), None, None) == 4
+    assert lib.pkv_kv_write(None, None, None, 0, None, None, by(d), None, None) == 0
+    assert lib.pkv_kv_write(FAKE, FAKE, FAKE, 4, FAKE, FAKE, by(_desc(pkv, num_blocks=0)),
+                            None, None) == 2
+
+
+def test_slot_mapping_host_checks(pkv):
+    lib = pkv.lib
+    assert lib.pkv_slot_mapping(FAKE, 4, FAKE, FAKE, -1, 3, 16, 8, FAKE, None, None) == 2
+    assert lib.pkv_slot_mapping(FAKE, 4, FAKE, FAKE, 2, 3, 0, 8, FAKE, None, None) == 2
+    assert lib.pkv_slot_mapping(None, 4, FAKE, FAKE, 2, 3, 16, 8, FAKE, None, None) == 1
+    assert lib.pkv_slot_mapping(FAKE, 0, FAKE, FAKE, 2, 3, 16, 8, FAKE, None, None) == 2
+    assert lib.pkv_slot_mapping(None, 0, None, None, 0, 0, 16, 8, None, None, None) == 0
+
+
+def _decode(pkv, **over):
+    a = dict(q=FAKE, B=2, H=8, k=FAKE, v=FAKE, desc=_desc(pkv), bt=FAKE, W=4, sl=FAKE, maxlen=64,
+             scale=0.125, max_ctas=0, out=FAKE, ws=FAKE, wsb=1 << 40, err=None)
+    a.update(over)
+    return pkv.lib.pkv_paged_attention_decode(a["q"], a["B"], a["H"], a["k"], a["v"],
+                                              ctypes.byref(a["desc"]), a["bt"], a["W"], a["sl"],
+                                              a["maxlen"], a["scale"], a["max_ctas"], a["out"],
+                                              a["ws"], a["wsb"], a["err"], None)
+
+
+def test_decode_host_checks(pkv):
+    assert _decode(pkv, q=None) == 1
+    assert _decode(pkv, H=7) == 2                      # n_heads % n_kv
+    assert _decode(pkv, maxlen=65) == 2                # > W * block_size
+    assert _decode(pkv, scale=float("nan")) == 5
+    assert _decode(pkv, max_ctas=-1) == 5
+    assert _decode(pkv, ws=None) == 6
+    assert _decode(pkv, wsb=16) == 6
+    assert _decode(pkv, out=FAKE + 8) == 4
+    assert _decode(pkv, desc=_desc(pkv, block_size=8), maxlen=32) == 7  # attention needs 16
+    assert _decode(pkv, desc=_desc(pkv, head_dim=48)) == 7
+    assert _decode(pkv, H=2 * 17) == 7                 # 17 query heads per KV head
+    assert _decode(pkv, B=0) == 0
+
+
+def test_prefill_host_checks(pkv):
+    lib = pkv.lib
+    d = _desc(pkv)
+    call = lambda **o: lib.pkv_paged_attention_prefill(
+        o.get("q", FAKE), o.get("cu", FAKE), o.get("B", 2), o.get("T", 10), o.get("mq", 5), 8, FAKE,
+        FAKE, ctypes.byref(o.get("desc", d)), FAKE, 4, FAKE, o.get("ml", 64), 0.125,
+        o.get("out", FAKE), None, 0, None, None)
+    assert call(cu=None) == 1
+    assert call(mq=11) == 2
+    assert call(mq=0) == 2
+    assert call(T=-1) == 2
+    assert call(desc=_desc(pkv, head_dim=40)) == 7
+    assert call(B=0) == 0
+    assert call(T=0) == 0
+
+
+def test_workspace_bytes_positive(pkv):
+    assert pkv.decode_workspace_bytes(4, 8, 16, 100) > 0
+    assert pkv.decode_workspace_bytes(0, 8, 16, 0) > 0

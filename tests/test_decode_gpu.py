@@ -1,0 +1,181 @@
+"""Paged decode attention on the GPU against the float64 oracle, through
+the C ABI: every workload shape, small ragged cases, split variants, and
+the pages' invariants (placement, prefix sharing, garbage in masked slots)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_step import GpuStep, OracleStep, assert_close, f64, raw
+from workloads import draw_plan, make_layer, tiny_plan, make_tiny_layer
+
+pytestmark = pytest.mark.gpu
+
+# (shape, layers checked).  All layers of the toy and SmolLM2 steps; three
+# layers of Llama-3.2-1B; first and last layer of LLaMA-7B; the one 70B layer.
+CASES = [("toy", [0]), ("smollm2-135m", list(range(30))), ("llama-3.2-1b", [0, 7, 15]),
+         ("llama-7b", [0, 31]), ("llama2-70b-mixed", [0])]
+
+
+def _sample_rows(plan, n=24):
+    nd = plan.n_decode
+    if nd <= n:
+        return list(range(nd))
+    lens = plan.seq_lens[:nd]
+    rng = np.random.default_rng(7)
+    pick = set(rng.choice(nd, n - 2, replace=False).tolist())
+    pick.add(int(np.argmax(lens)))
+    pick.add(int(np.argmin(lens)))
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("name,layers", CASES, ids=[c[0] for c in CASES])
+def test_decode_matches_oracle(name, layers):
+    plan = draw_plan(name)
+    for layer_id in layers:
+        layer = make_layer(plan, layer_id, fill=1e30)
+        g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+        o.run_write()
+        _, dec, _ = g.run()
+        rows = _sample_rows(plan) if name == "llama2-70b-mixed" else None
+        ref = o.decode(rows=rows)
+        rows = rows if rows is not None else list(range(plan.n_decode))
+        assert_close(f64(dec)[rows], ref[rows], plan.shape.dtype, f"{name} layer {layer_id}")
+        assert int(g.err.item()) == 0
+
+
+SMALL = [  # (n_heads, n_kv, head_dim, dtype)
+    (8, 4, 16, "f32"), (4, 4, 32, "f32"), (16, 2, 64, "f32"), (12, 4, 128, "f32"),
+    (9, 3, 64, "bf16"), (32, 8, 64, "bf16"), (64, 8, 128, "bf16"), (8, 8, 128, "bf16"),
+    (16, 1, 64, "bf16"), (6, 3, 16, "bf16"), (4, 2, 32, "bf16"),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[f"{h}x{k}x{d}-{t}" for h, k, d, t in SMALL])
+def test_decode_small_ragged(shape):
+    H, K, D, dt = shape
+    lens = [1, 2, 15, 16, 17, 31, 33, 64, 100, 257, 700]
+    plan = tiny_plan(lens, [1] * len(lens), n_heads=H, n_kv=K, head_dim=D, block_size=16,
+                     num_blocks=120, dtype=dt, seed=H * 100 + D)
+    layer = make_tiny_layer(plan, seed=D, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.run_write()
+    ref = o.decode()
+    for max_ctas in (0, 1, 3, 16):
+        _, dec, _ = g.run(max_ctas=max_ctas)
+        assert_close(f64(dec), ref, dt, f"max_ctas={max_ctas}")
+    assert int(g.err.item()) == 0
+
+
+def test_decode_empty_and_single_token():
+    plan = tiny_plan([0, 1, 1, 5], [0, 1, 1, 1], n_heads=8, n_kv=2, head_dim=64,
+                     block_size=16, num_blocks=8, dtype="bf16")
+    plan.n_decode = 4
+    layer = make_tiny_layer(plan, seed=3)
+    g = GpuStep(plan, layer)
+    g.write(g.slots())
+    dec = g.decode()
+    torch.cuda.synchronize()
+    out = dec.float().cpu()
+    assert torch.count_nonzero(out[0]) == 0  # no keys: zero output
+    # one key: the output is that key's value (softmax weight exactly 1)
+    kp = g.t["v_pool"].cpu()
+    for b in (1, 2):
+        blk = int(plan.block_tables[b, 0])
+        v0 = kp[blk, 0].float()  # [n_kv, hd]
+        for h in range(8):
+            assert torch.equal(out[b, h], v0[h // 4])
+
+
+def _relabel(plan, layer, seed):
+    """Move every block to a new physical id (data moved along)."""
+    nb = plan.shape.num_blocks
+    perm = np.random.default_rng(seed).permutation(nb)
+    kp = torch.empty_like(layer["k_pool"])
+    vp = torch.empty_like(layer["v_pool"])
+    kp[torch.from_numpy(perm)] = layer["k_pool"]
+    vp[torch.from_numpy(perm)] = layer["v_pool"]
+    return perm, kp, vp
+
+
+@pytest.mark.parametrize("name", ["toy", "smollm2-135m", "llama-3.2-1b"])
+@pytest.mark.parametrize("max_ctas", [0, 5])
+def test_decode_bit_identical_under_relabelling(name, max_ctas):
+    plan = draw_plan(name)
+    layer = make_layer(plan, 2)
+    g = GpuStep(plan, layer)
+    g.write(g.slots())
+    base = g.decode(max_ctas).clone()
+    perm, kp, vp = _relabel(plan, {"k_pool": g.t["k_pool"], "v_pool": g.t["v_pool"]}, 11)
+    bt2 = torch.from_numpy(perm[plan.block_tables].astype(np.int32)).cuda()
+    moved = g.decode(max_ctas, k_pool=kp, v_pool=vp, bt=bt2)
+    torch.cuda.synchronize()
+    assert torch.equal(base, moved)
+
+
+def test_decode_shared_prefix_equals_private_copies():
+    """SmolLM2 step: the 32-token system prompt in blocks 1 and 2 is shared
+    by all 30 tables ("nano-vLLM", How it works); giving every sequence
+    private copies of those blocks changes nothing, bit for bit."""
+    plan = draw_plan("smollm2-135m")
+    layer = make_layer(plan, 0)
+    g = GpuStep(plan, layer)
+    g.write(g.slots())
+    shared = g.decode().clone()
+    free = np.setdiff1d(np.arange(plan.shape.num_blocks), plan.held_blocks)
+    free = free[free != 0]
+    bt = plan.block_tables.copy()
+    kp, vp = g.t["k_pool"].clone(), g.t["v_pool"].clone()
+    cursor = 0
+    for b in range(plan.num_seqs):
+        for j in (0, 1):
+            new = int(free[cursor])
+            cursor += 1
+            kp[new] = kp[bt[b, j]]
+            vp[new] = vp[bt[b, j]]
+            bt[b, j] = new
+    private = g.decode(k_pool=kp, v_pool=vp, bt=torch.from_numpy(bt).cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(shared, private)
+
+
+@pytest.mark.parametrize("junk", [1e30, float("nan"), float("inf")])
+def test_decode_garbage_in_unused_slots(junk):
+    """Garbage in every slot no sequence uses (unheld blocks, the dummy block
+    0 that pads the tables, tails of last blocks) changes nothing ("nano-vLLM",
+    Correctness: the garbage pool proves the mask; NaN included here)."""
+    plan = draw_plan("smollm2-135m")
+    layer = make_layer(plan, 4)
+    g = GpuStep(plan, layer)
+    g.write(g.slots())
+    clean = g.decode().clone()
+    used = np.zeros(plan.shape.num_blocks * plan.shape.block_size, dtype=bool)
+    used[oracle.slot_mapping(plan.block_tables, plan.seq_lens, plan.seq_lens,
+                             plan.shape.block_size)] = True
+    mask = torch.from_numpy(~used).cuda()
+    kp = g.t["k_pool"].clone().reshape(used.shape[0], -1)
+    vp = g.t["v_pool"].clone().reshape(used.shape[0], -1)
+    kp[mask] = junk
+    vp[mask] = junk
+    dirty = g.decode(k_pool=kp.reshape(g.t["k_pool"].shape), v_pool=vp.reshape(g.t["v_pool"].shape))
+    torch.cuda.synchronize()
+    assert torch.equal(clean, dirty)
+
+
+def test_decode_reports_bad_lengths_and_ids():
+    import paged_kv_cache_write_gb300 as pkv
+    plan = tiny_plan([20, 40], [1, 1], n_heads=4, n_kv=2, head_dim=64, block_size=16,
+                     num_blocks=8, dtype="bf16")
+    layer = make_tiny_layer(plan)
+    g = GpuStep(plan, layer)
+    g.bt[0, 1] = -5
+    out = g.decode()
+    torch.cuda.synchronize()
+    assert g.err.item() & pkv.DEVERR["block_id"]
+    assert torch.isfinite(out.float()).all()
+    g.err.zero_()
+    g.seq_lens[1] = 999  # more than the table row holds and than max_seq_len
+    out = g.decode()
+    torch.cuda.synchronize()
+    assert g.err.item() & (pkv.DEVERR["length"] | pkv.DEVERR["table_width"])
+    assert torch.isfinite(out.float()).all()

@@ -1,0 +1,70 @@
+"""Chunked prefill attention on the GPU against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_step import GpuStep, OracleStep, assert_close, f64
+from workloads import draw_plan, make_layer, tiny_plan, make_tiny_layer
+
+pytestmark = pytest.mark.gpu
+
+
+def test_prefill_70b_mixed_step_sampled():
+    """LLaMA-2-70B mixed step: 4 chunks of 512 queries over 0..4096 tokens
+    of history; sampled queries (first, last, block edges, random) of every
+    chunk against the oracle one query at a time."""
+    plan = draw_plan("llama2-70b-mixed")
+    layer = make_layer(plan, 0, fill=1e30)
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.run_write()
+    _, _, pre = g.run()
+    got = f64(pre)
+    rng = np.random.default_rng(3)
+    nd = plan.n_decode
+    for b_rel in range(plan.num_seqs - nd):
+        c = int(plan.new_lens[nd + b_rel])
+        base = int(plan.cu_new_lens[nd + b_rel] - plan.cu_new_lens[nd])
+        qs = sorted({0, 1, 15, 16, 17, c - 1} | set(rng.choice(c, 6, replace=False).tolist()))
+        ref = np.stack([o.prefill_row(b_rel, i) for i in qs])
+        assert_close(got[[base + i for i in qs]], ref, "bf16", f"prefill seq {b_rel}")
+    assert int(g.err.item()) == 0
+
+
+SMALL = [(8, 4, 16, "f32"), (16, 2, 64, "f32"), (9, 3, 64, "bf16"), (32, 8, 64, "bf16"),
+         (64, 8, 128, "bf16"), (8, 8, 128, "bf16"), (16, 1, 64, "bf16"), (4, 2, 32, "bf16")]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[f"{h}x{k}x{d}-{t}" for h, k, d, t in SMALL])
+def test_prefill_small_ragged(shape):
+    H, K, D, dt = shape
+    hist = [0, 0, 3, 16, 37, 100]
+    chunk = [1, 40, 17, 16, 5, 33]
+    lens = [h + c for h, c in zip(hist, chunk)]
+    plan = tiny_plan(lens, chunk, n_heads=H, n_kv=K, head_dim=D, block_size=16, num_blocks=64,
+                     dtype=dt, seed=D + H)
+    layer = make_tiny_layer(plan, seed=H, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.run_write()
+    _, _, pre = g.run()
+    got = f64(pre)
+    for b in range(len(lens)):
+        ref = np.stack([o.prefill_row(b, i) for i in range(chunk[b])])
+        lo = int(plan.cu_new_lens[b])
+        assert_close(got[lo:lo + chunk[b]], ref, dt, f"seq {b}")
+    assert int(g.err.item()) == 0
+
+
+def test_prefill_chunk_of_one_equals_decode():
+    lens = [5, 33, 200]
+    for dt, (H, K, D) in (("bf16", (32, 8, 64)), ("f32", (8, 4, 16))):
+        plan = tiny_plan(lens, [1, 1, 1], n_heads=H, n_kv=K, head_dim=D, block_size=16,
+                         num_blocks=32, dtype=dt)
+        layer = make_tiny_layer(plan, seed=9)
+        g = GpuStep(plan, layer)
+        g.write(g.slots())
+        dec = g.decode(max_ctas=1)
+        cu = torch.arange(len(lens) + 1, dtype=torch.int32, device="cuda")
+        pre = g.pkv.paged_attention_prefill(g.t["q"], cu, g.t["k_pool"], g.t["v_pool"], g.bt,
+                                            g.seq_lens, plan.shape.scale, 1, max(lens))
+        torch.cuda.synchronize()
+        assert_close(f64(pre), f64(dec), dt, "prefill(c=1) vs decode")
