@@ -6,8 +6,8 @@ has the name of the C entry point without its ``pkv_`` prefix and only
 marshals arguments: it checks tensor devices, dtypes and layouts, passes
 raw device pointers and the current CUDA stream, and raises on a non-zero
 status.  Every step of the computation runs in the library's CUDA kernels;
-there is no CPU or PyTorch fallback, and importing this package on a
-machine without the built library raises.
+there is no CPU or PyTorch fallback: the library is loaded on first use
+and every call raises ImportError if it has not been built.
 
 PyTorch is used only for device memory and streams.
 """
@@ -39,50 +39,61 @@ class PoolDesc(ctypes.Structure):
                 ("dtype", ctypes.c_int32)]
 
 
-def _load():
-    if not os.path.exists(library_path):
-        raise ImportError(
-            f"{library_path} is missing: build it with "
-            "`python -m paged_kv_cache_write_gb300.build` (needs nvcc with sm_103a support)")
-    return ctypes.CDLL(library_path)
-
-
-lib = _load()
-
+_lib = None
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
 _sz = ctypes.c_size_t
 _f = ctypes.c_float
 _desc = ctypes.POINTER(PoolDesc)
 
-lib.pkv_status_string.restype = ctypes.c_char_p
-lib.pkv_status_string.argtypes = [_i32]
-lib.pkv_abi_version.restype = _i32
-lib.pkv_abi_version.argtypes = []
-lib.pkv_slot_mapping.restype = _i32
-lib.pkv_slot_mapping.argtypes = [_p, _i32, _p, _p, _i32, _i32, _i32, _i32, _p, _p, _p]
-lib.pkv_kv_write.restype = _i32
-lib.pkv_kv_write.argtypes = [_p, _p, _p, _i32, _p, _p, _desc, _p, _p]
-lib.pkv_kv_gather.restype = _i32
-lib.pkv_kv_gather.argtypes = [_p, _p, _desc, _p, _i32, _p, _p, _i32, _i32, _p, _p, _p, _p]
-lib.pkv_decode_workspace_bytes.restype = _sz
-lib.pkv_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
-lib.pkv_paged_attention_decode.restype = _i32
-lib.pkv_paged_attention_decode.argtypes = [_p, _i32, _i32, _p, _p, _desc, _p, _i32, _p, _i32, _f,
-                                           _i32, _p, _p, _sz, _p, _p]
-lib.pkv_prefill_workspace_bytes.restype = _sz
-lib.pkv_prefill_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
-lib.pkv_paged_attention_prefill.restype = _i32
-lib.pkv_paged_attention_prefill.argtypes = [_p, _p, _i32, _i32, _i32, _i32, _p, _p, _desc, _p,
-                                            _i32, _p, _i32, _f, _p, _p, _sz, _p, _p]
+
+def _load():
+    """Load libpkv.so once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise ImportError(
+            f"{library_path} is missing: build it with "
+            "`python -m paged_kv_cache_write_gb300.build` (needs nvcc with sm_103a support)")
+    L = ctypes.CDLL(library_path)
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_status_string.argtypes = [_i32]
+    L.pkv_abi_version.restype = _i32
+    L.pkv_abi_version.argtypes = []
+    L.pkv_slot_mapping.restype = _i32
+    L.pkv_slot_mapping.argtypes = [_p, _i32, _p, _p, _i32, _i32, _i32, _i32, _p, _p, _p]
+    L.pkv_kv_write.restype = _i32
+    L.pkv_kv_write.argtypes = [_p, _p, _p, _i32, _p, _p, _desc, _p, _p]
+    L.pkv_kv_gather.restype = _i32
+    L.pkv_kv_gather.argtypes = [_p, _p, _desc, _p, _i32, _p, _p, _i32, _i32, _p, _p, _p, _p]
+    L.pkv_decode_workspace_bytes.restype = _sz
+    L.pkv_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+    L.pkv_paged_attention_decode.restype = _i32
+    L.pkv_paged_attention_decode.argtypes = [_p, _i32, _i32, _p, _p, _desc, _p, _i32, _p, _i32,
+                                             _f, _i32, _p, _p, _sz, _p, _p]
+    L.pkv_prefill_workspace_bytes.restype = _sz
+    L.pkv_prefill_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
+    L.pkv_paged_attention_prefill.restype = _i32
+    L.pkv_paged_attention_prefill.argtypes = [_p, _p, _i32, _i32, _i32, _i32, _p, _p, _desc, _p,
+                                              _i32, _p, _i32, _f, _p, _p, _sz, _p, _p]
+    _lib = L
+    return L
+
+
+def __getattr__(name):
+    # `pkv.lib` loads the library on first access
+    if name == "lib":
+        return _load()
+    raise AttributeError(name)
 
 
 def status_string(status: int) -> str:
-    return lib.pkv_status_string(int(status)).decode()
+    return _load().pkv_status_string(int(status)).decode()
 
 
 def abi_version() -> int:
-    return int(lib.pkv_abi_version())
+    return int(_load().pkv_abi_version())
 
 
 class PkvError(RuntimeError):
@@ -141,7 +152,7 @@ def slot_mapping(block_tables, seq_lens, cu_new_lens, num_tokens: int, block_siz
     B, W = block_tables.shape
     if out is None:
         out = torch.empty(num_tokens, dtype=torch.int64, device=block_tables.device)
-    _check("pkv_slot_mapping", lib.pkv_slot_mapping(
+    _check("pkv_slot_mapping", _load().pkv_slot_mapping(
         _dev(block_tables, "block_tables", torch.int32), W, _dev(seq_lens, "seq_lens", torch.int32),
         _dev(cu_new_lens, "cu_new_lens", torch.int32), B, int(num_tokens), int(block_size),
         int(num_blocks), _dev(out, "out", torch.int64), _opt(err, "err", torch.int32),
@@ -159,7 +170,7 @@ def kv_write(k, v, slot_mapping, k_pool, v_pool, *, err=None, stream=None):
         raise ValueError("k, v must be [T, n_kv, head_dim] matching the pool")
     if slot_mapping.shape[0] != T:
         raise ValueError("slot_mapping must have one entry per token")
-    _check("pkv_kv_write", lib.pkv_kv_write(
+    _check("pkv_kv_write", _load().pkv_kv_write(
         _dev(k, "k", k_pool.dtype), _dev(v, "v", k_pool.dtype),
         _dev(slot_mapping, "slot_mapping", torch.int64), T, _dev(k_pool, "k_pool"),
         _dev(v_pool, "v_pool"), ctypes.byref(desc), _opt(err, "err", torch.int32),
@@ -176,7 +187,7 @@ def kv_gather(k_pool, v_pool, block_tables, seq_lens, cu_seq_lens, total_tokens:
         k_out = torch.empty(shape, dtype=k_pool.dtype, device=k_pool.device)
     if v_out is None:
         v_out = torch.empty(shape, dtype=k_pool.dtype, device=k_pool.device)
-    _check("pkv_kv_gather", lib.pkv_kv_gather(
+    _check("pkv_kv_gather", _load().pkv_kv_gather(
         _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), ctypes.byref(desc),
         _dev(block_tables, "block_tables", torch.int32), W, _dev(seq_lens, "seq_lens", torch.int32),
         _dev(cu_seq_lens, "cu_seq_lens", torch.int32), B, int(total_tokens),
@@ -186,7 +197,7 @@ def kv_gather(k_pool, v_pool, block_tables, seq_lens, cu_seq_lens, total_tokens:
 
 
 def decode_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len, max_ctas=0, block_size=16):
-    return int(lib.pkv_decode_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len, max_ctas,
+    return int(_load().pkv_decode_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len, max_ctas,
                                               block_size))
 
 
@@ -210,7 +221,7 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, seq_lens, scale: flo
     need = decode_workspace_bytes(B, H, hd, max_seq_len, max_ctas, desc.block_size)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    _check("pkv_paged_attention_decode", lib.pkv_paged_attention_decode(
+    _check("pkv_paged_attention_decode", _load().pkv_paged_attention_decode(
         _dev(q, "q", k_pool.dtype), B, H, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
         ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32), W,
         _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), float(scale), int(max_ctas),
@@ -221,7 +232,7 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, seq_lens, scale: flo
 
 
 def prefill_workspace_bytes(num_seqs, total_q, n_heads, head_dim, max_seq_len):
-    return int(lib.pkv_prefill_workspace_bytes(num_seqs, total_q, n_heads, head_dim, max_seq_len))
+    return int(_load().pkv_prefill_workspace_bytes(num_seqs, total_q, n_heads, head_dim, max_seq_len))
 
 
 def paged_attention_prefill(q, cu_q_lens, k_pool, v_pool, block_tables, seq_lens, scale: float,
@@ -239,7 +250,7 @@ def paged_attention_prefill(q, cu_q_lens, k_pool, v_pool, block_tables, seq_lens
         out = torch.empty_like(q)
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size())
-    _check("pkv_paged_attention_prefill", lib.pkv_paged_attention_prefill(
+    _check("pkv_paged_attention_prefill", _load().pkv_paged_attention_prefill(
         _dev(q, "q", k_pool.dtype), _dev(cu_q_lens, "cu_q_lens", torch.int32), B, T,
         int(max_q_len), H, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), ctypes.byref(desc),
         _dev(block_tables, "block_tables", torch.int32), W,
