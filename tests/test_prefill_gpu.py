@@ -38,10 +38,11 @@ SMALL = [(8, 4, 16, "f32"), (16, 2, 64, "f32"), (9, 3, 64, "bf16"), (32, 8, 64, 
 def test_prefill_small_ragged(shape):
     H, K, D, dt = shape
     hist = [0, 0, 3, 16, 37, 100]
-    chunk = [1, 40, 17, 16, 5, 33]
+    chunk = [40, 1, 17, 16, 5, 33]
     lens = [h + c for h, c in zip(hist, chunk)]
     plan = tiny_plan(lens, chunk, n_heads=H, n_kv=K, head_dim=D, block_size=16, num_blocks=64,
                      dtype=dt, seed=D + H)
+    plan.n_decode = 0  # every row is a prefill chunk (one of them a single query)
     layer = make_tiny_layer(plan, seed=H, fill=float("nan"))
     g, o = GpuStep(plan, layer), OracleStep(plan, layer)
     o.run_write()
