@@ -64,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers materialised per step (0 = the workload's own count)")
     return ap.parse_args(argv)
 
 
@@ -290,11 +292,11 @@ def run_reference(args, rank, world):
     return 0
 
 
-def workload_config(plan):
+def workload_config(plan, n_layers=None):
     sh = plan.shape
     from workloads import TIMED_LAYERS
     return {"workload": WORKLOAD_LABEL if plan.shape.name == WORKLOAD else plan.shape.name,
-            "layers_timed": TIMED_LAYERS[sh.name], "layers_model": sh.layers,
+            "layers_timed": n_layers or TIMED_LAYERS[sh.name], "layers_model": sh.layers,
             "decode_seqs": int(plan.n_decode), "prefill_seqs": int(plan.num_seqs - plan.n_decode),
             "prefill_chunk_tokens": int(plan.new_lens[plan.n_decode:].max()) if plan.num_seqs > plan.n_decode else 0,
             "n_heads": sh.n_heads, "n_kv": sh.n_kv, "head_dim": sh.head_dim,
@@ -317,7 +319,7 @@ def run_gb300(args, rank, world, local):
 
     plan = draw_plan(args.workload)
     sh = plan.shape
-    n_layers = TIMED_LAYERS[sh.name]
+    n_layers = args.layers if args.layers > 0 else TIMED_LAYERS[sh.name]
     acc = step_accounting(plan)
     layers_cpu = [make_layer(plan, l) for l in range(n_layers)]
     L = [{n: t.to(dev) for n, t in lay.items()} for lay in layers_cpu]
@@ -477,7 +479,7 @@ def run_gb300(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if sh.dtype == "bf16" else "f32",
-        "data": "synthetic (seeded; workloads/)", "config": workload_config(plan),
+        "data": "synthetic (seeded; workloads/)", "config": workload_config(plan, n_layers),
         "decode_tokens_per_s": dec_tok_s,
         "decode_tokens_per_s_note": f"{nd} decode tokens per step of {sh.layers} layers, "
                                     f"{n_layers} timed layer(s) scaled by {sh.layers / n_layers:g}",
