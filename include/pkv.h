@@ -249,6 +249,39 @@ pkv_status pkv_paged_attention_prefill(const void* q, const int32_t* cu_q_lens,
                                        void* workspace, size_t workspace_bytes,
                                        int32_t* err_word, void* stream);
 
+/*
+ * pkv_paged_attention_decode_noalloc - decode attention for callers that
+ * cannot allocate device memory.
+ *
+ * The pages have no counterpart of this entry point.  It computes exactly
+ * what pkv_paged_attention_decode computes, with the same arguments minus
+ * the workspace, for callers that may not call cudaMalloc or have no
+ * scratch to lend: a plug-in inside a framework that owns all device
+ * memory through its own arena (a raw cudaMalloc bypasses its accounting
+ * and synchronises the whole device), a per-token loop that cannot afford
+ * that synchronisation, or a plain C caller without an allocator.
+ *
+ * Its scratch is one array of PKV_NOALLOC_SCRATCH_BYTES compiled into the
+ * library; every GPU that loads the library holds it until the process
+ * exits.  The first call on each device looks up the array's device
+ * address (make that first call before any stream capture).  The call
+ * itself allocates nothing.  Nothing in the array must start at zero.
+ * Calls whose kernels overlap on the GPU (e.g. issued on two streams)
+ * race on the shared array: issue them on one stream.  A batch needing
+ * more scratch than the array holds returns PKV_ERR_WORKSPACE without
+ * launching (a smaller max_ctas shrinks the need).
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t num_seqs, int32_t n_heads,
+                                              const void* k_pool, const void* v_pool,
+                                              const pkv_pool_desc* pool,
+                                              const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq,
+                                              const int32_t* seq_lens, int32_t max_seq_len,
+                                              float scale, int32_t max_ctas, void* out,
+                                              int32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

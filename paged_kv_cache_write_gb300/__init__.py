@@ -22,7 +22,7 @@ __all__ = [
     "lib", "library_path", "PoolDesc", "PKV_F32", "PKV_BF16", "DEVERR",
     "slot_mapping", "kv_write", "kv_gather", "decode_workspace_bytes",
     "paged_attention_decode", "prefill_workspace_bytes", "paged_attention_prefill",
-    "status_string", "abi_version",
+    "status_string", "abi_version", "paged_attention_decode_noalloc",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -257,4 +257,31 @@ def paged_attention_prefill(q, cu_q_lens, k_pool, v_pool, block_tables, seq_lens
         _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), float(scale),
         _dev(out, "out", k_pool.dtype), ws_ptr, ws_bytes, _opt(err, "err", torch.int32),
         _stream(stream)))
+    return out
+
+
+def paged_attention_decode_noalloc(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
+                                   max_seq_len: int, *, out=None, max_ctas: int = 0, err=None,
+                                   stream=None):
+    """Decode attention using the library's built-in scratch instead of a
+    caller workspace (for callers that cannot allocate device memory).
+
+    Same result as :func:`paged_attention_decode`.  Calls overlapping on
+    the GPU share the built-in scratch and race; the first call on a
+    device should come before any stream capture.
+    """
+    L = _load()
+    fn = L.pkv_paged_attention_decode_noalloc
+    fn.restype = _i32
+    fn.argtypes = [_p, _i32, _i32, _p, _p, _desc, _p, _i32, _p, _i32, _f, _i32, _p, _p, _p]
+    desc = pool_desc(k_pool)
+    B, H, hd = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pkv_paged_attention_decode_noalloc", fn(
+        _dev(q, "q", k_pool.dtype), B, H, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+        ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len),
+        float(scale), int(max_ctas), _dev(out, "out", k_pool.dtype),
+        _opt(err, "err", torch.int32), _stream(stream)))
     return out

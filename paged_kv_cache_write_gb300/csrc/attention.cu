@@ -947,6 +947,34 @@ struct DecodeLaunch {
   }
 };
 
+// Exact workspace of the grid DecodeLaunch::run would launch for these
+// arguments (run() lays the workspace out the same way).
+template <typename T, int HD, int MAXR, bool MMA>
+size_t decode_exact_workspace(const AttnArgs& a, int hg) {
+  const int rep = a.n_heads / a.pool.n_kv;
+  const int row_bytes = hg * HD * a.pool.elem_bytes();
+  const int stage_bytes = 2 * kBS * (row_bytes + 16);
+  const int threads = (hg + 1) * 32;
+  const size_t scratch = DecodeLaunch<T, HD, MAXR, MMA>::scratch_bytes(hg);
+  const int nstages = stages_for(stage_bytes, static_cast<int>(scratch), 110 * 1024);
+  const size_t smem = kBarrierBytes + size_t(nstages) * stage_bytes + scratch;
+  auto kern = decode_kernel<T, HD, MAXR, MMA>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess)
+    return 0;
+  if (per_sm < 1) per_sm = 1;
+  int G = sm_count() * per_sm;
+  if (a.max_ctas > 0 && a.max_ctas < G) G = a.max_ctas;
+  const int rows_per_group = hg * rep;
+  const size_t cu_bytes = (size_t(a.num_seqs + 1) * 4 + 255) / 256 * 256;
+  const size_t ml_bytes = (size_t(2) * G * rows_per_group * 2 * 4 + 255) / 256 * 256;
+  const size_t o_bytes = size_t(2) * G * rows_per_group * HD * 4;
+  return cu_bytes + ml_bytes + o_bytes;
+}
+
 template <typename T, int HD, int MAXR, bool MMA>
 struct PrefillLaunch {
   static cudaError_t run(const AttnArgs& a, cudaStream_t stream) {
@@ -1049,6 +1077,34 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s) {
     case 16: return by_rep_simt<DecodeLaunch, __nv_bfloat16, 16>(rep, a, s, hg);
     default: return by_rep_simt<DecodeLaunch, __nv_bfloat16, 32>(rep, a, s, hg);
   }
+}
+
+size_t decode_workspace_bytes_exact(const AttnArgs& a) {
+  const PoolShape& pool = a.pool;
+  const int rep = a.n_heads / pool.n_kv;
+  const int hg = decode_group(pool);
+  if (use_mma(pool)) {
+    if (pool.head_dim == 64) return decode_exact_workspace<__nv_bfloat16, 64, 16, true>(a, hg);
+    return decode_exact_workspace<__nv_bfloat16, 128, 16, true>(a, hg);
+  }
+  const bool small = rep <= 4;
+  if (pool.dtype == PKV_F32) {
+    switch (pool.head_dim) {
+      case 16: return small ? decode_exact_workspace<float, 16, 4, false>(a, hg)
+                            : decode_exact_workspace<float, 16, 16, false>(a, hg);
+      case 32: return small ? decode_exact_workspace<float, 32, 4, false>(a, hg)
+                            : decode_exact_workspace<float, 32, 16, false>(a, hg);
+      case 64: return small ? decode_exact_workspace<float, 64, 4, false>(a, hg)
+                            : decode_exact_workspace<float, 64, 16, false>(a, hg);
+      default: return small ? decode_exact_workspace<float, 128, 4, false>(a, hg)
+                            : decode_exact_workspace<float, 128, 16, false>(a, hg);
+    }
+  }
+  if (pool.head_dim == 16)
+    return small ? decode_exact_workspace<__nv_bfloat16, 16, 4, false>(a, hg)
+                 : decode_exact_workspace<__nv_bfloat16, 16, 16, false>(a, hg);
+  return small ? decode_exact_workspace<__nv_bfloat16, 32, 4, false>(a, hg)
+               : decode_exact_workspace<__nv_bfloat16, 32, 16, false>(a, hg);
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t s) {

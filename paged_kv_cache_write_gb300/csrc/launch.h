@@ -55,6 +55,8 @@ int32_t decode_default_partition(int32_t num_seqs, int32_t n_kv, int32_t max_seq
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim,
                               int32_t max_seq_len, int32_t partition_tokens);
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream);
+// Workspace the decode launch for `a` needs on the current device (0 on error).
+size_t decode_workspace_bytes_exact(const AttnArgs& a);
 
 bool prefill_supported(const PoolShape& pool, int32_t n_heads);
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream);
