@@ -1110,6 +1110,7 @@ size_t decode_workspace_bytes_exact(const AttnArgs& a) {
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t s) {
   const PoolShape& pool = a.pool;
   const int rep = a.n_heads / pool.n_kv;
+  if (prefill_tc_supported(pool, a.n_heads)) return launch_prefill_tc(a, s);
   if (use_mma(pool)) {
     if (pool.head_dim == 64) return PrefillLaunch<__nv_bfloat16, 64, 16, true>::run(a, s);
     return PrefillLaunch<__nv_bfloat16, 128, 16, true>::run(a, s);

@@ -61,4 +61,8 @@ size_t decode_workspace_bytes_exact(const AttnArgs& a);
 bool prefill_supported(const PoolShape& pool, int32_t n_heads);
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream);
 
+// tcgen05 prefill (bf16, head_dim 64/128, 1/2/4/8/16 query heads per KV head).
+bool prefill_tc_supported(const PoolShape& pool, int32_t n_heads);
+cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t stream);
+
 }  // namespace pkv

@@ -1,0 +1,466 @@
+// Chunked-prefill attention on the 5th-generation tensor cores (tcgen05,
+// TMEM accumulators, TMA-staged operands) for bf16 pools.
+//
+// What is computed ("Build a Mini vLLM" section 4, prefill: causal
+// attention after the chunk's K/V is written): query i of a chunk of c
+// queries at the end of an L-token sequence attends keys 0 .. L - c + i of
+// its KV head, read in place through the block table.
+//
+// One CTA owns 128 MMA rows of one (sequence, KV head): 128 / rep
+// consecutive queries x the rep query heads that share the KV head, so one
+// K/V tile feeds every head of the GQA group.  Keys are processed in tiles
+// of 64 (four 16-token blocks).
+//
+//  warp 4    TMA producer: the Q tile once (two 64-column halves, 128-byte
+//            swizzle), then per key tile one 16-row box per block and half
+//            for K and for V into a two-stage ring.
+//  warp 5    allocates 256 TMEM columns (S tile 0, S tile 1, O) and one
+//            lane issues the MMAs:  S_j = Q K_j^T  (smem x smem -> TMEM),
+//            then after softmax  O += P_j V_j  (P read from TMEM, V
+//            MN-major from smem).  S_{j+1} is issued before waiting for P_j
+//            so the tensor core runs while softmax works.
+//  warps 0-3 softmax: thread r owns TMEM lane r (one query row): loads its
+//            64 scores, masks causally, keeps a running max in log2 units
+//            and only rescales O when the max grows by more than 2^8,
+//            writes P as bf16 over its S tile, and in the epilogue
+//            normalises O and stores the row.
+//
+// Value rows past the sequence end inside the last key tile are zeroed in
+// shared memory before P V reads them, so garbage in unused pool slots
+// cannot reach the output.  Every wait is bounded; on a timeout the kernel
+// flags PKV_DEVERR_TIMEOUT, drains its copies and MMAs, frees its TMEM and
+// returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "launch.h"
+#include "tcgen05.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kRows = 128;      // MMA rows per CTA
+constexpr int kTileKeys = 64;   // keys per S tile
+constexpr int kBlk = 16;        // tokens per pool block
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows past 2^8
+constexpr uint32_t kTmemCols = 256;  // S0 [0,64) S1 [64,128) O [128,128+HD)
+
+struct TcParams {
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  const int32_t* cu_q;
+  __nv_bfloat16* out;
+  int32_t* err;
+  int B, n_heads, n_kv, rep, W, num_blocks, max_len, total_q, q_per_tile;
+  float scale_log2;
+};
+
+template <int HD>
+struct Layout {
+  static constexpr int NH = HD / 64;                      // 128-byte column halves
+  static constexpr int Q_HALF = kRows * 128;              // 16 KB
+  static constexpr int KV_HALF = kTileKeys * 128;         // 8 KB
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = NH * Q_HALF;               // stage s: K at K_OFF + s*STAGE
+  static constexpr int STAGE = 2 * NH * KV_HALF;          // K then V
+  static constexpr int V_IN_STAGE = NH * KV_HALF;
+  static constexpr int BAR_OFF = K_OFF + 2 * STAGE;
+  static constexpr int BYTES = BAR_OFF + 256;
+  // launch request: 1 KB alignment slack, and at least 90 KB so at most two
+  // CTAs share an SM (two x 256 TMEM columns fill its 512)
+  static constexpr int REQUEST = (BYTES + 1024) > 90 * 1024 ? (BYTES + 1024) : 90 * 1024;
+};
+
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, TcParams p) {
+  using Lay = Layout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int b = blockIdx.z;
+  const int g = blockIdx.y;
+  const int q0 = __ldg(p.cu_q + b);
+  const int c = __ldg(p.cu_q + b + 1) - q0;
+  const int i0 = blockIdx.x * p.q_per_tile;
+  if (i0 >= c) return;  // idle CTA: leave before any barrier or TMEM use
+  if (q0 < 0 || q0 + c > p.total_q) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.err, PKV_DEVERR_LENGTH);
+    return;
+  }
+  int L = __ldg(p.seq_lens + b);
+  if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) {
+    if (L < c || L < 0) report(p.err, PKV_DEVERR_LENGTH);
+    else if (L > p.max_len)
+      report(p.err, L > p.W * kBlk ? PKV_DEVERR_TABLE_WIDTH : PKV_DEVERR_LENGTH);
+  }
+  if (L > p.max_len) L = p.max_len;
+  if (L < c) return;
+  const int i_end = min(c, i0 + p.q_per_tile);
+  const int n_tiles = (L - c + i_end - 1) / kTileKeys + 1;
+  const int n_blocks_seq = (L + kBlk - 1) / kBlk;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFF);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;    // [2]
+  uint64_t* v_full = bars + 3;    // [2]
+  uint64_t* kv_empty = bars + 5;  // [2]
+  uint64_t* s_full = bars + 7;    // [2]
+  uint64_t* p_ready = bars + 9;   // [2]
+  uint64_t* o_done = bars + 11;
+  uint64_t* drain = bars + 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(v_full + i, 1);
+      mbar_init(kv_empty + i, 1);
+      mbar_init(s_full + i, 1);
+      mbar_init(p_ready + i, kRows);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t o_tm = tmem + 128;
+  uint8_t* q_s = smem + Lay::Q_OFF;
+  auto k_st = [&](int st) { return smem + Lay::K_OFF + st * Lay::STAGE; };
+  auto v_st = [&](int st) { return smem + Lay::K_OFF + st * Lay::STAGE + Lay::V_IN_STAGE; };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, Lay::NH * Lay::Q_HALF);
+      for (int h = 0; h < Lay::NH; ++h)
+        tc::tma_load_3d(q_s + h * Lay::Q_HALF, &tq, h * 64, g * p.rep, q0 + i0, q_full);
+    }
+    const int32_t* row = p.bt + int64_t(b) * p.W;
+    int issued = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (*abort_flag) break;
+      const int st = j & 1;
+      const uint32_t use = j >> 1;
+      const int jb = j * 4 + lane;  // lanes 0-3: the tile's four blocks
+      int blk = 0;
+      bool load = lane < 4 && jb < n_blocks_seq;
+      if (load) {
+        blk = __ldg(row + jb);
+        if (blk < 0 || blk >= p.num_blocks) {
+          report(p.err, PKV_DEVERR_BLOCK_ID);
+          load = false;
+        }
+      }
+      const uint32_t nload = __popc(__ballot_sync(0xffffffffu, load));
+      if (use > 0 && !wait_all(kv_empty + st, (use - 1) & 1)) {
+        if (lane == 0) {
+          report(p.err, PKV_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      const uint32_t bytes = nload * Lay::NH * kBlk * 128;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(k_full + st, bytes);
+        mbar_arrive_expect_tx(v_full + st, bytes);
+      }
+      __syncwarp();
+      if (load) {
+        for (int h = 0; h < Lay::NH; ++h) {
+          const int off = h * Lay::KV_HALF + lane * kBlk * 128;
+          tc::tma_load_3d(k_st(st) + off, &tk, h * 64, g, blk * kBlk, k_full + st);
+          tc::tma_load_3d(v_st(st) + off, &tv, h * 64, g, blk * kBlk, v_full + st);
+        }
+      }
+      ++issued;
+    }
+    if (*abort_flag) {  // let copies in flight land before the CTA exits
+      for (int j = max(0, issued - 2); j < issued; ++j) {
+        mbar_wait(k_full + (j & 1), (j >> 1) & 1);
+        mbar_wait(v_full + (j & 1), (j >> 1) & 1);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, kTileKeys, false, false);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, HD, false, true);
+      const uint32_t q_addr = smem_addr(q_s);
+      bool ok = mbar_wait(q_full, 0);
+      auto issue_qk = [&](int j) {
+        const uint32_t k_addr = smem_addr(k_st(j & 1));
+        const uint32_t d = tmem + (j & 1) * kTileKeys;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off_q = (kk >> 2) * Lay::Q_HALF + (kk & 3) * 32;
+          const uint32_t off_k = (kk >> 2) * Lay::KV_HALF + (kk & 3) * 32;
+          tc::mma_ss(d, tc::sw128_desc(q_addr + off_q, 16, 1024),
+                     tc::sw128_desc(k_addr + off_k, 16, 1024), idesc_qk, kk > 0);
+        }
+        tc::commit(s_full + (j & 1));
+      };
+      if (ok && (ok = mbar_wait(k_full, 0))) {
+        tc::fence_after_sync();
+        issue_qk(0);
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        if (j + 1 < n_tiles) {
+          if (!(ok = mbar_wait(k_full + ((j + 1) & 1), ((j + 1) >> 1) & 1))) break;
+          tc::fence_after_sync();
+          issue_qk(j + 1);
+        }
+        if (!(ok = mbar_wait(p_ready + (j & 1), (j >> 1) & 1))) break;
+        if (!(ok = mbar_wait(v_full + (j & 1), (j >> 1) & 1))) break;
+        tc::fence_after_sync();
+        const uint32_t v_addr = smem_addr(v_st(j & 1));
+        const uint32_t p_tm = tmem + (j & 1) * kTileKeys;
+#pragma unroll
+        for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+          // 16 keys = two 8-row groups of the V tile; P: 16 bf16 = 8 columns
+          tc::mma_ts(o_tm, p_tm + kk * 8, tc::sw128_desc(v_addr + kk * 2048, Lay::KV_HALF, 1024),
+                     idesc_pv, j > 0 || kk > 0);
+        }
+        tc::commit(o_done);
+        tc::commit(kv_empty + (j & 1));
+      }
+      if (!ok) {
+        report(p.err, PKV_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // every MMA issued above has finished before TMEM is released
+      tc::commit(drain);
+      mbar_wait(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int r = threadIdx.x;  // TMEM lane = MMA row
+    const int qi = i0 + r / p.rep;
+    const int hh = r - (r / p.rep) * p.rep;
+    const bool active = qi < c;
+    const int last = active ? L - c + qi : -1;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m_used = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!(ok = wait_all(s_full + (j & 1), (j >> 1) & 1))) break;
+      tc::fence_after_sync();
+      const uint32_t s_tm = tmem + lane_base + (j & 1) * kTileKeys;
+      uint32_t sr[64];
+      tc::tmem_ld32(s_tm, *reinterpret_cast<uint32_t(*)[32]>(sr));
+      tc::tmem_ld32(s_tm + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      tc::tmem_wait_ld();
+      const int pos0 = j * kTileKeys;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kTileKeys; ++k) {
+        const float x = (pos0 + k <= last) ? __uint_as_float(sr[k]) * p.scale_log2 : -INFINITY;
+        sr[k] = __float_as_uint(x);
+        mx = fmaxf(mx, x);
+      }
+      const float m_new = fmaxf(m_used, mx);
+      const bool grow = m_new > m_used + kRescaleLog2;
+      const float alpha = grow ? fast_exp2(m_used - m_new) : 1.f;
+      if (grow) m_used = m_new;
+      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+      uint32_t pk[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int k = 0; k < kTileKeys / 2; ++k) {
+        const float p0 = fast_exp2(__uint_as_float(sr[2 * k]) - mref);
+        const float p1 = fast_exp2(__uint_as_float(sr[2 * k + 1]) - mref);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        const float2 pr = __bfloat1622float2(pb);
+        psum += pr.x + pr.y;  // the same rounded weights as P V uses
+        pk[k] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+      l_sum = l_sum * alpha + psum;
+      if (j > 0) {
+        // P V of the previous tile must be done before O is rescaled (and
+        // this keeps the o_done phases in step)
+        if (!(ok = wait_all(o_done, (j - 1) & 1))) break;
+        tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int ch = 0; ch < HD / 32; ++ch) {
+            uint32_t ov[32];
+            tc::tmem_ld32(o_tm + lane_base + ch * 32, ov);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+            tc::tmem_st32(o_tm + lane_base + ch * 32, ov);
+          }
+        }
+      }
+      tc::tmem_st32(s_tm, pk);
+      tc::tmem_wait_st();
+      if (pos0 + kTileKeys > L) {
+        // value rows at or past the sequence end: zero them (whole 128-byte
+        // rows, so the swizzle does not matter) before P V reads them
+        if (!(ok = wait_all(v_full + (j & 1), (j >> 1) & 1))) break;
+        const int first = L - pos0;  // >= 1
+        const int chunks = (kTileKeys - first) * Lay::NH * 8;
+        uint8_t* vt = v_st(j & 1);
+        for (int idx = r; idx < chunks; idx += kRows) {
+          const int rowi = first + idx / (Lay::NH * 8);
+          const int h = (idx / 8) % Lay::NH;
+          const int ch = idx % 8;
+          *reinterpret_cast<uint4*>(vt + h * Lay::KV_HALF + rowi * 128 + ch * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tc::fence_before_sync();
+      mbar_arrive(p_ready + (j & 1));
+    }
+    if (ok) ok = wait_all(o_done, (n_tiles - 1) & 1);
+    if (ok) {
+      tc::fence_after_sync();
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      __nv_bfloat16* orow = p.out + (int64_t(q0 + qi) * p.n_heads + g * p.rep + hh) * HD;
+#pragma unroll 1
+      for (int ch = 0; ch < HD / 32; ++ch) {
+        uint32_t ov[32];
+        tc::tmem_ld32(o_tm + lane_base + ch * 32, ov);
+        tc::tmem_wait_ld();
+        if (active) {
+          uint32_t pkd[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(ov[2 * k]) * inv,
+                                                            __uint_as_float(ov[2 * k + 1]) * inv);
+            pkd[k] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_uint4(pkd[4 * k], pkd[4 * k + 1], pkd[4 * k + 2], pkd[4 * k + 3]);
+        }
+      }
+    } else if (lane == 0) {
+      report(p.err, PKV_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+  // ------------------------------------------------------------ teardown
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor (dim0 contiguous) with a 128-byte-swizzled box.
+bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
+               uint32_t b2) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD>
+cudaError_t run_tc(const AttnArgs& a, cudaStream_t stream) {
+  using Lay = Layout<HD>;
+  const PoolShape& pool = a.pool;
+  const int rep = a.n_heads / pool.n_kv;
+  TcParams p{};
+  p.bt = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.cu_q = a.cu_q_lens;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.err = a.err;
+  p.B = a.num_seqs;
+  p.n_heads = a.n_heads;
+  p.n_kv = pool.n_kv;
+  p.rep = rep;
+  p.W = a.max_blocks_per_seq;
+  p.num_blocks = pool.num_blocks;
+  p.max_len = min(a.max_seq_len, a.max_blocks_per_seq * kBlk);
+  p.total_q = a.total_q;
+  p.q_per_tile = kRows / rep;
+  p.scale_log2 = a.scale * kLog2e;
+  CUtensorMap tq, tk, tv;
+  const uint64_t slots = uint64_t(pool.num_blocks) * pool.block_size;
+  if (!encode_3d(&tq, a.q, HD, a.n_heads, a.total_q, uint64_t(HD) * 2,
+                 uint64_t(a.n_heads) * HD * 2, 64, rep, kRows / rep) ||
+      !encode_3d(&tk, a.k_pool, HD, pool.n_kv, slots, uint64_t(HD) * 2,
+                 uint64_t(pool.n_kv) * HD * 2, 64, 1, kBlk) ||
+      !encode_3d(&tv, a.v_pool, HD, pool.n_kv, slots, uint64_t(HD) * 2,
+                 uint64_t(pool.n_kv) * HD * 2, 64, 1, kBlk))
+    return cudaErrorInvalidValue;
+  auto kern = prefill_tc_kernel<HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Lay::REQUEST);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.max_q_len + p.q_per_tile - 1) / p.q_per_tile;
+  dim3 grid(tiles, pool.n_kv, a.num_seqs);
+  kern<<<grid, kThreads, Lay::REQUEST, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PoolShape& pool, int32_t n_heads) {
+  if (pool.dtype != PKV_BF16 || pool.block_size != kBlk) return false;
+  if (pool.head_dim != 64 && pool.head_dim != 128) return false;
+  if (pool.n_kv <= 0 || n_heads % pool.n_kv != 0) return false;
+  const int rep = n_heads / pool.n_kv;
+  return rep == 1 || rep == 2 || rep == 4 || rep == 8 || rep == 16;
+}
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.max_q_len == 0) return cudaSuccess;
+  return a.pool.head_dim == 64 ? run_tc<64>(a, stream) : run_tc<128>(a, stream);
+}
+
+}  // namespace pkv
