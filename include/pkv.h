@@ -203,6 +203,7 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t hea
  * sequence unsplit.
  *
  *   q, out     [num_seqs, n_heads, head_dim] of pool->dtype
+ *   scale      positive and finite (else PKV_ERR_RANGE)
  *   workspace  device scratch of at least pkv_decode_workspace_bytes(...)
  *   Supported: head_dim 16, 32, 64, 128 (f32 and bf16; bf16 64 and 128
  *              run on tensor cores);

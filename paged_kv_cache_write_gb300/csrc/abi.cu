@@ -41,7 +41,7 @@ pkv_status check_attention(const void* q, int32_t num_seqs, int32_t n_heads, con
   if (num_seqs < 0 || n_heads <= 0 || max_blocks_per_seq < 0 || max_seq_len < 0)
     return PKV_ERR_SHAPE;
   if (n_heads % shape->n_kv != 0) return PKV_ERR_SHAPE;
-  if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
+  if (!(scale > 0.f) || scale == __builtin_inff())
     return PKV_ERR_RANGE;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PKV_ERR_NULL;

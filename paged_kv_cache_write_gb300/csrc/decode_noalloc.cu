@@ -86,7 +86,7 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
   if (num_seqs < 0 || n_heads <= 0 || max_blocks_per_seq < 0 || max_seq_len < 0)
     return PKV_ERR_SHAPE;
   if (n_heads % shape.n_kv != 0) return PKV_ERR_SHAPE;
-  if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
+  if (!(scale > 0.f) || scale == __builtin_inff())
     return PKV_ERR_RANGE;
   if (max_ctas < 0) return PKV_ERR_RANGE;
   if (!pkv::decode_supported(shape, n_heads)) return PKV_ERR_UNSUPPORTED;

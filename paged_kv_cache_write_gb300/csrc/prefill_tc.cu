@@ -164,15 +164,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int32_t* row = p.bt + int64_t(b) * p.W;
     int issued = 0;
+    int ids = 0;  // lane l holds the id of block (j / 8) * 32 + l
     for (int j = 0; j < n_tiles; ++j) {
       if (*abort_flag) break;
       const int st = j & 1;
       const uint32_t use = j >> 1;
+      if ((j & 7) == 0) {
+        const int jb32 = j * 4 + lane;
+        ids = jb32 < n_blocks_seq ? __ldg(row + jb32) : 0;
+      }
       const int jb = j * 4 + lane;  // lanes 0-3: the tile's four blocks
+      const int blk_l = __shfl_sync(0xffffffffu, ids, ((j & 7) * 4 + lane) & 31);
       int blk = 0;
       bool load = lane < 4 && jb < n_blocks_seq;
       if (load) {
-        blk = __ldg(row + jb);
+        blk = blk_l;
         if (blk < 0 || blk >= p.num_blocks) {
           report(p.err, PKV_DEVERR_BLOCK_ID);
           load = false;
@@ -278,29 +284,35 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc::tmem_ld32(s_tm + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tc::tmem_wait_ld();
       const int pos0 = j * kTileKeys;
+      if (pos0 + kTileKeys - 1 > last) {  // tile crosses this row's causal limit
+#pragma unroll
+        for (int k = 0; k < kTileKeys; ++k)
+          if (pos0 + k > last) sr[k] = __float_as_uint(-INFINITY);
+      }
+      // the max is taken on raw scores (scale > 0); scale and shift then
+      // fold into one packed FMA per pair of scores
       float mx = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < kTileKeys; ++k) {
-        const float x = (pos0 + k <= last) ? __uint_as_float(sr[k]) * p.scale_log2 : -INFINITY;
-        sr[k] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
-      }
-      const float m_new = fmaxf(m_used, mx);
+      for (int k = 0; k < kTileKeys; ++k) mx = fmaxf(mx, __uint_as_float(sr[k]));
+      const float m_new = fmaxf(m_used, mx * p.scale_log2);
       const bool grow = m_new > m_used + kRescaleLog2;
       const float alpha = grow ? fast_exp2(m_used - m_new) : 1.f;
       if (grow) m_used = m_new;
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 nm2 = make_float2(-mref, -mref);
       uint32_t pk[32];
-      float psum = 0.f;
+      float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < kTileKeys / 2; ++k) {
-        const float p0 = fast_exp2(__uint_as_float(sr[2 * k]) - mref);
-        const float p1 = fast_exp2(__uint_as_float(sr[2 * k + 1]) - mref);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        const float2 pr = __bfloat1622float2(pb);
-        psum += pr.x + pr.y;  // the same rounded weights as P V uses
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]),
+                                                __uint_as_float(sr[2 * k + 1])), sc2, nm2);
+        const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        acc = __fadd2_rn(acc, pe);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(pe.x, pe.y);
         pk[k] = *reinterpret_cast<const uint32_t*>(&pb);
       }
+      const float psum = acc.x + acc.y;
       l_sum = l_sum * alpha + psum;
       if (j > 0) {
         // P V of the previous tile must be done before O is rescaled (and
@@ -313,8 +325,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint32_t ov[32];
             tc::tmem_ld32(o_tm + lane_base + ch * 32, ov);
             tc::tmem_wait_ld();
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+            for (int k = 0; k < 16; ++k) {
+              const float2 o2 = __fmul2_rn(
+                  make_float2(__uint_as_float(ov[2 * k]), __uint_as_float(ov[2 * k + 1])), a2);
+              ov[2 * k] = __float_as_uint(o2.x);
+              ov[2 * k + 1] = __float_as_uint(o2.y);
+            }
             tc::tmem_st32(o_tm + lane_base + ch * 32, ov);
           }
         }

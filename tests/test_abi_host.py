@@ -96,6 +96,8 @@ def test_decode_host_checks(pkv):
     assert _decode(pkv, H=7) == 2                      # n_heads % n_kv
     assert _decode(pkv, maxlen=65) == 2                # > W * block_size
     assert _decode(pkv, scale=float("nan")) == 5
+    assert _decode(pkv, scale=-0.5) == 5                # the score scale must be positive
+    assert _decode(pkv, scale=0.0) == 5
     assert _decode(pkv, max_ctas=-1) == 5
     assert _decode(pkv, ws=None) == 6
     assert _decode(pkv, wsb=16) == 6

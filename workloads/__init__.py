@@ -72,13 +72,17 @@ SHAPES = {
     "llama-3.2-1b": Shape("llama-3.2-1b", "bf16", 16, 32, 8, 64, 16, 32768, True),
     "llama-7b": Shape("llama-7b", "bf16", 32, 32, 32, 128, 16, 2048, False),
     "llama2-70b-mixed": Shape("llama2-70b-mixed", "bf16", 80, 64, 8, 128, 16, 65536, True),
+    # the prefill half of the 70B mixed step alone, in a small pool (profiling)
+    "llama2-70b-prefill": Shape("llama2-70b-prefill", "bf16", 80, 64, 8, 128, 16, 2048, True),
 }
-CONFIG_IDS = {"toy": 1, "smollm2-135m": 2, "llama-3.2-1b": 3, "llama-7b": 4, "llama2-70b-mixed": 5}
+CONFIG_IDS = {"toy": 1, "smollm2-135m": 2, "llama-3.2-1b": 3, "llama-7b": 4, "llama2-70b-mixed": 5,
+              "llama2-70b-prefill": 6}
 
 # Layers materialised (each with its own pool) in one timed step.  The toy
 # step is one layer.  One 70B pool of 65,536 blocks is 4.3 GB, so that step
 # is timed on one layer and per-step token rates are scaled by its 80 layers.
-TIMED_LAYERS = {"toy": 1, "smollm2-135m": 30, "llama-3.2-1b": 16, "llama-7b": 32, "llama2-70b-mixed": 1}
+TIMED_LAYERS = {"toy": 1, "smollm2-135m": 30, "llama-3.2-1b": 16, "llama-7b": 32, "llama2-70b-mixed": 1,
+                "llama2-70b-prefill": 1}
 
 
 @dataclass
@@ -144,6 +148,9 @@ def draw_plan(name: str, *, num_seqs: int | None = None) -> Plan:
         hist = np.array([0, 1365, 2731, 4096], dtype=np.int64)
         lens = np.concatenate([dec, hist + 512])
         n_decode = b
+    elif name == "llama2-70b-prefill":
+        lens = np.array([0, 1365, 2731, 4096], dtype=np.int64) + 512
+        n_decode = 0
     else:
         raise KeyError(name)
 
