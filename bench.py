@@ -64,6 +64,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every kernel from the host each step instead of replaying "
+                         "the step as a CUDA graph")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers materialised per step (0 = the workload's own count)")
     return ap.parse_args(argv)
@@ -283,7 +286,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(plan),
+        "data": "synthetic", "config": workload_config(plan, None, "cpu oracle"),
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -292,7 +295,7 @@ def run_reference(args, rank, world):
     return 0
 
 
-def workload_config(plan, n_layers=None):
+def workload_config(plan, n_layers=None, launch="cuda_graph"):
     sh = plan.shape
     from workloads import TIMED_LAYERS
     return {"workload": WORKLOAD_LABEL if plan.shape.name == WORKLOAD else plan.shape.name,
@@ -302,7 +305,8 @@ def workload_config(plan, n_layers=None):
             "n_heads": sh.n_heads, "n_kv": sh.n_kv, "head_dim": sh.head_dim,
             "block_size": sh.block_size, "num_blocks": sh.num_blocks, "dtype": sh.dtype,
             "sum_seq_len": int(plan.seq_lens.sum()),
-            "l2": "inputs larger than L2 (each step reads >1 GB of KV), no flush"}
+            "l2": "inputs larger than L2 (each step reads >100 MB of KV), no flush",
+            "launch": launch}
 
 
 def run_gb300(args, rank, world, local):
@@ -376,11 +380,51 @@ def run_gb300(args, rank, world, local):
 
     launches_per_step = 1 + n_layers * (1 + (3 if nd else 0) + (1 if has_pre else 0))
 
+    def decode_all():
+        for li, lay in enumerate(L):
+            pkv.paged_attention_decode(lay["q"][:nd], lay["k_pool"], lay["v_pool"], bt[:nd],
+                                       seq_lens[:nd], sh.scale, max_dec, out=dec_out[li],
+                                       workspace=ws, err=err)
+
+    def prefill_all():
+        for li, lay in enumerate(L):
+            pkv.paged_attention_prefill(lay["q"][nd:], cu_q, lay["k_pool"], lay["v_pool"], bt[nd:],
+                                        seq_lens[nd:], sh.scale, max_q, max_pre, out=pre_out[li],
+                                        err=err)
+
+    def capture(fn):
+        """Warm fn up on a side stream, then record it as a CUDA graph."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    def time_graph(g, reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
+    use_graph = not args.no_graph
+    if use_graph:
+        g_step = capture(step)
+        for _ in range(max(args.warmup, 3)):
+            g_step.replay()
+        torch.cuda.synchronize()
 
     # ---- device-resident timing
     barrier(world)
@@ -389,15 +433,25 @@ def run_gb300(args, rank, world, local):
     with ClockSampler(local) as clk:
         start.record(stream)
         for _ in range(args.steps):
-            step(timed=True)
+            if use_graph:
+                g_step.replay()
+            else:
+                step(timed=True)
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     ms = start.elapsed_time(stop)
     ms_max = max_over_ranks(ms, world, dev)
     ms_step = ms_max / args.steps
-    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_dec])) if ev_dec else None
-    pre_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_pre])) if ev_pre else None
+    if use_graph:
+        # per-call durations of the dominant kernels: graphs of one layer-loop
+        # of decode calls and of prefill calls, replayed right after the step
+        reps = max(10, args.steps // 2)
+        dec_ms = time_graph(capture(decode_all), reps) / n_layers if nd else None
+        pre_ms = time_graph(capture(prefill_all), reps) / n_layers if has_pre else None
+    else:
+        dec_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_dec])) if ev_dec else None
+        pre_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_pre])) if ev_pre else None
 
     per_layer = acc["decode_bytes"] + acc["prefill_bytes"] + acc["write_bytes"]
     step_bytes = per_layer * n_layers
@@ -430,12 +484,13 @@ def run_gb300(args, rank, world, local):
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
+        run_e2e = capture(e2e_step).replay if use_graph else e2e_step
         barrier(world)
         e_steps = max(3, args.steps // 3)
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
         for _ in range(e_steps):
-            e2e_step()
+            run_e2e()
         s1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev) / e_steps
@@ -458,6 +513,9 @@ def run_gb300(args, rank, world, local):
     if dec_ms:
         ach = acc["decode_bytes"] / (dec_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": "paged_attention_decode (plan + split + merge)",
+                "timing": ("CUDA events around graph replays of one layer loop of decode calls, "
+                           "after the step's timed region" if use_graph else
+                           "CUDA events around every decode call inside the timed region"),
                 "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                 "peak_source": f"hbm_gbs of {src}", "traffic": None,
                 "algorithmic_bytes_per_launch": acc["decode_bytes"], "ms_per_launch": dec_ms}
@@ -479,7 +537,7 @@ def run_gb300(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if sh.dtype == "bf16" else "f32",
-        "data": "synthetic (seeded; workloads/)", "config": workload_config(plan, n_layers),
+        "data": "synthetic (seeded; workloads/)", "config": workload_config(plan, n_layers, "cuda_graph" if use_graph else "eager"),
         "decode_tokens_per_s": dec_tok_s,
         "decode_tokens_per_s_note": f"{nd} decode tokens per step of {sh.layers} layers, "
                                     f"{n_layers} timed layer(s) scaled by {sh.layers / n_layers:g}",

@@ -41,6 +41,7 @@
 #include <type_traits>
 
 #include "device.cuh"
+#include "host_cache.h"
 #include "launch.h"
 
 namespace pkv {
@@ -463,10 +464,14 @@ struct DecodeParams {
   const int32_t* seq_lens;
   int32_t* err;
   int32_t* cu_units;  // [B+1] units (16-token blocks x head groups) before each sequence
-  float* ws_o;        // [2 * grid][HG * rep][HD]
-  float* ws_ml;       // [2 * grid][HG * rep][2]
-  int B, n_heads, n_kv, rep, hg_size, n_groups, W, num_blocks, max_len, head_dim;
-  int elem_bytes, nstages;
+  int4* starts;       // [grid] each CTA's first segment: (sequence, head group, block, -)
+  int32_t* bounds;    // [grid + 1] first unit of each CTA's range (bounds[grid] = total)
+  int4* splits;       // [grid] split groups: (sequence, head group, first CTA, last CTA)
+  int32_t* n_splits;  // number of entries in splits
+  float* ws_o;        // [2 * grid][HG * rep][HD] partial outputs
+  float* ws_ml;       // [2 * grid][HG * rep][2] partial max (log2 units) and exp-sum
+  int B, n_heads, n_kv, rep, hg_size, n_groups, W, num_blocks, max_len, max_seq_len, head_dim;
+  int elem_bytes, nstages, grid;
   float scale_log2;
 };
 
@@ -482,18 +487,47 @@ __device__ __forceinline__ int seq_of_unit(const int32_t* cu, int B, int u) {
   int lo = 0, hi = B;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(cu + mid) <= u) lo = mid; else hi = mid;
+    if (cu[mid] <= u) lo = mid; else hi = mid;
   }
   return lo;
 }
 
+// First unit of CTA c's range when U units are split evenly over G CTAs.
 __device__ __forceinline__ int range_begin(int64_t c, int64_t U, int64_t G) {
   return static_cast<int>((c * U) / G);
 }
 
-// Exclusive scan of units per sequence; reports bad lengths once.
-__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p, int max_seq_len) {
+// Owner CTA of unit u: the largest c with range_begin(c) <= u.
+__device__ __forceinline__ int owner_of(int u, int U, int G) {
+  int lo = 0, hi = G;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (range_begin(mid, U, G) <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Let the dependent launch (the main decode kernel) start its prologue.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding kernel has finished and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// One CTA: exclusive scan of units per sequence, each CTA's first segment,
+// zero outputs for empty sequences; reports bad
+// lengths once.  The scan is kept in shared memory (when it fits) for the
+// per-CTA searches.
+constexpr int kPlanSmemSeqs = 8191;
+constexpr int kPlanSmemGrid = 2431;
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
+  pdl_launch_dependents();
   __shared__ int warp_tot[32];
+  __shared__ int cu_s[kPlanSmemSeqs + 1];
+  const bool in_smem = p.B <= kPlanSmemSeqs;
+  int* cu = in_smem ? cu_s : p.cu_units;
   const int tid = threadIdx.x;
   const int chunk = (p.B + blockDim.x - 1) / blockDim.x;
   const int b0 = tid * chunk;
@@ -501,11 +535,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p, int m
   int local = 0;
   for (int b = b0; b < b1; ++b) {
     const int L = __ldg(p.seq_lens + b);
-    if (L < 0 || L > max_seq_len) report(p.err, PKV_DEVERR_LENGTH);
+    if (L < 0 || L > p.max_seq_len) report(p.err, PKV_DEVERR_LENGTH);
     else if (L > p.W * kBS) report(p.err, PKV_DEVERR_TABLE_WIDTH);
     local += p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
   }
-  // block-wide exclusive scan of `local`
   const int lane = tid & 31, wid = tid >> 5;
   int incl = local;
 #pragma unroll
@@ -527,72 +560,247 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p, int m
   __syncthreads();
   int run = incl - local + (wid > 0 ? warp_tot[wid - 1] : 0);
   for (int b = b0; b < b1; ++b) {
-    p.cu_units[b] = run;
-    run += p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
+    const int nb = p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
+    cu[b] = run;
+    if (in_smem) p.cu_units[b] = run;
+    run += nb;
   }
-  if (tid == blockDim.x - 1) p.cu_units[p.B] = run;
+  if (tid == blockDim.x - 1) {
+    cu[p.B] = run;
+    if (in_smem) p.cu_units[p.B] = run;
+  }
+  __syncthreads();  // the prefix is complete (same CTA: visible after the barrier)
+  const int U = cu[p.B];
+  __shared__ int rb_s[kPlanSmemGrid + 1];
+  __shared__ int n_split_s;
+  const bool rb_in_smem = p.grid <= kPlanSmemGrid;
+  int* rb = rb_in_smem ? rb_s : p.bounds;
+  if (tid == 0) n_split_s = 0;
+  for (int c = tid; c <= p.grid; c += blockDim.x) {
+    const int v = range_begin(c, U, p.grid);
+    rb[c] = v;
+    if (rb_in_smem) p.bounds[c] = v;
+  }
+  __syncthreads();
+  for (int c = tid; c < p.grid; c += blockDim.x) {
+    const int r0 = rb[c];
+    int4 st = make_int4(0, 0, 0, 0);
+    if (r0 < rb[c + 1]) {
+      const int b = seq_of_unit(cu, p.B, r0);
+      const int base = cu[b];
+      const int nblk = (used_len(p, b) + kBS - 1) / kBS;
+      const int grp = (r0 - base) / nblk;
+      const int j = (r0 - base) - grp * nblk;
+      st = make_int4(b, grp, j, 0);
+      if (j > 0) {
+        // CTA c begins inside a group: if it is the first CTA to do so, the
+        // group is split and listed once, with its first and last CTA
+        const int a = r0 - j;
+        int lo = 0, hi = p.grid;  // owner of unit a: largest c' with rb[c'] <= a
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (rb[mid] <= a) lo = mid; else hi = mid;
+        }
+        const int c0 = lo;
+        int first = c0 + 1;
+        while (rb[first + 1] == rb[first]) ++first;
+        if (first == c) {
+          const int e = a + nblk - 1;  // owner of the group's last unit
+          lo = c;
+          hi = p.grid;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (rb[mid] <= e) lo = mid; else hi = mid;
+          }
+          p.splits[atomicAdd(&n_split_s, 1)] = make_int4(b, grp, c0, lo);
+        }
+      }
+    }
+    p.starts[c] = st;
+  }
+  __syncthreads();
+  if (tid == 0) *p.n_splits = n_split_s;
+  // empty sequences get a zero output (no CTA owns any of their units)
+  T* out = static_cast<T*>(p.out);
+  const int row_elems = p.n_heads * HD;
+  for (int b = wid; b < p.B; b += blockDim.x >> 5) {
+    if (used_len(p, b) != 0) continue;
+    for (int i = lane; i < row_elems; i += 32) out[int64_t(b) * row_elems + i] = Elem<T>::from_f(0.f);
+  }
 }
 
-// A contiguous run of units of one (sequence, head group) inside this
-// CTA's range.
-struct Segment {
-  int b, grp, L, j_first, n_blocks;  // blocks j_first .. j_first+n_blocks-1
-  bool whole;                        // the run is the sequence's entire group
-  bool first_in_range;               // the run starts at this CTA's range start
+// Walks this CTA's contiguous range of units segment by segment: a segment
+// is the run of units of one (sequence, head group) inside the range.
+struct Cursor {
+  int b, grp, j, L, nblk;
+
+  __device__ __forceinline__ void load(const DecodeParams& p, int4 st) {
+    b = st.x;
+    grp = st.y;
+    j = st.z;
+    L = used_len(p, b);
+    nblk = (L + kBS - 1) / kBS;
+  }
+  // advance past n units of the current group
+  __device__ __forceinline__ void advance(const DecodeParams& p, int n) {
+    j += n;
+    if (j < nblk) return;
+    j = 0;
+    if (++grp < p.n_groups) return;
+    grp = 0;
+    do {
+      ++b;
+      L = b < p.B ? used_len(p, b) : 1;
+    } while (L == 0);
+    nblk = (L + kBS - 1) / kBS;
+  }
 };
 
-__device__ __forceinline__ Segment segment_at(const DecodeParams& p, int u, int range_start,
-                                              int range_end) {
-  Segment s;
-  s.b = seq_of_unit(p.cu_units, p.B, u);
-  const int base = __ldg(p.cu_units + s.b);
-  s.L = used_len(p, s.b);
-  const int nblk = (s.L + kBS - 1) / kBS;
-  s.grp = (u - base) / nblk;
-  s.j_first = (u - base) - s.grp * nblk;
-  const int grp_end = base + (s.grp + 1) * nblk;
-  const int end = min(range_end, grp_end);
-  s.n_blocks = end - u;
-  s.whole = (s.j_first == 0) && (end == grp_end);
-  s.first_in_range = (u == range_start);
-  return s;
+// Merge the partial results of one (sequence, head group) that several
+// CTAs computed: out = sum_c w_c o_c / sum_c w_c with w_c = exp2(m_c - M) l_c.
+// Parts are taken kMergeParts at a time with a running maximum, so any
+// number works.  Each thread keeps its (at most kMergeEpt) outputs in
+// registers and issues the loads of one part for all of them together.
+constexpr int kMergeParts = 8;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeEpt = 32;  // rows * head_dim <= 8192 = 256 threads x 32
+
+template <typename T, int HD>
+__device__ void merge_group(const DecodeParams& p, int b, int grp, int a, int c0, int c1,
+                            float* scratch) {
+  const int rows = p.hg_size * p.rep;
+  const int E = rows * HD;
+  float* m_s = scratch;                   // [rows][kMergeParts]
+  float* w_s = m_s + rows * kMergeParts;  // [rows][kMergeParts]
+  float* M_s = w_s + rows * kMergeParts;  // [rows]
+  float* den_s = M_s + rows;              // [rows]
+  float* alpha_s = den_s + rows;          // [rows]
+  int* slot_s = reinterpret_cast<int*>(alpha_s + rows);  // [kMergeParts + 1]
+  const int t = threadIdx.x;
+  float acc[kMergeEpt];
+#pragma unroll
+  for (int i = 0; i < kMergeEpt; ++i) acc[i] = 0.f;
+  for (int r = t; r < rows; r += kMergeThreads) {
+    M_s[r] = -INFINITY;
+    den_s[r] = 0.f;
+  }
+  for (int cs = c0; cs <= c1; cs += kMergeParts) {
+    __syncthreads();
+    if (t < 32) {  // the parts of CTAs cs .. cs+7 whose range is not empty
+      const int c = cs + t;
+      bool has = false;
+      int lo = 0;
+      if (t < kMergeParts && c <= c1) {
+        lo = __ldcg(p.bounds + c);
+        has = __ldcg(p.bounds + c + 1) > lo;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, has);
+      if (has) slot_s[__popc(m & ((1u << t) - 1))] = (c == c0 && lo != a) ? 2 * c + 1 : 2 * c;
+      if (t == 0) slot_s[kMergeParts] = __popc(m);
+    }
+    __syncthreads();
+    const int np = slot_s[kMergeParts];
+    if (np == 0) continue;
+    for (int i = t; i < rows * np; i += kMergeThreads) {
+      const int r = i / np, k = i - (i / np) * np;
+      const int64_t prow = int64_t(slot_s[k]) * rows + r;
+      m_s[r * kMergeParts + k] = __ldcg(p.ws_ml + prow * 2);
+      w_s[r * kMergeParts + k] = __ldcg(p.ws_ml + prow * 2 + 1);
+    }
+    __syncthreads();
+    for (int r = t; r < rows; r += kMergeThreads) {
+      float cm = -INFINITY;
+      for (int k = 0; k < np; ++k) cm = fmaxf(cm, m_s[r * kMergeParts + k]);
+      const float Mn = fmaxf(M_s[r], cm);
+      const float alpha = fast_exp2(M_s[r] - Mn);
+      float den = den_s[r] * alpha;
+      for (int k = 0; k < np; ++k) {
+        const float w = fast_exp2(m_s[r * kMergeParts + k] - Mn) * w_s[r * kMergeParts + k];
+        w_s[r * kMergeParts + k] = w;
+        den += w;
+      }
+      M_s[r] = Mn;
+      den_s[r] = den;
+      alpha_s[r] = alpha;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kMergeEpt; ++i) {
+      const int e = t + i * kMergeThreads;
+      if (e < E) acc[i] *= alpha_s[e / HD];
+    }
+    for (int k = 0; k < np; ++k) {
+      const float* po = p.ws_o + int64_t(slot_s[k]) * rows * HD;
+      float v[kMergeEpt];
+#pragma unroll
+      for (int i = 0; i < kMergeEpt; ++i) {
+        const int e = t + i * kMergeThreads;
+        v[i] = e < E ? __ldcg(po + e) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kMergeEpt; ++i) {
+        const int e = t + i * kMergeThreads;
+        if (e < E) acc[i] = fmaf(w_s[(e / HD) * kMergeParts + k], v[i], acc[i]);
+      }
+    }
+  }
+  __syncthreads();
+  T* out = static_cast<T*>(p.out) + (int64_t(b) * p.n_heads + grp * rows) * HD;
+#pragma unroll
+  for (int i = 0; i < kMergeEpt; ++i) {
+    const int e = t + i * kMergeThreads;
+    if (e < E) {
+      const float den = den_s[e / HD];
+      out[e] = Elem<T>::from_f(den > 0.f ? acc[i] / den : 0.f);
+    }
+  }
+}
+
+// Largest decode CTA of an instantiation: one producer warp plus one warp
+// per KV head of the group (at most 8 heads, at most 1 KB of row data).
+template <typename T, int HD>
+constexpr int decode_max_threads() {
+  return ((1024 / (HD * int(sizeof(T))) < 8 ? 1024 / (HD * int(sizeof(T))) : 8) + 1) * 32;
 }
 
 template <typename T, int HD, int MAXR, bool MMA>
-__global__ void __launch_bounds__(288) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   using Rows = typename RowsOf<T, HD, MAXR, MMA>::type;
   const int consumers = p.hg_size;
   const int row_bytes = p.hg_size * HD * p.elem_bytes;
   Ring ring = make_ring(smem, p.nstages, row_bytes);
   ring_init(ring, consumers);
+  pdl_wait();  // the plan kernel's work prefix and starts
+  pdl_launch_dependents();  // the merge kernel may be scheduled (it waits for this grid)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int U = __ldg(p.cu_units + p.B);
+  const int U = __ldcg(p.cu_units + p.B);
   const int G = gridDim.x;
   const int r0 = range_begin(blockIdx.x, U, G);
   const int r1 = range_begin(blockIdx.x + 1, U, G);
   const int64_t token_pitch = int64_t(p.n_kv) * HD * p.elem_bytes;  // bytes per pool slot
   const int rows_per_group = p.hg_size * p.rep;
+  Cursor cur;
+  if (r0 < r1) cur.load(p, __ldcg(p.starts + blockIdx.x));
 
   if (warp == consumers) {
     // ------------------------------------------------------ producer
     uint32_t it = 0;
     bool ok = true;
     for (int u = r0; u < r1 && ok;) {
-      const Segment s = segment_at(p, u, r0, r1);
-      const int32_t* row = p.bt + int64_t(s.b) * p.W;
-      const int64_t head_off = int64_t(s.grp) * p.hg_size * HD * p.elem_bytes;
-      for (int jj = 0; jj < s.n_blocks && ok; jj += 32) {
-        const int j_lane = s.j_first + jj + lane;
-        int id = (jj + lane < s.n_blocks) ? __ldg(row + j_lane) : 0;
-        const int n_here = min(32, s.n_blocks - jj);
+      const int n = min(r1 - u, cur.nblk - cur.j);
+      const int32_t* row = p.bt + int64_t(cur.b) * p.W;
+      const int64_t head_off = int64_t(cur.grp) * p.hg_size * HD * p.elem_bytes;
+      for (int jj = 0; jj < n && ok; jj += 32) {
+        int id = (jj + lane < n) ? __ldg(row + cur.j + jj + lane) : 0;
+        const int n_here = min(32, n - jj);
         for (int k = 0; k < n_here; ++k) {
           if (*ring.abort_flag) { ok = false; break; }
           const int blk = __shfl_sync(0xffffffffu, id, k);
-          const int j = s.j_first + jj + k;
-          int valid = min(kBS, s.L - j * kBS);
+          const int j = cur.j + jj + k;
+          int valid = min(kBS, cur.L - j * kBS);
           if (blk < 0 || blk >= p.num_blocks) {
             if (lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
             valid = 0;
@@ -606,7 +814,8 @@ __global__ void __launch_bounds__(288) decode_kernel(DecodeParams p) {
           ++it;
         }
       }
-      u += s.n_blocks;
+      u += n;
+      cur.advance(p, n);
     }
     if (!ok) ring_drain(ring, it);
   } else if (warp < consumers) {
@@ -619,17 +828,19 @@ __global__ void __launch_bounds__(288) decode_kernel(DecodeParams p) {
     uint32_t it = 0;
     bool ok = true;
     const T* q = static_cast<const T*>(p.q);
+    T* out = static_cast<T*>(p.out);
     for (int u = r0; u < r1 && ok;) {
-      const Segment s = segment_at(p, u, r0, r1);
-      const int kv_head = s.grp * p.hg_size + warp;
+      const int n = min(r1 - u, cur.nblk - cur.j);
+      const int b = cur.b;
+      const int kv_head = cur.grp * p.hg_size + warp;
       const int head0 = kv_head * p.rep;
-      const int last = s.L - 1;
+      const int last = cur.L - 1;
       rows.begin(
           [&](int r) -> const T* {
-            return r < p.rep ? q + (int64_t(s.b) * p.n_heads + head0 + r) * HD : nullptr;
+            return r < p.rep ? q + (int64_t(b) * p.n_heads + head0 + r) * HD : nullptr;
           },
           [&](int) { return last; });
-      for (int k = 0; k < s.n_blocks; ++k) {
+      for (int k = 0; k < n; ++k) {
         if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
           *ring.abort_flag = 1;
           ok = false;
@@ -638,96 +849,26 @@ __global__ void __launch_bounds__(288) decode_kernel(DecodeParams p) {
         const int st = static_cast<int>(it % ring.nstages);
         const int hoff = warp * HD * p.elem_bytes;
         rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride,
-                   (s.j_first + k) * kBS, p.scale_log2);
+                   (cur.j + k) * kBS, p.scale_log2);
         ring_release(ring, it);
         ++it;
       }
       if (!ok) break;
-      if (s.whole) {
-        T* out = static_cast<T*>(p.out);
+      const bool whole = (cur.j == 0) && (n == cur.nblk);
+      if (whole) {
         rows.store([&](int r) -> T* {
-          return r < p.rep ? out + (int64_t(s.b) * p.n_heads + head0 + r) * HD : nullptr;
+          return r < p.rep ? out + (int64_t(b) * p.n_heads + head0 + r) * HD : nullptr;
         });
       } else {
-        const int slot = 2 * blockIdx.x + (s.first_in_range ? 0 : 1);
+        // partial result of a group split over several CTAs
+        const int slot = 2 * blockIdx.x + (u == r0 ? 0 : 1);
         const int64_t base_row = int64_t(slot) * rows_per_group + warp * p.rep;
         rows.store_partial(
             [&](int r) -> float* { return r < p.rep ? p.ws_o + (base_row + r) * HD : nullptr; },
             [&](int r) -> float* { return p.ws_ml + (base_row + r) * 2; });
       }
-      u += s.n_blocks;
-    }
-  }
-}
-
-// Owner CTA of unit u: the largest c with range_begin(c) <= u.
-__device__ __forceinline__ int owner_of(int u, int U, int G) {
-  int lo = 0, hi = G;  // answer in [lo, hi)
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (range_begin(mid, U, G) <= u) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-// Combine the partials of every (sequence, head group) that was split over
-// several CTAs; write zeros for empty sequences.  One warp per (sequence,
-// query head).
-template <typename T, int HD>
-__global__ void decode_merge_kernel(DecodeParams p, int G) {
-  const int warps_per_cta = blockDim.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t total = int64_t(p.B) * p.n_heads;
-  const int U = __ldg(p.cu_units + p.B);
-  const int rows_per_group = p.hg_size * p.rep;
-  for (int64_t wi = int64_t(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5); wi < total;
-       wi += int64_t(gridDim.x) * warps_per_cta) {
-    const int b = static_cast<int>(wi / p.n_heads);
-    const int h = static_cast<int>(wi - int64_t(b) * p.n_heads);
-    T* out = static_cast<T*>(p.out) + wi * HD;
-    const int L = used_len(p, b);
-    if (L == 0) {
-      for (int d = lane; d < HD; d += 32) out[d] = Elem<T>::from_f(0.f);
-      continue;
-    }
-    const int nblk = (L + kBS - 1) / kBS;
-    const int kv_head = h / p.rep;
-    const int grp = kv_head / p.hg_size;
-    const int row_in_group = (kv_head - grp * p.hg_size) * p.rep + (h - kv_head * p.rep);
-    const int a = __ldg(p.cu_units + b) + grp * nblk;  // first unit of (b, grp)
-    const int e = a + nblk;                            // one past the last
-    const int c0 = owner_of(a, U, G);
-    const int c1 = owner_of(e - 1, U, G);
-    if (c0 == c1) continue;  // finished inside one CTA
-    // pass 1: common maximum
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) {
-      if (range_begin(c + 1, U, G) == range_begin(c, U, G)) continue;  // empty range
-      const int slot = (c == c0 && range_begin(c, U, G) != a) ? 2 * c + 1 : 2 * c;
-      M = fmaxf(M, p.ws_ml[(int64_t(slot) * rows_per_group + row_in_group) * 2]);
-    }
-    float acc[(HD + 31) / 32];
-#pragma unroll
-    for (int i = 0; i < (HD + 31) / 32; ++i) acc[i] = 0.f;
-    float den = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-      if (range_begin(c + 1, U, G) == range_begin(c, U, G)) continue;  // empty range
-      const int slot = (c == c0 && range_begin(c, U, G) != a) ? 2 * c + 1 : 2 * c;
-      const int64_t row = int64_t(slot) * rows_per_group + row_in_group;
-      const float w = fast_exp2(p.ws_ml[row * 2] - M) * p.ws_ml[row * 2 + 1];
-      den += w;
-      const float* po = p.ws_o + row * HD;
-#pragma unroll
-      for (int i = 0; i < (HD + 31) / 32; ++i) {
-        const int d = lane + 32 * i;
-        if (d < HD) acc[i] = fmaf(w, po[d], acc[i]);
-      }
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-    for (int i = 0; i < (HD + 31) / 32; ++i) {
-      const int d = lane + 32 * i;
-      if (d < HD) out[d] = Elem<T>::from_f(acc[i] * inv);
+      u += n;
+      cur.advance(p, n);
     }
   }
 }
@@ -881,10 +1022,66 @@ int stages_for(int stage_bytes, int scratch_bytes, int target_bytes) {
   return ns;
 }
 
+// Merge of the split groups listed by the plan kernel, one CTA each.
+// Launched as a programmatic dependent of the main kernel.
+template <typename T, int HD>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) float merge_smem[];
+  pdl_wait();  // the main kernel's partials
+  if (static_cast<int>(blockIdx.x) >= __ldcg(p.n_splits)) return;
+  const int4 sp = __ldcg(p.splits + blockIdx.x);  // (sequence, head group, first CTA, last CTA)
+  const int nblk = (used_len(p, sp.x) + kBS - 1) / kBS;
+  const int a = __ldcg(p.cu_units + sp.x) + sp.y * nblk;
+  merge_group<T, HD>(p, sp.x, sp.y, a, sp.z, sp.w, merge_smem);
+}
+
+// Shared memory merge_group needs for one group.
+size_t merge_smem_bytes(int rows, int) {
+  return (2 * size_t(rows) * kMergeParts + 3 * size_t(rows)) * 4 + (kMergeParts + 1) * 4;
+}
+
+// Decode workspace layout: cu_units [B+1] | starts [G] | bounds [G+1] |
+// splits [G] | n_splits | partial max/sum [2G][rows][2] | partial outputs
+// [2G][rows][HD], each region 256-byte aligned.
+struct DecodeWs {
+  size_t cu, starts, bounds, splits, n_splits, ml, o, total;
+  DecodeWs(int num_seqs, size_t G, size_t rows_per_group, int head_dim) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    cu = 0;
+    starts = up(size_t(num_seqs + 1) * 4);
+    bounds = starts + up(G * 16);
+    splits = bounds + up((G + 1) * 4);
+    n_splits = splits + up(G * 16);
+    ml = n_splits + 256;
+    o = ml + up(2 * G * rows_per_group * 2 * 4);
+    total = o + 2 * G * rows_per_group * size_t(head_dim) * 4;
+  }
+};
+
 template <typename T, int HD, int MAXR, bool MMA>
 struct DecodeLaunch {
   static size_t scratch_bytes(int warps) {
     return MMA ? 0 : size_t(warps) * RowsOf<T, HD, MAXR, MMA>::kScratch * sizeof(float);
+  }
+  static size_t smem_bytes(int hg, int elem_bytes, int* nstages) {
+    const int row_bytes = hg * HD * elem_bytes;
+    const int stage_bytes = 2 * kBS * (row_bytes + 16);
+    const size_t scratch = scratch_bytes(hg);
+    *nstages = stages_for(stage_bytes, static_cast<int>(scratch), 110 * 1024);
+    return kBarrierBytes + size_t(*nstages) * stage_bytes + scratch;
+  }
+  // Persistent grid: every SM filled with as many CTAs as fit, capped by max_ctas.
+  static cudaError_t grid(const AttnArgs& a, int hg, int* G, size_t* smem, int* nstages) {
+    *smem = smem_bytes(hg, a.pool.elem_bytes(), nstages);
+    static KernelSetup setup;
+    int per_sm = 0;
+    const cudaError_t e = kernel_setup(setup, decode_kernel<T, HD, MAXR, MMA>,
+                                       static_cast<int>(*smem), (hg + 1) * 32, &per_sm);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    *G = sm_count() * per_sm;
+    if (a.max_ctas > 0 && a.max_ctas < *G) *G = a.max_ctas;
+    return cudaSuccess;
   }
   static cudaError_t run(const AttnArgs& a, int hg, cudaStream_t stream) {
     const PoolShape& pool = a.pool;
@@ -905,74 +1102,64 @@ struct DecodeLaunch {
     p.W = a.max_blocks_per_seq;
     p.num_blocks = pool.num_blocks;
     p.max_len = min(a.max_seq_len, a.max_blocks_per_seq * kBS);
+    p.max_seq_len = a.max_seq_len;
     p.head_dim = HD;
     p.elem_bytes = pool.elem_bytes();
     p.scale_log2 = a.scale * kLog2e;
-    const int row_bytes = hg * HD * p.elem_bytes;
-    const int stage_bytes = 2 * kBS * (row_bytes + 16);
-    const int threads = (hg + 1) * 32;
-    const size_t scratch = scratch_bytes(hg);
-    p.nstages = stages_for(stage_bytes, static_cast<int>(scratch), 110 * 1024);
-    const size_t smem = kBarrierBytes + size_t(p.nstages) * stage_bytes + scratch;
-    auto kern = decode_kernel<T, HD, MAXR, MMA>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    int G = 0;
+    size_t smem = 0;
+    cudaError_t e = grid(a, hg, &G, &smem, &p.nstages);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    int G = sm_count() * per_sm;
-    if (a.max_ctas > 0 && a.max_ctas < G) G = a.max_ctas;
-    // workspace: cu_units | ml | o
+    p.grid = G;
+    const DecodeWs L(a.num_seqs, G, size_t(hg) * p.rep, HD);
+    if (L.total > a.workspace_bytes) return cudaErrorInvalidValue;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-    const int rows_per_group = hg * p.rep;
-    const size_t cu_bytes = (size_t(a.num_seqs + 1) * 4 + 255) / 256 * 256;
-    const size_t ml_bytes = (size_t(2) * G * rows_per_group * 2 * 4 + 255) / 256 * 256;
-    const size_t o_bytes = size_t(2) * G * rows_per_group * HD * 4;
-    if (cu_bytes + ml_bytes + o_bytes > a.workspace_bytes) return cudaErrorInvalidValue;
-    p.cu_units = reinterpret_cast<int32_t*>(ws);
-    p.ws_ml = reinterpret_cast<float*>(ws + cu_bytes);
-    p.ws_o = reinterpret_cast<float*>(ws + cu_bytes + ml_bytes);
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(p, a.max_seq_len);
+    p.cu_units = reinterpret_cast<int32_t*>(ws + L.cu);
+    p.starts = reinterpret_cast<int4*>(ws + L.starts);
+    p.bounds = reinterpret_cast<int32_t*>(ws + L.bounds);
+    p.splits = reinterpret_cast<int4*>(ws + L.splits);
+    p.n_splits = reinterpret_cast<int32_t*>(ws + L.n_splits);
+    p.ws_ml = reinterpret_cast<float*>(ws + L.ml);
+    p.ws_o = reinterpret_cast<float*>(ws + L.o);
+    decode_plan_kernel<T, HD><<<1, 1024, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kern<<<G, threads, smem, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t warps = int64_t(a.num_seqs) * a.n_heads;
-    int mgrid = static_cast<int>((warps + 7) / 8);
-    if (mgrid > sm_count() * 16) mgrid = sm_count() * 16;
-    if (mgrid < 1) mgrid = 1;
-    decode_merge_kernel<T, HD><<<mgrid, 256, 0, stream>>>(p, G);
+    // the main kernel may start while the plan kernel runs: it waits for
+    // the plan's results (griddepcontrol.wait) after its prologue
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3((hg + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<T, HD, MAXR, MMA>, p);
+    if (e != cudaSuccess) return e;
+    // split groups: one small CTA per main-kernel boundary, most exit at once
+    const size_t msmem = merge_smem_bytes(hg * p.rep, HD);
+    static KernelSetup merge_setup;
+    e = kernel_setup(merge_setup, decode_merge_kernel<T, HD>, static_cast<int>(msmem),
+                     kMergeThreads, nullptr);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = msmem;
+    e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, HD>, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
 };
 
 // Exact workspace of the grid DecodeLaunch::run would launch for these
-// arguments (run() lays the workspace out the same way).
+// arguments.
 template <typename T, int HD, int MAXR, bool MMA>
 size_t decode_exact_workspace(const AttnArgs& a, int hg) {
-  const int rep = a.n_heads / a.pool.n_kv;
-  const int row_bytes = hg * HD * a.pool.elem_bytes();
-  const int stage_bytes = 2 * kBS * (row_bytes + 16);
-  const int threads = (hg + 1) * 32;
-  const size_t scratch = DecodeLaunch<T, HD, MAXR, MMA>::scratch_bytes(hg);
-  const int nstages = stages_for(stage_bytes, static_cast<int>(scratch), 110 * 1024);
-  const size_t smem = kBarrierBytes + size_t(nstages) * stage_bytes + scratch;
-  auto kern = decode_kernel<T, HD, MAXR, MMA>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return 0;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess)
-    return 0;
-  if (per_sm < 1) per_sm = 1;
-  int G = sm_count() * per_sm;
-  if (a.max_ctas > 0 && a.max_ctas < G) G = a.max_ctas;
-  const int rows_per_group = hg * rep;
-  const size_t cu_bytes = (size_t(a.num_seqs + 1) * 4 + 255) / 256 * 256;
-  const size_t ml_bytes = (size_t(2) * G * rows_per_group * 2 * 4 + 255) / 256 * 256;
-  const size_t o_bytes = size_t(2) * G * rows_per_group * HD * 4;
-  return cu_bytes + ml_bytes + o_bytes;
+  int G = 0, nstages = 0;
+  size_t smem = 0;
+  if (DecodeLaunch<T, HD, MAXR, MMA>::grid(a, hg, &G, &smem, &nstages) != cudaSuccess) return 0;
+  return DecodeWs(a.num_seqs, G, size_t(hg) * (a.n_heads / a.pool.n_kv), HD).total;
 }
 
 template <typename T, int HD, int MAXR, bool MMA>
@@ -1007,8 +1194,9 @@ struct PrefillLaunch {
     p.nstages = stages_for(stage_bytes, static_cast<int>(scratch), 100 * 1024);
     const size_t smem = kBarrierBytes + size_t(p.nstages) * stage_bytes + scratch;
     auto kern = prefill_kernel<T, HD, MAXR, MMA>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static KernelSetup setup;
+    cudaError_t e = kernel_setup(setup, kern, static_cast<int>(smem),
+                                 (p.consumer_warps + 1) * 32, nullptr);
     if (e != cudaSuccess) return e;
     const int tile_q = p.consumer_warps * p.queries_per_warp;
     const int tiles = (a.max_q_len + tile_q - 1) / tile_q;
@@ -1045,16 +1233,10 @@ bool prefill_supported(const PoolShape& pool, int32_t n_heads) { return decode_s
 
 int32_t decode_default_partition(int32_t, int32_t, int32_t, int32_t) { return 0; }
 
-// Upper bound of the decode workspace: cu_units plus two partial slots per
-// CTA of the largest grid this device can run (every SM full of the
-// smallest CTA).
+// Upper bound of the decode workspace over every grid this device can run.
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim, int32_t, int32_t) {
-  const size_t G = size_t(sm_count()) * 16;
-  const size_t rows = size_t(n_heads);  // rows per group <= n_heads
-  const size_t cu = (size_t(num_seqs + 1) * 4 + 255) / 256 * 256;
-  const size_t ml = (2 * G * rows * 2 * 4 + 255) / 256 * 256;
-  const size_t o = 2 * G * rows * size_t(head_dim) * 4;
-  return cu + ml + o;
+  // rows per head group <= n_heads; at most 16 resident CTAs per SM
+  return DecodeWs(num_seqs, size_t(sm_count()) * 16, size_t(n_heads), head_dim).total;
 }
 
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s) {

@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include "device.cuh"
+#include "host_cache.h"
 #include "launch.h"
 #include "tcgen05.cuh"
 
@@ -457,8 +458,8 @@ cudaError_t run_tc(const AttnArgs& a, cudaStream_t stream) {
                  uint64_t(pool.n_kv) * HD * 2, 64, 1, kBlk))
     return cudaErrorInvalidValue;
   auto kern = prefill_tc_kernel<HD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Lay::REQUEST);
+  static KernelSetup setup;
+  const cudaError_t e = kernel_setup(setup, kern, Lay::REQUEST, kThreads, nullptr);
   if (e != cudaSuccess) return e;
   const int tiles = (a.max_q_len + p.q_per_tile - 1) / p.q_per_tile;
   dim3 grid(tiles, pool.n_kv, a.num_seqs);
