@@ -6,23 +6,26 @@
 // queries at the end of an L-token sequence attends keys 0 .. L - c + i of
 // its KV head, read in place through the block table.
 //
-// One CTA owns 128 MMA rows of one (sequence, KV head): 128 / rep
-// consecutive queries x the rep query heads that share the KV head, so one
-// K/V tile feeds every head of the GQA group.  Keys are processed in tiles
-// of 64 (four 16-token blocks).
+// One CTA (one per SM) owns two 128-row tiles, A and B, of one (sequence,
+// KV head): each row is one (query, query head) pair, 128 / rep queries x
+// the rep query heads that share the KV head, so one K/V tile feeds every
+// head of the GQA group and both tiles.  Keys go in tiles of 128 (eight
+// 16-token blocks).
 //
-//  warp 4    TMA producer: the Q tile once (two 64-column halves, 128-byte
+//  warp 8    TMA producer: Q_A and Q_B once (64-column halves, 128-byte
 //            swizzle), then per key tile one 16-row box per block and half
 //            for K and for V into a two-stage ring.
-//  warp 5    allocates 256 TMEM columns (S tile 0, S tile 1, O) and one
-//            lane issues the MMAs:  S_j = Q K_j^T  (smem x smem -> TMEM),
-//            then after softmax  O += P_j V_j  (P read from TMEM, V
-//            MN-major from smem).  S_{j+1} is issued before waiting for P_j
-//            so the tensor core runs while softmax works.
-//  warps 0-3 softmax: thread r owns TMEM lane r (one query row): loads its
-//            64 scores, masks causally, keeps a running max in log2 units
-//            and only rescales O when the max grows by more than 2^8,
-//            writes P as bf16 over its S tile, and in the epilogue
+//  warp 9    allocates all 512 TMEM columns (S_A, S_B, O_A, O_B) and one
+//            lane issues the MMAs in ping-pong order:
+//               S_A = Q_A K_j^T, S_B = Q_B K_j^T, then for each tile once its
+//               softmax is done: O_X += P_X V_j and at once S_X = Q_X K_{j+1}^T,
+//            so the tensor core works on one tile while the other tile's
+//            softmax runs.  P_X is read from TMEM (it overwrites S_X as bf16),
+//            V MN-major from shared memory.
+//  warps 0-3 softmax of tile A, warps 4-7 of tile B: thread r owns TMEM lane
+//            r (one row), loads its 128 scores, masks causally, keeps a
+//            running max in log2 units and rescales O only when the max grows
+//            by more than 2^8, writes P as bf16, and in the epilogue
 //            normalises O and stores the row.
 //
 // Value rows past the sequence end inside the last key tile are zeroed in
@@ -43,15 +46,16 @@ namespace pkv {
 
 namespace {
 
-constexpr int kRows = 128;      // MMA rows per CTA
-constexpr int kTileKeys = 64;   // keys per S tile
-constexpr int kBlk = 16;        // tokens per pool block
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kRows = 128;       // MMA rows per tile
+constexpr int kTileKeys = 128;   // keys per S tile
+constexpr int kBlk = 16;         // tokens per pool block
+constexpr int kBlocksPerTile = kTileKeys / kBlk;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows past 2^8
-constexpr uint32_t kTmemCols = 256;  // S0 [0,64) S1 [64,128) O [128,128+HD)
+constexpr uint32_t kTmemCols = 512;  // S_A [0,128) S_B [128,256) O_A [256,..) O_B [384,..)
 
 struct TcParams {
   const int32_t* bt;
@@ -65,18 +69,18 @@ struct TcParams {
 
 template <int HD>
 struct Layout {
-  static constexpr int NH = HD / 64;                      // 128-byte column halves
-  static constexpr int Q_HALF = kRows * 128;              // 16 KB
-  static constexpr int KV_HALF = kTileKeys * 128;         // 8 KB
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = NH * Q_HALF;               // stage s: K at K_OFF + s*STAGE
-  static constexpr int STAGE = 2 * NH * KV_HALF;          // K then V
+  static constexpr int NH = HD / 64;                    // 128-byte column halves
+  static constexpr int Q_HALF = kRows * 128;            // 16 KB
+  static constexpr int KV_HALF = kTileKeys * 128;       // 16 KB
+  static constexpr int Q_TILE = NH * Q_HALF;
+  static constexpr int K_OFF = 2 * Q_TILE;              // stage s: K at K_OFF + s*STAGE
+  static constexpr int STAGE = 2 * NH * KV_HALF;        // K then V
   static constexpr int V_IN_STAGE = NH * KV_HALF;
   static constexpr int BAR_OFF = K_OFF + 2 * STAGE;
   static constexpr int BYTES = BAR_OFF + 256;
-  // launch request: 1 KB alignment slack, and at least 90 KB so at most two
-  // CTAs share an SM (two x 256 TMEM columns fill its 512)
-  static constexpr int REQUEST = (BYTES + 1024) > 90 * 1024 ? (BYTES + 1024) : 90 * 1024;
+  // + 1 KB alignment slack; at least 120 KB so only one CTA fits per SM (it
+  // takes all 512 TMEM columns)
+  static constexpr int REQUEST = (BYTES + 1024) > 120 * 1024 ? (BYTES + 1024) : 120 * 1024;
 };
 
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
@@ -85,7 +89,7 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, TcParams p) {
   using Lay = Layout<HD>;
@@ -97,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int g = blockIdx.y;
   const int q0 = __ldg(p.cu_q + b);
   const int c = __ldg(p.cu_q + b + 1) - q0;
-  const int i0 = blockIdx.x * p.q_per_tile;
+  const int i0 = blockIdx.x * 2 * p.q_per_tile;  // first query of tile A
   if (i0 >= c) return;  // idle CTA: leave before any barrier or TMEM use
   if (q0 < 0 || q0 + c > p.total_q) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.err, PKV_DEVERR_LENGTH);
@@ -111,20 +115,20 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (L > p.max_len) L = p.max_len;
   if (L < c) return;
-  const int i_end = min(c, i0 + p.q_per_tile);
+  const int i_end = min(c, i0 + 2 * p.q_per_tile);
   const int n_tiles = (L - c + i_end - 1) / kTileKeys + 1;
   const int n_blocks_seq = (L + kBlk - 1) / kBlk;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [2]
-  uint64_t* v_full = bars + 3;    // [2]
-  uint64_t* kv_empty = bars + 5;  // [2]
-  uint64_t* s_full = bars + 7;    // [2]
-  uint64_t* p_ready = bars + 9;   // [2]
-  uint64_t* o_done = bars + 11;
-  uint64_t* drain = bars + 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* k_full = bars + 1;    // [2] per stage
+  uint64_t* v_full = bars + 3;    // [2] per stage
+  uint64_t* kv_empty = bars + 5;  // [2] per stage
+  uint64_t* s_full = bars + 7;    // [2] per tile A/B
+  uint64_t* p_ready = bars + 9;   // [2] per tile A/B
+  uint64_t* o_done = bars + 11;   // [2] per tile A/B
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -137,8 +141,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(kv_empty + i, 1);
       mbar_init(s_full + i, 1);
       mbar_init(p_ready + i, kRows);
+      mbar_init(o_done + i, 1);
     }
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -151,33 +155,36 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t o_tm = tmem + 128;
-  uint8_t* q_s = smem + Lay::Q_OFF;
+  auto q_tile = [&](int x) { return smem + x * Lay::Q_TILE; };
   auto k_st = [&](int st) { return smem + Lay::K_OFF + st * Lay::STAGE; };
   auto v_st = [&](int st) { return smem + Lay::K_OFF + st * Lay::STAGE + Lay::V_IN_STAGE; };
+  auto s_tm = [&](int x) { return tmem + uint32_t(x) * kTileKeys; };
+  auto o_tm = [&](int x) { return tmem + 256u + uint32_t(x) * 128u; };
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, Lay::NH * Lay::Q_HALF);
-      for (int h = 0; h < Lay::NH; ++h)
-        tc::tma_load_3d(q_s + h * Lay::Q_HALF, &tq, h * 64, g * p.rep, q0 + i0, q_full);
+      mbar_arrive_expect_tx(q_full, 2 * Lay::Q_TILE);
+      for (int x = 0; x < 2; ++x)
+        for (int h = 0; h < Lay::NH; ++h)
+          tc::tma_load_3d(q_tile(x) + h * Lay::Q_HALF, &tq, h * 64, g * p.rep,
+                          q0 + i0 + x * p.q_per_tile, q_full);
     }
     const int32_t* row = p.bt + int64_t(b) * p.W;
     int issued = 0;
-    int ids = 0;  // lane l holds the id of block (j / 8) * 32 + l
+    int ids = 0;  // lane l holds the id of block (j / 4) * 32 + l
     for (int j = 0; j < n_tiles; ++j) {
       if (*abort_flag) break;
       const int st = j & 1;
       const uint32_t use = j >> 1;
-      if ((j & 7) == 0) {
-        const int jb32 = j * 4 + lane;
+      if ((j & 3) == 0) {
+        const int jb32 = j * kBlocksPerTile + lane;
         ids = jb32 < n_blocks_seq ? __ldg(row + jb32) : 0;
       }
-      const int jb = j * 4 + lane;  // lanes 0-3: the tile's four blocks
-      const int blk_l = __shfl_sync(0xffffffffu, ids, ((j & 7) * 4 + lane) & 31);
+      const int jb = j * kBlocksPerTile + lane;  // lanes 0-7: the tile's eight blocks
+      const int blk_l = __shfl_sync(0xffffffffu, ids, ((j & 3) * kBlocksPerTile + lane) & 31);
       int blk = 0;
-      bool load = lane < 4 && jb < n_blocks_seq;
+      bool load = lane < kBlocksPerTile && jb < n_blocks_seq;
       if (load) {
         blk = blk_l;
         if (blk < 0 || blk >= p.num_blocks) {
@@ -219,43 +226,47 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, kTileKeys, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, HD, false, true);
-      const uint32_t q_addr = smem_addr(q_s);
-      bool ok = mbar_wait(q_full, 0);
-      auto issue_qk = [&](int j) {
+      auto issue_qk = [&](int x, int j) {
+        const uint32_t q_addr = smem_addr(q_tile(x));
         const uint32_t k_addr = smem_addr(k_st(j & 1));
-        const uint32_t d = tmem + (j & 1) * kTileKeys;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off_q = (kk >> 2) * Lay::Q_HALF + (kk & 3) * 32;
           const uint32_t off_k = (kk >> 2) * Lay::KV_HALF + (kk & 3) * 32;
-          tc::mma_ss(d, tc::sw128_desc(q_addr + off_q, 16, 1024),
+          tc::mma_ss(s_tm(x), tc::sw128_desc(q_addr + off_q, 16, 1024),
                      tc::sw128_desc(k_addr + off_k, 16, 1024), idesc_qk, kk > 0);
         }
-        tc::commit(s_full + (j & 1));
+        tc::commit(s_full + x);
       };
-      if (ok && (ok = mbar_wait(k_full, 0))) {
-        tc::fence_after_sync();
-        issue_qk(0);
-      }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles) {
-          if (!(ok = mbar_wait(k_full + ((j + 1) & 1), ((j + 1) >> 1) & 1))) break;
-          tc::fence_after_sync();
-          issue_qk(j + 1);
-        }
-        if (!(ok = mbar_wait(p_ready + (j & 1), (j >> 1) & 1))) break;
-        if (!(ok = mbar_wait(v_full + (j & 1), (j >> 1) & 1))) break;
-        tc::fence_after_sync();
+      auto issue_pv = [&](int x, int j) {
         const uint32_t v_addr = smem_addr(v_st(j & 1));
-        const uint32_t p_tm = tmem + (j & 1) * kTileKeys;
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; ++kk) {
           // 16 keys = two 8-row groups of the V tile; P: 16 bf16 = 8 columns
-          tc::mma_ts(o_tm, p_tm + kk * 8, tc::sw128_desc(v_addr + kk * 2048, Lay::KV_HALF, 1024),
-                     idesc_pv, j > 0 || kk > 0);
+          tc::mma_ts(o_tm(x), s_tm(x) + kk * 8,
+                     tc::sw128_desc(v_addr + kk * 2048, Lay::KV_HALF, 1024), idesc_pv,
+                     j > 0 || kk > 0);
         }
-        tc::commit(o_done);
-        tc::commit(kv_empty + (j & 1));
+        tc::commit(o_done + x);
+      };
+      bool ok = mbar_wait(q_full, 0) && mbar_wait(k_full, 0);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_qk(0, 0);
+        issue_qk(1, 0);
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const bool more = j + 1 < n_tiles;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (!(ok = mbar_wait(p_ready + x, j & 1))) break;
+          if (x == 0 && !(ok = mbar_wait(v_full + (j & 1), (j >> 1) & 1))) break;
+          if (x == 0 && more && !(ok = mbar_wait(k_full + ((j + 1) & 1), ((j + 1) >> 1) & 1)))
+            break;
+          tc::fence_after_sync();
+          issue_pv(x, j);
+          if (x == 1) tc::commit(kv_empty + (j & 1));  // K_j and V_j are no longer read
+          if (more) issue_qk(x, j + 1);
+        }
       }
       if (!ok) {
         report(p.err, PKV_DEVERR_TIMEOUT);
@@ -268,21 +279,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
-    const int r = threadIdx.x;  // TMEM lane = MMA row
-    const int qi = i0 + r / p.rep;
+    const int x = warp >> 2;                   // tile A (warps 0-3) or B (warps 4-7)
+    const int r = threadIdx.x - x * kRows;     // TMEM lane = row of the tile
+    const int qi = i0 + x * p.q_per_tile + r / p.rep;
     const int hh = r - (r / p.rep) * p.rep;
     const bool active = qi < c;
     const int last = active ? L - c + qi : -1;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!(ok = wait_all(s_full + (j & 1), (j >> 1) & 1))) break;
+      if (!(ok = wait_all(s_full + x, j & 1))) break;
       tc::fence_after_sync();
-      const uint32_t s_tm = tmem + lane_base + (j & 1) * kTileKeys;
-      uint32_t sr[64];
-      tc::tmem_ld32(s_tm, *reinterpret_cast<uint32_t(*)[32]>(sr));
-      tc::tmem_ld32(s_tm + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      const uint32_t s_addr = s_tm(x) + lane_base;
+      uint32_t sr[kTileKeys];
+#pragma unroll
+      for (int ch = 0; ch < kTileKeys / 32; ++ch)
+        tc::tmem_ld32(s_addr + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + ch * 32));
       tc::tmem_wait_ld();
       const int pos0 = j * kTileKeys;
       if (pos0 + kTileKeys - 1 > last) {  // tile crosses this row's causal limit
@@ -290,8 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int k = 0; k < kTileKeys; ++k)
           if (pos0 + k > last) sr[k] = __float_as_uint(-INFINITY);
       }
-      // the max is taken on raw scores (scale > 0); scale and shift then
-      // fold into one packed FMA per pair of scores
+      // max on raw scores (scale > 0); scale and shift fold into one packed FMA
       float mx = -INFINITY;
 #pragma unroll
       for (int k = 0; k < kTileKeys; ++k) mx = fmaxf(mx, __uint_as_float(sr[k]));
@@ -302,31 +314,37 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       const float2 nm2 = make_float2(-mref, -mref);
-      uint32_t pk[32];
       float2 acc = make_float2(0.f, 0.f);
+      // P overwrites the first half of S_X in TMEM, 16 columns per 32 scores;
+      // the scores are already in registers
 #pragma unroll
-      for (int k = 0; k < kTileKeys / 2; ++k) {
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]),
-                                                __uint_as_float(sr[2 * k + 1])), sc2, nm2);
-        const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-        acc = __fadd2_rn(acc, pe);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(pe.x, pe.y);
-        pk[k] = *reinterpret_cast<const uint32_t*>(&pb);
+      for (int ch = 0; ch < kTileKeys / 32; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int e = ch * 32 + 2 * k;
+          const float2 t2 = __ffma2_rn(
+              make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nm2);
+          const float2 pe = make_float2(fast_exp2(t2.x), fast_exp2(t2.y));
+          acc = __fadd2_rn(acc, pe);
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(pe.x, pe.y);
+          pk[k] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+        tc::tmem_st16(s_addr + ch * 16, pk);
       }
-      const float psum = acc.x + acc.y;
-      l_sum = l_sum * alpha + psum;
+      l_sum = l_sum * alpha + (acc.x + acc.y);
       if (j > 0) {
         // P V of the previous tile must be done before O is rescaled (and
         // this keeps the o_done phases in step)
-        if (!(ok = wait_all(o_done, (j - 1) & 1))) break;
+        if (!(ok = wait_all(o_done + x, (j - 1) & 1))) break;
         tc::fence_after_sync();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int ch = 0; ch < HD / 32; ++ch) {
             uint32_t ov[32];
-            tc::tmem_ld32(o_tm + lane_base + ch * 32, ov);
+            tc::tmem_ld32(o_tm(x) + lane_base + ch * 32, ov);
             tc::tmem_wait_ld();
-            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               const float2 o2 = __fmul2_rn(
@@ -334,15 +352,15 @@ __global__ void __launch_bounds__(kThreads, 2)
               ov[2 * k] = __float_as_uint(o2.x);
               ov[2 * k + 1] = __float_as_uint(o2.y);
             }
-            tc::tmem_st32(o_tm + lane_base + ch * 32, ov);
+            tc::tmem_st32(o_tm(x) + lane_base + ch * 32, ov);
           }
         }
       }
-      tc::tmem_st32(s_tm, pk);
       tc::tmem_wait_st();
-      if (pos0 + kTileKeys > L) {
+      if (x == 0 && pos0 + kTileKeys > L) {
         // value rows at or past the sequence end: zero them (whole 128-byte
-        // rows, so the swizzle does not matter) before P V reads them
+        // rows, so the swizzle does not matter) before P V reads them; tile
+        // A's P V is the first reader of this V tile
         if (!(ok = wait_all(v_full + (j & 1), (j >> 1) & 1))) break;
         const int first = L - pos0;  // >= 1
         const int chunks = (kTileKeys - first) * Lay::NH * 8;
@@ -350,16 +368,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int idx = r; idx < chunks; idx += kRows) {
           const int rowi = first + idx / (Lay::NH * 8);
           const int h = (idx / 8) % Lay::NH;
-          const int ch = idx % 8;
-          *reinterpret_cast<uint4*>(vt + h * Lay::KV_HALF + rowi * 128 + ch * 16) =
+          const int chk = idx % 8;
+          *reinterpret_cast<uint4*>(vt + h * Lay::KV_HALF + rowi * 128 + chk * 16) =
               make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
       tc::fence_before_sync();
-      mbar_arrive(p_ready + (j & 1));
+      mbar_arrive(p_ready + x);
     }
-    if (ok) ok = wait_all(o_done, (n_tiles - 1) & 1);
+    if (ok) ok = wait_all(o_done + x, (n_tiles - 1) & 1);
     if (ok) {
       tc::fence_after_sync();
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -367,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll 1
       for (int ch = 0; ch < HD / 32; ++ch) {
         uint32_t ov[32];
-        tc::tmem_ld32(o_tm + lane_base + ch * 32, ov);
+        tc::tmem_ld32(o_tm(x) + lane_base + ch * 32, ov);
         tc::tmem_wait_ld();
         if (active) {
           uint32_t pkd[16];
@@ -461,8 +479,8 @@ cudaError_t run_tc(const AttnArgs& a, cudaStream_t stream) {
   static KernelSetup setup;
   const cudaError_t e = kernel_setup(setup, kern, Lay::REQUEST, kThreads, nullptr);
   if (e != cudaSuccess) return e;
-  const int tiles = (a.max_q_len + p.q_per_tile - 1) / p.q_per_tile;
-  dim3 grid(tiles, pool.n_kv, a.num_seqs);
+  const int pairs = (a.max_q_len + 2 * p.q_per_tile - 1) / (2 * p.q_per_tile);
+  dim3 grid(pairs, pool.n_kv, a.num_seqs);
   kern<<<grid, kThreads, Lay::REQUEST, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
