@@ -12,9 +12,10 @@
 // head of the GQA group and both tiles.  Keys go in tiles of 128 (eight
 // 16-token blocks).
 //
-//  warp 8    TMA producer: Q_A and Q_B once (64-column halves, 128-byte
-//            swizzle), then per key tile one 16-row box per block and half
-//            for K and for V into a two-stage ring.
+//  warp 8    TMA producer for Q_A and Q_B (once; 64-column halves, 128-byte
+//            swizzle) and K: per key tile one 16-row box per block and half
+//            into a three-stage ring, so K runs two tiles ahead of the MMAs;
+//  warp 10   TMA producer for V into a two-stage ring.
 //  warp 9    allocates all 512 TMEM columns (S_A, S_B, O_A, O_B) and one
 //            lane issues the MMAs in ping-pong order:
 //               S_A = Q_A K_j^T, S_B = Q_B K_j^T, then for each tile once its
@@ -50,9 +51,12 @@ constexpr int kRows = 128;       // MMA rows per tile
 constexpr int kTileKeys = 128;   // keys per S tile
 constexpr int kBlk = 16;         // tokens per pool block
 constexpr int kBlocksPerTile = kTileKeys / kBlk;
-constexpr int kProducerWarp = 8;
+constexpr int kProducerWarp = 8;   // Q and K
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kVProducerWarp = 10;  // V
+constexpr int kThreads = 11 * 32;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows past 2^8
 constexpr uint32_t kTmemCols = 512;  // S_A [0,128) S_B [128,256) O_A [256,..) O_B [384,..)
@@ -73,10 +77,10 @@ struct Layout {
   static constexpr int Q_HALF = kRows * 128;            // 16 KB
   static constexpr int KV_HALF = kTileKeys * 128;       // 16 KB
   static constexpr int Q_TILE = NH * Q_HALF;
-  static constexpr int K_OFF = 2 * Q_TILE;              // stage s: K at K_OFF + s*STAGE
-  static constexpr int STAGE = 2 * NH * KV_HALF;        // K then V
-  static constexpr int V_IN_STAGE = NH * KV_HALF;
-  static constexpr int BAR_OFF = K_OFF + 2 * STAGE;
+  static constexpr int KV_TILE = NH * KV_HALF;
+  static constexpr int K_OFF = 2 * Q_TILE;               // K stage s at K_OFF + s * KV_TILE
+  static constexpr int V_OFF = K_OFF + kKStages * KV_TILE;
+  static constexpr int BAR_OFF = V_OFF + kVStages * KV_TILE;
   static constexpr int BYTES = BAR_OFF + 256;
   // + 1 KB alignment slack; at least 120 KB so only one CTA fits per SM (it
   // takes all 512 TMEM columns)
@@ -121,24 +125,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [2] per stage
-  uint64_t* v_full = bars + 3;    // [2] per stage
-  uint64_t* kv_empty = bars + 5;  // [2] per stage
-  uint64_t* s_full = bars + 7;    // [2] per tile A/B
-  uint64_t* p_ready = bars + 9;   // [2] per tile A/B
-  uint64_t* o_done = bars + 11;   // [2] per tile A/B
-  uint64_t* drain = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* k_full = bars + 1;    // [3] per K stage
+  uint64_t* k_empty = bars + 4;   // [3]
+  uint64_t* v_full = bars + 7;    // [2] per V stage
+  uint64_t* v_empty = bars + 9;   // [2]
+  uint64_t* s_full = bars + 11;   // [2] per tile A/B
+  uint64_t* p_ready = bars + 13;  // [2] per tile A/B
+  uint64_t* o_done = bars + 15;   // [2] per tile A/B
+  uint64_t* drain = bars + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(k_full + i, 1);
+      mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(v_full + i, 1);
-      mbar_init(kv_empty + i, 1);
+      mbar_init(v_empty + i, 1);
       mbar_init(s_full + i, 1);
       mbar_init(p_ready + i, kRows);
       mbar_init(o_done + i, 1);
@@ -156,14 +164,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   auto q_tile = [&](int x) { return smem + x * Lay::Q_TILE; };
-  auto k_st = [&](int st) { return smem + Lay::K_OFF + st * Lay::STAGE; };
-  auto v_st = [&](int st) { return smem + Lay::K_OFF + st * Lay::STAGE + Lay::V_IN_STAGE; };
+  auto k_st = [&](int j) { return smem + Lay::K_OFF + (j % kKStages) * Lay::KV_TILE; };
+  auto v_st = [&](int j) { return smem + Lay::V_OFF + (j % kVStages) * Lay::KV_TILE; };
   auto s_tm = [&](int x) { return tmem + uint32_t(x) * kTileKeys; };
   auto o_tm = [&](int x) { return tmem + 256u + uint32_t(x) * 128u; };
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp == kProducerWarp || warp == kVProducerWarp) {
+    // ---------------------------------------------------------- producers
+    const bool is_k = warp == kProducerWarp;
+    const int nst = is_k ? kKStages : kVStages;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    const CUtensorMap* map = is_k ? &tk : &tv;
+    if (is_k && lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * Lay::Q_TILE);
       for (int x = 0; x < 2; ++x)
         for (int h = 0; h < Lay::NH; ++h)
@@ -175,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ids = 0;  // lane l holds the id of block (j / 4) * 32 + l
     for (int j = 0; j < n_tiles; ++j) {
       if (*abort_flag) break;
-      const int st = j & 1;
-      const uint32_t use = j >> 1;
+      const int st = j % nst;
+      const uint32_t use = j / nst;
       if ((j & 3) == 0) {
         const int jb32 = j * kBlocksPerTile + lane;
         ids = jb32 < n_blocks_seq ? __ldg(row + jb32) : 0;
@@ -188,38 +201,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (load) {
         blk = blk_l;
         if (blk < 0 || blk >= p.num_blocks) {
-          report(p.err, PKV_DEVERR_BLOCK_ID);
+          if (is_k) report(p.err, PKV_DEVERR_BLOCK_ID);
           load = false;
         }
       }
       const uint32_t nload = __popc(__ballot_sync(0xffffffffu, load));
-      if (use > 0 && !wait_all(kv_empty + st, (use - 1) & 1)) {
+      if (use > 0 && !wait_all(empty + st, (use - 1) & 1)) {
         if (lane == 0) {
           report(p.err, PKV_DEVERR_TIMEOUT);
           *abort_flag = 1;
         }
         break;
       }
-      const uint32_t bytes = nload * Lay::NH * kBlk * 128;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(k_full + st, bytes);
-        mbar_arrive_expect_tx(v_full + st, bytes);
-      }
+      if (lane == 0) mbar_arrive_expect_tx(full + st, nload * Lay::NH * kBlk * 128);
       __syncwarp();
       if (load) {
-        for (int h = 0; h < Lay::NH; ++h) {
-          const int off = h * Lay::KV_HALF + lane * kBlk * 128;
-          tc::tma_load_3d(k_st(st) + off, &tk, h * 64, g, blk * kBlk, k_full + st);
-          tc::tma_load_3d(v_st(st) + off, &tv, h * 64, g, blk * kBlk, v_full + st);
-        }
+        uint8_t* dst = is_k ? k_st(j) : v_st(j);
+        for (int h = 0; h < Lay::NH; ++h)
+          tc::tma_load_3d(dst + h * Lay::KV_HALF + lane * kBlk * 128, map, h * 64, g, blk * kBlk,
+                          full + st);
       }
       ++issued;
     }
     if (*abort_flag) {  // let copies in flight land before the CTA exits
-      for (int j = max(0, issued - 2); j < issued; ++j) {
-        mbar_wait(k_full + (j & 1), (j >> 1) & 1);
-        mbar_wait(v_full + (j & 1), (j >> 1) & 1);
-      }
+      for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(full + j % nst, (j / nst) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, HD, false, true);
       auto issue_qk = [&](int x, int j) {
         const uint32_t q_addr = smem_addr(q_tile(x));
-        const uint32_t k_addr = smem_addr(k_st(j & 1));
+        const uint32_t k_addr = smem_addr(k_st(j));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off_q = (kk >> 2) * Lay::Q_HALF + (kk & 3) * 32;
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(s_full + x);
       };
       auto issue_pv = [&](int x, int j) {
-        const uint32_t v_addr = smem_addr(v_st(j & 1));
+        const uint32_t v_addr = smem_addr(v_st(j));
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; ++kk) {
           // 16 keys = two 8-row groups of the V tile; P: 16 bf16 = 8 columns
@@ -254,18 +259,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         issue_qk(0, 0);
         issue_qk(1, 0);
+        tc::commit(k_empty);  // K_0 is no longer read
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const bool more = j + 1 < n_tiles;
+        const int kn = (j + 1) % kKStages;
         for (int x = 0; x < 2 && ok; ++x) {
           if (!(ok = mbar_wait(p_ready + x, j & 1))) break;
-          if (x == 0 && !(ok = mbar_wait(v_full + (j & 1), (j >> 1) & 1))) break;
-          if (x == 0 && more && !(ok = mbar_wait(k_full + ((j + 1) & 1), ((j + 1) >> 1) & 1)))
-            break;
+          if (x == 0 && !(ok = mbar_wait(v_full + (j % kVStages), (j / kVStages) & 1))) break;
+          if (x == 0 && more && !(ok = mbar_wait(k_full + kn, ((j + 1) / kKStages) & 1))) break;
           tc::fence_after_sync();
           issue_pv(x, j);
-          if (x == 1) tc::commit(kv_empty + (j & 1));  // K_j and V_j are no longer read
+          if (x == 1) tc::commit(v_empty + (j % kVStages));  // V_j is no longer read
           if (more) issue_qk(x, j + 1);
+          if (x == 1 && more) tc::commit(k_empty + kn);      // K_{j+1} is no longer read
         }
       }
       if (!ok) {
@@ -361,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // value rows at or past the sequence end: zero them (whole 128-byte
         // rows, so the swizzle does not matter) before P V reads them; tile
         // A's P V is the first reader of this V tile
-        if (!(ok = wait_all(v_full + (j & 1), (j >> 1) & 1))) break;
+        if (!(ok = wait_all(v_full + (j % kVStages), (j / kVStages) & 1))) break;
         const int first = L - pos0;  // >= 1
         const int chunks = (kTileKeys - first) * Lay::NH * 8;
-        uint8_t* vt = v_st(j & 1);
+        uint8_t* vt = v_st(j);
         for (int idx = r; idx < chunks; idx += kRows) {
           const int rowi = first + idx / (Lay::NH * 8);
           const int h = (idx / 8) % Lay::NH;
