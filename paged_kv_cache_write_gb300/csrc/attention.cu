@@ -465,15 +465,42 @@ struct DecodeParams {
   int32_t* err;
   int32_t* cu_units;  // [B+1] units (16-token blocks x head groups) before each sequence
   int4* starts;       // [grid] each CTA's first segment: (sequence, head group, block, -)
-  int32_t* bounds;    // [grid + 1] first unit of each CTA's range (bounds[grid] = total)
-  int4* splits;       // [grid] split groups: (sequence, head group, first CTA, last CTA)
-  int32_t* n_splits;  // number of entries in splits
+  int4* splits;       // [grid] per CTA: the split group it merges (sequence, head group,
+                      // first CTA, last CTA), sequence = -1 if none
+  int32_t* total_units;  // one int: units of the whole batch
   float* ws_o;        // [2 * grid][HG * rep][HD] partial outputs
   float* ws_ml;       // [2 * grid][HG * rep][2] partial max (log2 units) and exp-sum
   int B, n_heads, n_kv, rep, hg_size, n_groups, W, num_blocks, max_len, max_seq_len, head_dim;
   int elem_bytes, nstages, grid;
+  int plan_in_kernel;  // 1: each CTA scans the lengths itself (no plan kernel)
   float scale_log2;
 };
+
+// Exclusive prefix sum of `local` over the CTA's threads in thread order;
+// every thread calls it.  warp_tot: 32 ints of shared memory.
+__device__ __forceinline__ int cta_exclusive_scan(int local, int* warp_tot) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += y;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  return incl - local + (wid > 0 ? warp_tot[wid - 1] : 0);
+}
 
 // Length used for sequence b: seq_lens[b] clamped to [0, max_len]
 // (max_len = min(max_seq_len, table width * 16)).
@@ -492,9 +519,12 @@ __device__ __forceinline__ int seq_of_unit(const int32_t* cu, int B, int u) {
   return lo;
 }
 
-// First unit of CTA c's range when U units are split evenly over G CTAs.
-__device__ __forceinline__ int range_begin(int64_t c, int64_t U, int64_t G) {
-  return static_cast<int>((c * U) / G);
+// First unit of CTA c's range when U units are split evenly over G CTAs
+// (32-bit division when the product fits).
+__device__ __forceinline__ int range_begin(int c, int U, int G) {
+  const uint64_t n = uint64_t(uint32_t(c)) * uint32_t(U);
+  if (n <= 0xffffffffull) return static_cast<int>(uint32_t(n) / uint32_t(G));
+  return static_cast<int>(n / uint64_t(G));
 }
 
 // Owner CTA of unit u: the largest c with range_begin(c) <= u.
@@ -514,12 +544,67 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // Wait until the preceding kernel has finished and its writes are visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// One CTA: exclusive scan of units per sequence, each CTA's first segment,
-// zero outputs for empty sequences; reports bad
-// lengths once.  The scan is kept in shared memory (when it fits) for the
-// per-CTA searches.
+// Plan for batches too large for the main kernel's own scan: one CTA
+// computes the exclusive scan of units per sequence, each CTA's first
+// segment and the batch total, zeroes outputs of empty sequences and
+// reports bad lengths once.
 constexpr int kPlanSmemSeqs = 8191;
-constexpr int kPlanSmemGrid = 2431;
+// Batches up to this size are planned by every main-kernel CTA itself.
+constexpr int kKernelPlanSeqs = 2048;
+
+// Units (16-token blocks x head groups) of sequence b.
+__device__ __forceinline__ int units_of(const DecodeParams& p, int b) {
+  return p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
+}
+
+__device__ __forceinline__ void check_length(const DecodeParams& p, int b) {
+  const int L = __ldg(p.seq_lens + b);
+  if (L < 0 || L > p.max_seq_len) report(p.err, PKV_DEVERR_LENGTH);
+  else if (L > p.W * kBS) report(p.err, PKV_DEVERR_TABLE_WIDTH);
+}
+
+// The split group CTA c merges.  CTA c's range starts at block j of head
+// group grp of sequence b (nblk blocks per group).  If j > 0 the group is
+// split, and c merges it when c is the first non-empty CTA to start inside
+// it.  Entry: (b, grp, first CTA | last CTA << 16, first unit of the
+// group); b = -1 when c merges nothing.
+__device__ __forceinline__ int4 split_entry(int c, int G, int U, int b, int grp, int j,
+                                            int nblk) {
+  if (j == 0) return make_int4(-1, 0, 0, 0);
+  const int a = range_begin(c, U, G) - j;  // the group's first unit
+  int lo = 0, hi = c;  // owner of unit a: largest c' with range_begin(c') <= a
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (range_begin(mid, U, G) <= a) lo = mid; else hi = mid;
+  }
+  const int c0 = lo;
+  int first = c0 + 1;  // CTAs between c0 and c with an empty range start nowhere
+  while (range_begin(first + 1, U, G) == range_begin(first, U, G)) ++first;
+  if (first != c) return make_int4(-1, 0, 0, 0);
+  const int e = a + nblk - 1;  // owner of the group's last unit
+  lo = c;
+  hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (range_begin(mid, U, G) <= e) lo = mid; else hi = mid;
+  }
+  return make_int4(b, grp, c0 | (lo << 16), a);
+}
+
+// Zero the output rows of empty sequences b = first, first + stride, ...;
+// the CTA's warps share them.  empty(b) tells whether b has no tokens.
+template <typename T, int HD, typename Empty>
+__device__ __forceinline__ void zero_empty(const DecodeParams& p, int first, int stride,
+                                           Empty empty) {
+  T* out = static_cast<T*>(p.out);
+  const int row_elems = p.n_heads * HD;
+  const int lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  for (int b = first + int(threadIdx.x >> 5) * stride; b < p.B; b += nw * stride) {
+    if (!empty(b)) continue;
+    for (int i = lane; i < row_elems; i += 32) out[int64_t(b) * row_elems + i] = Elem<T>::from_f(0.f);
+  }
+}
 
 template <typename T, int HD>
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
@@ -534,99 +619,32 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   const int b1 = min(p.B, b0 + chunk);
   int local = 0;
   for (int b = b0; b < b1; ++b) {
-    const int L = __ldg(p.seq_lens + b);
-    if (L < 0 || L > p.max_seq_len) report(p.err, PKV_DEVERR_LENGTH);
-    else if (L > p.W * kBS) report(p.err, PKV_DEVERR_TABLE_WIDTH);
-    local += p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
+    check_length(p, b);
+    local += units_of(p, b);
   }
-  const int lane = tid & 31, wid = tid >> 5;
-  int incl = local;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
-  }
-  if (lane == 31) warp_tot[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    int t = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, t, off);
-      if (lane >= off) t += y;
-    }
-    warp_tot[lane] = t;  // inclusive over warps
-  }
-  __syncthreads();
-  int run = incl - local + (wid > 0 ? warp_tot[wid - 1] : 0);
+  int run = cta_exclusive_scan(local, warp_tot);
   for (int b = b0; b < b1; ++b) {
-    const int nb = p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
     cu[b] = run;
-    if (in_smem) p.cu_units[b] = run;
-    run += nb;
+    run += units_of(p, b);
   }
   if (tid == blockDim.x - 1) {
     cu[p.B] = run;
-    if (in_smem) p.cu_units[p.B] = run;
+    *p.total_units = run;
   }
   __syncthreads();  // the prefix is complete (same CTA: visible after the barrier)
   const int U = cu[p.B];
-  __shared__ int rb_s[kPlanSmemGrid + 1];
-  __shared__ int n_split_s;
-  const bool rb_in_smem = p.grid <= kPlanSmemGrid;
-  int* rb = rb_in_smem ? rb_s : p.bounds;
-  if (tid == 0) n_split_s = 0;
-  for (int c = tid; c <= p.grid; c += blockDim.x) {
-    const int v = range_begin(c, U, p.grid);
-    rb[c] = v;
-    if (rb_in_smem) p.bounds[c] = v;
-  }
-  __syncthreads();
   for (int c = tid; c < p.grid; c += blockDim.x) {
-    const int r0 = rb[c];
+    const int r0 = range_begin(c, U, p.grid);
     int4 st = make_int4(0, 0, 0, 0);
-    if (r0 < rb[c + 1]) {
+    if (r0 < range_begin(c + 1, U, p.grid)) {
       const int b = seq_of_unit(cu, p.B, r0);
-      const int base = cu[b];
       const int nblk = (used_len(p, b) + kBS - 1) / kBS;
-      const int grp = (r0 - base) / nblk;
-      const int j = (r0 - base) - grp * nblk;
-      st = make_int4(b, grp, j, 0);
-      if (j > 0) {
-        // CTA c begins inside a group: if it is the first CTA to do so, the
-        // group is split and listed once, with its first and last CTA
-        const int a = r0 - j;
-        int lo = 0, hi = p.grid;  // owner of unit a: largest c' with rb[c'] <= a
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (rb[mid] <= a) lo = mid; else hi = mid;
-        }
-        const int c0 = lo;
-        int first = c0 + 1;
-        while (rb[first + 1] == rb[first]) ++first;
-        if (first == c) {
-          const int e = a + nblk - 1;  // owner of the group's last unit
-          lo = c;
-          hi = p.grid;
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (rb[mid] <= e) lo = mid; else hi = mid;
-          }
-          p.splits[atomicAdd(&n_split_s, 1)] = make_int4(b, grp, c0, lo);
-        }
-      }
+      const int grp = (r0 - cu[b]) / nblk;
+      st = make_int4(b, grp, (r0 - cu[b]) - grp * nblk, 0);
     }
     p.starts[c] = st;
   }
-  __syncthreads();
-  if (tid == 0) *p.n_splits = n_split_s;
-  // empty sequences get a zero output (no CTA owns any of their units)
-  T* out = static_cast<T*>(p.out);
-  const int row_elems = p.n_heads * HD;
-  for (int b = wid; b < p.B; b += blockDim.x >> 5) {
-    if (used_len(p, b) != 0) continue;
-    for (int i = lane; i < row_elems; i += 32) out[int64_t(b) * row_elems + i] = Elem<T>::from_f(0.f);
-  }
+  zero_empty<T, HD>(p, 0, 1, [&](int b) { return used_len(p, b) == 0; });
 }
 
 // Walks this CTA's contiguous range of units segment by segment: a segment
@@ -666,8 +684,9 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeEpt = 32;  // rows * head_dim <= 8192 = 256 threads x 32
 
 template <typename T, int HD>
-__device__ void merge_group(const DecodeParams& p, int b, int grp, int a, int c0, int c1,
+__device__ void merge_group(const DecodeParams& p, int b, int grp, int a, int c0, int c1, int U,
                             float* scratch) {
+  const int G = p.grid;
   const int rows = p.hg_size * p.rep;
   const int E = rows * HD;
   float* m_s = scratch;                   // [rows][kMergeParts]
@@ -691,8 +710,8 @@ __device__ void merge_group(const DecodeParams& p, int b, int grp, int a, int c0
       bool has = false;
       int lo = 0;
       if (t < kMergeParts && c <= c1) {
-        lo = __ldcg(p.bounds + c);
-        has = __ldcg(p.bounds + c + 1) > lo;
+        lo = range_begin(c, U, G);
+        has = range_begin(c + 1, U, G) > lo;
       }
       const unsigned m = __ballot_sync(0xffffffffu, has);
       if (has) slot_s[__popc(m & ((1u << t) - 1))] = (c == c0 && lo != a) ? 2 * c + 1 : 2 * c;
@@ -771,19 +790,59 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
   const int row_bytes = p.hg_size * HD * p.elem_bytes;
   Ring ring = make_ring(smem, p.nstages, row_bytes);
   ring_init(ring, consumers);
-  pdl_wait();  // the plan kernel's work prefix and starts
+  pdl_wait();  // inputs written by the preceding kernel (the plan, when there is one)
   pdl_launch_dependents();  // the merge kernel may be scheduled (it waits for this grid)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int U = __ldcg(p.cu_units + p.B);
   const int G = gridDim.x;
+  int U;
+  int4 st = make_int4(0, 0, 0, 0);
+  if (p.plan_in_kernel) {
+    // Scan the units per sequence in the (still unused) ring stages.
+    int* cu_s = reinterpret_cast<int*>(ring.stages);  // [B + 1]
+    int* warp_tot = cu_s + p.B + 1;                    // [32]
+    const int nt = blockDim.x;
+    for (int b = threadIdx.x; b < p.B; b += nt) {
+      if (blockIdx.x == 0) check_length(p, b);
+      cu_s[b] = units_of(p, b);
+    }
+    __syncthreads();
+    const int chunk = (p.B + nt - 1) / nt;
+    const int b0 = min(p.B, int(threadIdx.x) * chunk);
+    const int b1 = min(p.B, b0 + chunk);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) local += cu_s[b];
+    int run = cta_exclusive_scan(local, warp_tot);
+    for (int b = b0; b < b1; ++b) {
+      const int n = cu_s[b];
+      cu_s[b] = run;
+      run += n;
+    }
+    if (threadIdx.x == nt - 1) cu_s[p.B] = run;
+    __syncthreads();
+    U = cu_s[p.B];
+    const int r0 = range_begin(blockIdx.x, U, G);
+    if (r0 < range_begin(blockIdx.x + 1, U, G)) {
+      const int b = seq_of_unit(cu_s, p.B, r0);
+      const int nblk = (used_len(p, b) + kBS - 1) / kBS;
+      const int grp = (r0 - cu_s[b]) / nblk;
+      st = make_int4(b, grp, (r0 - cu_s[b]) - grp * nblk, 0);
+    }
+    zero_empty<T, HD>(p, blockIdx.x, G, [&](int b) { return cu_s[b + 1] == cu_s[b]; });
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.total_units = U;
+    fence_proxy_async_smem();  // the scan's stores come before the ring's copies
+    __syncthreads();
+  } else {
+    U = __ldcg(p.total_units);
+    st = __ldcg(p.starts + blockIdx.x);
+  }
   const int r0 = range_begin(blockIdx.x, U, G);
   const int r1 = range_begin(blockIdx.x + 1, U, G);
   const int64_t token_pitch = int64_t(p.n_kv) * HD * p.elem_bytes;  // bytes per pool slot
   const int rows_per_group = p.hg_size * p.rep;
   Cursor cur;
-  if (r0 < r1) cur.load(p, __ldcg(p.starts + blockIdx.x));
+  if (r0 < r1) cur.load(p, st);
 
   if (warp == consumers) {
     // ------------------------------------------------------ producer
@@ -818,6 +877,12 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
       cur.advance(p, n);
     }
     if (!ok) ring_drain(ring, it);
+    // the split group this CTA merges (read by the merge kernel)
+    if (lane == 0) {
+      p.splits[blockIdx.x] = r0 < r1 ? split_entry(blockIdx.x, G, U, st.x, st.y, st.z,
+                                                   (used_len(p, st.x) + kBS - 1) / kBS)
+                                     : make_int4(-1, 0, 0, 0);
+    }
   } else if (warp < consumers) {
     // ------------------------------------------------------ consumers
     Rows rows;
@@ -1022,17 +1087,18 @@ int stages_for(int stage_bytes, int scratch_bytes, int target_bytes) {
   return ns;
 }
 
-// Merge of the split groups listed by the plan kernel, one CTA each.
+// Merge of the split groups, one CTA per main-kernel CTA: CTA c merges the
+// group main-kernel CTA c recorded, if any.
 // Launched as a programmatic dependent of the main kernel.
 template <typename T, int HD>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
   extern __shared__ __align__(16) float merge_smem[];
-  pdl_wait();  // the main kernel's partials
-  if (static_cast<int>(blockIdx.x) >= __ldcg(p.n_splits)) return;
-  const int4 sp = __ldcg(p.splits + blockIdx.x);  // (sequence, head group, first CTA, last CTA)
-  const int nblk = (used_len(p, sp.x) + kBS - 1) / kBS;
-  const int a = __ldcg(p.cu_units + sp.x) + sp.y * nblk;
-  merge_group<T, HD>(p, sp.x, sp.y, a, sp.z, sp.w, merge_smem);
+  pdl_wait();  // the main kernel's partials and split entries
+  const int4 sp = __ldcg(p.splits + blockIdx.x);
+  if (sp.x < 0) return;
+  const uint32_t ctas = static_cast<uint32_t>(sp.z);
+  merge_group<T, HD>(p, sp.x, sp.y, sp.w, int(ctas & 0xffffu), int(ctas >> 16),
+                     __ldcg(p.total_units), merge_smem);
 }
 
 // Shared memory merge_group needs for one group.
@@ -1040,19 +1106,18 @@ size_t merge_smem_bytes(int rows, int) {
   return (2 * size_t(rows) * kMergeParts + 3 * size_t(rows)) * 4 + (kMergeParts + 1) * 4;
 }
 
-// Decode workspace layout: cu_units [B+1] | starts [G] | bounds [G+1] |
-// splits [G] | n_splits | partial max/sum [2G][rows][2] | partial outputs
+// Decode workspace layout: cu_units [B+1] | starts [G] | splits [G] |
+// total units | partial max/sum [2G][rows][2] | partial outputs
 // [2G][rows][HD], each region 256-byte aligned.
 struct DecodeWs {
-  size_t cu, starts, bounds, splits, n_splits, ml, o, total;
+  size_t cu, starts, splits, total_units, ml, o, total;
   DecodeWs(int num_seqs, size_t G, size_t rows_per_group, int head_dim) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     cu = 0;
     starts = up(size_t(num_seqs + 1) * 4);
-    bounds = starts + up(G * 16);
-    splits = bounds + up((G + 1) * 4);
-    n_splits = splits + up(G * 16);
-    ml = n_splits + 256;
+    splits = starts + up(G * 16);
+    total_units = splits + up(G * 16);
+    ml = total_units + 256;
     o = ml + up(2 * G * rows_per_group * 2 * 4);
     total = o + 2 * G * rows_per_group * size_t(head_dim) * 4;
   }
@@ -1110,21 +1175,27 @@ struct DecodeLaunch {
     size_t smem = 0;
     cudaError_t e = grid(a, hg, &G, &smem, &p.nstages);
     if (e != cudaSuccess) return e;
+    if (G > 65535) return cudaErrorInvalidValue;  // split entries pack CTA indices in 16 bits
     p.grid = G;
     const DecodeWs L(a.num_seqs, G, size_t(hg) * p.rep, HD);
     if (L.total > a.workspace_bytes) return cudaErrorInvalidValue;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     p.cu_units = reinterpret_cast<int32_t*>(ws + L.cu);
     p.starts = reinterpret_cast<int4*>(ws + L.starts);
-    p.bounds = reinterpret_cast<int32_t*>(ws + L.bounds);
     p.splits = reinterpret_cast<int4*>(ws + L.splits);
-    p.n_splits = reinterpret_cast<int32_t*>(ws + L.n_splits);
+    p.total_units = reinterpret_cast<int32_t*>(ws + L.total_units);
     p.ws_ml = reinterpret_cast<float*>(ws + L.ml);
     p.ws_o = reinterpret_cast<float*>(ws + L.o);
-    decode_plan_kernel<T, HD><<<1, 1024, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // the main kernel may start while the plan kernel runs: it waits for
-    // the plan's results (griddepcontrol.wait) after its prologue
+    // small batches: every CTA scans the lengths in its ring stages
+    const size_t ring_bytes = smem - kBarrierBytes - scratch_bytes(hg);
+    p.plan_in_kernel =
+        a.num_seqs <= kKernelPlanSeqs && size_t(a.num_seqs + 1 + 32) * 4 <= ring_bytes;
+    if (!p.plan_in_kernel) {
+      decode_plan_kernel<T, HD><<<1, 1024, 0, stream>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // the main kernel may start while the preceding kernel runs: it waits
+    // for that kernel's results (griddepcontrol.wait) after its prologue
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3((hg + 1) * 32);
