@@ -527,17 +527,7 @@ __device__ __forceinline__ int range_begin(int c, int U, int G) {
   return static_cast<int>(n / uint64_t(G));
 }
 
-// Owner CTA of unit u: the largest c with range_begin(c) <= u.
-__device__ __forceinline__ int owner_of(int u, int U, int G) {
-  int lo = 0, hi = G;  // answer in [lo, hi)
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (range_begin(mid, U, G) <= u) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-// Let the dependent launch (the main decode kernel) start its prologue.
+// Let the programmatic dependent launch start its prologue.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -674,105 +664,26 @@ struct Cursor {
   }
 };
 
-// Merge the partial results of one (sequence, head group) that several
-// CTAs computed: out = sum_c w_c o_c / sum_c w_c with w_c = exp2(m_c - M) l_c.
-// Parts are taken kMergeParts at a time with a running maximum, so any
-// number works.  Each thread keeps its (at most kMergeEpt) outputs in
-// registers and issues the loads of one part for all of them together.
-constexpr int kMergeParts = 8;
+// Merge of split groups: out = sum_c w_c o_c / sum_c w_c over the CTAs c
+// that computed parts of one (sequence, head group), w_c = exp2(m_c - M) l_c.
+// One thread copies the parts' partial outputs (rows x head_dim fp32 each)
+// into shared memory with bulk copies, all in flight together, while the
+// CTA loads their max / sum pairs; parts are taken up to
+// merge_parts_per_round at a time with a running maximum, so any number
+// works.
 constexpr int kMergeThreads = 256;
-constexpr int kMergeEpt = 32;  // rows * head_dim <= 8192 = 256 threads x 32
+constexpr int kMergeMaxParts = 16;           // parts per round (one warp's ballot)
+constexpr int kMergeSmemBudget = 128 * 1024;  // partial outputs staged per round
+constexpr int kMergeVec = 8;  // float4 per thread: rows * head_dim <= 8192 = 256 x 8 x 4
 
-template <typename T, int HD>
-__device__ void merge_group(const DecodeParams& p, int b, int grp, int a, int c0, int c1, int U,
-                            float* scratch) {
-  const int G = p.grid;
-  const int rows = p.hg_size * p.rep;
-  const int E = rows * HD;
-  float* m_s = scratch;                   // [rows][kMergeParts]
-  float* w_s = m_s + rows * kMergeParts;  // [rows][kMergeParts]
-  float* M_s = w_s + rows * kMergeParts;  // [rows]
-  float* den_s = M_s + rows;              // [rows]
-  float* alpha_s = den_s + rows;          // [rows]
-  int* slot_s = reinterpret_cast<int*>(alpha_s + rows);  // [kMergeParts + 1]
-  const int t = threadIdx.x;
-  float acc[kMergeEpt];
-#pragma unroll
-  for (int i = 0; i < kMergeEpt; ++i) acc[i] = 0.f;
-  for (int r = t; r < rows; r += kMergeThreads) {
-    M_s[r] = -INFINITY;
-    den_s[r] = 0.f;
-  }
-  for (int cs = c0; cs <= c1; cs += kMergeParts) {
-    __syncthreads();
-    if (t < 32) {  // the parts of CTAs cs .. cs+7 whose range is not empty
-      const int c = cs + t;
-      bool has = false;
-      int lo = 0;
-      if (t < kMergeParts && c <= c1) {
-        lo = range_begin(c, U, G);
-        has = range_begin(c + 1, U, G) > lo;
-      }
-      const unsigned m = __ballot_sync(0xffffffffu, has);
-      if (has) slot_s[__popc(m & ((1u << t) - 1))] = (c == c0 && lo != a) ? 2 * c + 1 : 2 * c;
-      if (t == 0) slot_s[kMergeParts] = __popc(m);
-    }
-    __syncthreads();
-    const int np = slot_s[kMergeParts];
-    if (np == 0) continue;
-    for (int i = t; i < rows * np; i += kMergeThreads) {
-      const int r = i / np, k = i - (i / np) * np;
-      const int64_t prow = int64_t(slot_s[k]) * rows + r;
-      m_s[r * kMergeParts + k] = __ldcg(p.ws_ml + prow * 2);
-      w_s[r * kMergeParts + k] = __ldcg(p.ws_ml + prow * 2 + 1);
-    }
-    __syncthreads();
-    for (int r = t; r < rows; r += kMergeThreads) {
-      float cm = -INFINITY;
-      for (int k = 0; k < np; ++k) cm = fmaxf(cm, m_s[r * kMergeParts + k]);
-      const float Mn = fmaxf(M_s[r], cm);
-      const float alpha = fast_exp2(M_s[r] - Mn);
-      float den = den_s[r] * alpha;
-      for (int k = 0; k < np; ++k) {
-        const float w = fast_exp2(m_s[r * kMergeParts + k] - Mn) * w_s[r * kMergeParts + k];
-        w_s[r * kMergeParts + k] = w;
-        den += w;
-      }
-      M_s[r] = Mn;
-      den_s[r] = den;
-      alpha_s[r] = alpha;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kMergeEpt; ++i) {
-      const int e = t + i * kMergeThreads;
-      if (e < E) acc[i] *= alpha_s[e / HD];
-    }
-    for (int k = 0; k < np; ++k) {
-      const float* po = p.ws_o + int64_t(slot_s[k]) * rows * HD;
-      float v[kMergeEpt];
-#pragma unroll
-      for (int i = 0; i < kMergeEpt; ++i) {
-        const int e = t + i * kMergeThreads;
-        v[i] = e < E ? __ldcg(po + e) : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < kMergeEpt; ++i) {
-        const int e = t + i * kMergeThreads;
-        if (e < E) acc[i] = fmaf(w_s[(e / HD) * kMergeParts + k], v[i], acc[i]);
-      }
-    }
-  }
-  __syncthreads();
-  T* out = static_cast<T*>(p.out) + (int64_t(b) * p.n_heads + grp * rows) * HD;
-#pragma unroll
-  for (int i = 0; i < kMergeEpt; ++i) {
-    const int e = t + i * kMergeThreads;
-    if (e < E) {
-      const float den = den_s[e / HD];
-      out[e] = Elem<T>::from_f(den > 0.f ? acc[i] / den : 0.f);
-    }
-  }
+__host__ __device__ inline int merge_parts_per_round(int rows, int hd) {
+  const int n = kMergeSmemBudget / (rows * hd * 4);
+  return n < 1 ? 1 : (n > kMergeMaxParts ? kMergeMaxParts : n);
+}
+// Bytes of the merge CTA's shared memory before the staged partial outputs.
+__host__ __device__ inline int merge_head_bytes(int rows, int parts) {
+  const int b = 16 + (kMergeMaxParts + 1) * 4 + (2 * rows * parts + 3 * rows) * 4;
+  return (b + 127) / 128 * 128;
 }
 
 // Largest decode CTA of an instantiation: one producer warp plus one warp
@@ -1088,22 +999,138 @@ int stages_for(int stage_bytes, int scratch_bytes, int target_bytes) {
 }
 
 // Merge of the split groups, one CTA per main-kernel CTA: CTA c merges the
-// group main-kernel CTA c recorded, if any.
-// Launched as a programmatic dependent of the main kernel.
+// group main-kernel CTA c recorded, if any.  Launched as a programmatic
+// dependent of the main kernel.
 template <typename T, int HD>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
-  extern __shared__ __align__(16) float merge_smem[];
+  extern __shared__ __align__(128) uint8_t merge_smem[];
+  const int t = threadIdx.x;
+  const int rows = p.hg_size * p.rep;
+  const int E = rows * HD;  // elements of one part
+  const int P = merge_parts_per_round(rows, HD);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(merge_smem);
+  int* slot_s = reinterpret_cast<int*>(merge_smem + 16);  // [kMergeMaxParts + 1]
+  float* m_s = reinterpret_cast<float*>(slot_s + kMergeMaxParts + 1);  // [rows][P]
+  float* w_s = m_s + rows * P;                                         // [rows][P]
+  float* M_s = w_s + rows * P;                                         // [rows]
+  float* den_s = M_s + rows;                                           // [rows]
+  float* alpha_s = den_s + rows;                                       // [rows]
+  float* o_s = reinterpret_cast<float*>(merge_smem + merge_head_bytes(rows, P));  // [P][E]
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
   pdl_wait();  // the main kernel's partials and split entries
   const int4 sp = __ldcg(p.splits + blockIdx.x);
   if (sp.x < 0) return;
-  const uint32_t ctas = static_cast<uint32_t>(sp.z);
-  merge_group<T, HD>(p, sp.x, sp.y, sp.w, int(ctas & 0xffffu), int(ctas >> 16),
-                     __ldcg(p.total_units), merge_smem);
+  const int U = __ldcg(p.total_units);
+  const int G = p.grid;
+  const int a = sp.w;  // the group's first unit
+  const int c0 = sp.z & 0xffff, c1 = static_cast<int>(static_cast<uint32_t>(sp.z) >> 16);
+  float4 acc[kMergeVec];
+#pragma unroll
+  for (int j = 0; j < kMergeVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = t; r < rows; r += kMergeThreads) {
+    M_s[r] = -INFINITY;
+    den_s[r] = 0.f;
+  }
+  uint32_t phase = 0;
+  for (int cs = c0; cs <= c1; cs += P) {
+    __syncthreads();  // the previous round's reads of the staging area are done
+    if (t < 32) {     // slots of the parts of CTAs cs .. cs+P-1 whose range is not empty
+      const int c = cs + t;
+      bool has = false;
+      int lo = 0;
+      if (t < P && c <= c1) {
+        lo = range_begin(c, U, G);
+        has = range_begin(c + 1, U, G) > lo;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, has);
+      // c0 holds the group's first units at the end of its range unless
+      // its range starts at the group (then they are its first segment)
+      if (has) slot_s[__popc(m & ((1u << t) - 1))] = (c == c0 && lo != a) ? 2 * c + 1 : 2 * c;
+      if (t == 0) slot_s[kMergeMaxParts] = __popc(m);
+    }
+    __syncthreads();
+    const int np = slot_s[kMergeMaxParts];
+    if (np == 0) continue;
+    if (t == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np * E * 4));
+      for (int k = 0; k < np; ++k)
+        bulk_copy_g2s(o_s + k * E, p.ws_o + int64_t(slot_s[k]) * E, static_cast<uint32_t>(E * 4),
+                      bar);
+    }
+    for (int i = t; i < rows * np; i += kMergeThreads) {
+      const int r = i / np, k = i - r * np;
+      const int64_t prow = int64_t(slot_s[k]) * rows + r;
+      m_s[r * P + k] = __ldcg(p.ws_ml + prow * 2);
+      w_s[r * P + k] = __ldcg(p.ws_ml + prow * 2 + 1);
+    }
+    __syncthreads();
+    for (int r = t; r < rows; r += kMergeThreads) {
+      float cm = -INFINITY;
+      for (int k = 0; k < np; ++k) cm = fmaxf(cm, m_s[r * P + k]);
+      const float Mn = fmaxf(M_s[r], cm);  // finite: every part saw at least one key
+      const float alpha = fast_exp2(M_s[r] - Mn);
+      float den = den_s[r] * alpha;
+      for (int k = 0; k < np; ++k) {
+        const float w = fast_exp2(m_s[r * P + k] - Mn) * w_s[r * P + k];
+        w_s[r * P + k] = w;
+        den += w;
+      }
+      M_s[r] = Mn;
+      den_s[r] = den;
+      alpha_s[r] = alpha;
+    }
+    const bool ok = mbar_wait(bar, phase);
+    phase ^= 1u;
+    if (__syncthreads_or(!ok)) {  // copies did not land: report, let them finish, stop
+      if (t == 0) {
+        report(p.err, PKV_DEVERR_TIMEOUT);
+        mbar_wait(bar, phase ^ 1u);
+      }
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < kMergeVec; ++j) {
+      const int e = (t + j * kMergeThreads) * 4;
+      if (e < E) {
+        const int r = e / HD;
+        const float al = alpha_s[r];
+        float4 x = make_float4(acc[j].x * al, acc[j].y * al, acc[j].z * al, acc[j].w * al);
+        for (int k = 0; k < np; ++k) {
+          const float w = w_s[r * P + k];
+          const float4 o = *reinterpret_cast<const float4*>(o_s + k * E + e);
+          x.x = fmaf(w, o.x, x.x);
+          x.y = fmaf(w, o.y, x.y);
+          x.z = fmaf(w, o.z, x.z);
+          x.w = fmaf(w, o.w, x.w);
+        }
+        acc[j] = x;
+      }
+    }
+  }
+  __syncthreads();
+  T* out = static_cast<T*>(p.out) + (int64_t(sp.x) * p.n_heads + sp.y * rows) * HD;
+#pragma unroll
+  for (int j = 0; j < kMergeVec; ++j) {
+    const int e = (t + j * kMergeThreads) * 4;
+    if (e < E) {
+      const float den = den_s[e / HD];
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      out[e + 0] = Elem<T>::from_f(acc[j].x * inv);
+      out[e + 1] = Elem<T>::from_f(acc[j].y * inv);
+      out[e + 2] = Elem<T>::from_f(acc[j].z * inv);
+      out[e + 3] = Elem<T>::from_f(acc[j].w * inv);
+    }
+  }
 }
 
-// Shared memory merge_group needs for one group.
-size_t merge_smem_bytes(int rows, int) {
-  return (2 * size_t(rows) * kMergeParts + 3 * size_t(rows)) * 4 + (kMergeParts + 1) * 4;
+// Shared memory of the merge kernel.
+size_t merge_smem_bytes(int rows, int hd) {
+  const int P = merge_parts_per_round(rows, hd);
+  return size_t(merge_head_bytes(rows, P)) + size_t(P) * rows * hd * 4;
 }
 
 // Decode workspace layout: cu_units [B+1] | starts [G] | splits [G] |
