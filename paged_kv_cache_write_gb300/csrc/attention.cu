@@ -556,8 +556,13 @@ __device__ __forceinline__ void check_length(const DecodeParams& p, int b) {
 // The split group CTA c merges.  CTA c's range starts at block j of head
 // group grp of sequence b (nblk blocks per group).  If j > 0 the group is
 // split, and c merges it when c is the first non-empty CTA to start inside
-// it.  Entry: (b, grp, first CTA | last CTA << 16, first unit of the
-// group); b = -1 when c merges nothing.
+// it.  Entry: (b, grp | flags, first CTA | last CTA << 16, first unit of
+// the group); b = -1 when c merges nothing.  Flags: kSplitC0Tail (the
+// first CTA's part is the last segment of its range, not its first) and
+// kSplitDense (every CTA has a non-empty range, U >= G).
+constexpr int kSplitC0Tail = 1 << 16;
+constexpr int kSplitDense = 1 << 17;
+
 __device__ __forceinline__ int4 split_entry(int c, int G, int U, int b, int grp, int j,
                                             int nblk) {
   if (j == 0) return make_int4(-1, 0, 0, 0);
@@ -578,7 +583,8 @@ __device__ __forceinline__ int4 split_entry(int c, int G, int U, int b, int grp,
     const int mid = (lo + hi) >> 1;
     if (range_begin(mid, U, G) <= e) lo = mid; else hi = mid;
   }
-  return make_int4(b, grp, c0 | (lo << 16), a);
+  const int flags = (range_begin(c0, U, G) != a ? kSplitC0Tail : 0) | (U >= G ? kSplitDense : 0);
+  return make_int4(b, grp | flags, c0 | (lo << 16), a);
 }
 
 // Zero the output rows of empty sequences b = first, first + stride, ...;
@@ -673,7 +679,9 @@ struct Cursor {
 // works.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeMaxParts = 16;           // parts per round (one warp's ballot)
-constexpr int kMergeSmemBudget = 128 * 1024;  // partial outputs staged per round
+// partial outputs staged per round; with the head this stays under 100 KB,
+// so a merge CTA fits on an SM beside a main-kernel CTA
+constexpr int kMergeSmemBudget = 96 * 1024;
 constexpr int kMergeVec = 8;  // float4 per thread: rows * head_dim <= 8192 = 256 x 8 x 4
 
 __host__ __device__ inline int merge_parts_per_round(int rows, int hd) {
@@ -1023,9 +1031,11 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   pdl_wait();  // the main kernel's partials and split entries
   const int4 sp = __ldcg(p.splits + blockIdx.x);
   if (sp.x < 0) return;
-  const int U = __ldcg(p.total_units);
+  const int grp = sp.y & 0xffff;
+  const bool c0_tail = (sp.y & kSplitC0Tail) != 0;
+  const bool dense = (sp.y & kSplitDense) != 0;
+  const int U = dense ? 0 : __ldcg(p.total_units);  // only sparse grids look at range starts
   const int G = p.grid;
-  const int a = sp.w;  // the group's first unit
   const int c0 = sp.z & 0xffff, c1 = static_cast<int>(static_cast<uint32_t>(sp.z) >> 16);
   float4 acc[kMergeVec];
 #pragma unroll
@@ -1039,16 +1049,12 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     __syncthreads();  // the previous round's reads of the staging area are done
     if (t < 32) {     // slots of the parts of CTAs cs .. cs+P-1 whose range is not empty
       const int c = cs + t;
-      bool has = false;
-      int lo = 0;
-      if (t < P && c <= c1) {
-        lo = range_begin(c, U, G);
-        has = range_begin(c + 1, U, G) > lo;
-      }
+      bool has = t < P && c <= c1;
+      if (has && !dense) has = range_begin(c + 1, U, G) > range_begin(c, U, G);
       const unsigned m = __ballot_sync(0xffffffffu, has);
       // c0 holds the group's first units at the end of its range unless
       // its range starts at the group (then they are its first segment)
-      if (has) slot_s[__popc(m & ((1u << t) - 1))] = (c == c0 && lo != a) ? 2 * c + 1 : 2 * c;
+      if (has) slot_s[__popc(m & ((1u << t) - 1))] = (c == c0 && c0_tail) ? 2 * c + 1 : 2 * c;
       if (t == 0) slot_s[kMergeMaxParts] = __popc(m);
     }
     __syncthreads();
@@ -1112,7 +1118,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     }
   }
   __syncthreads();
-  T* out = static_cast<T*>(p.out) + (int64_t(sp.x) * p.n_heads + sp.y * rows) * HD;
+  T* out = static_cast<T*>(p.out) + (int64_t(sp.x) * p.n_heads + grp * rows) * HD;
 #pragma unroll
   for (int j = 0; j < kMergeVec; ++j) {
     const int e = (t + j * kMergeThreads) * 4;
