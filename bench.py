@@ -3,8 +3,11 @@
 
 A step is one pass of the whole hot path over one batch: the slot mapping
 of the step's new tokens, and per layer the KV write, paged decode
-attention (plan + persistent split kernel + merge) and chunked-prefill
-attention.  The default workload is one layer of a LLaMA-2-70B-shaped
+attention (persistent split kernel + merge) and chunked-prefill attention.
+By default the decode rows' KV write is fused into the decode launch
+(pkv_paged_attention_decode_append), so the separate KV write and the slot
+mapping cover only the prefill chunks; --separate-write runs the plain
+write-then-decode sequence instead.  The default workload is one layer of a LLaMA-2-70B-shaped
 (GQA-8) mixed step: 256 decode sequences with log-normal lengths
 (median 1024, clipped to 16..8192) plus 4 prefill sequences each with a
 512-token causal chunk over 0..4096 tokens of paged history, in a pool of
@@ -67,6 +70,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every kernel from the host each step instead of replaying "
                          "the step as a CUDA graph")
+    ap.add_argument("--separate-write", action="store_true",
+                    help="write every new token with kv_write, then run plain decode "
+                         "(instead of the fused decode-with-append launch)")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers materialised per step (0 = the workload's own count)")
     return ap.parse_args(argv)
@@ -351,19 +357,31 @@ def run_gb300(args, rank, world, local):
 
     ev_dec, ev_pre = [], []
 
+    fused = not args.separate_write
+
     def step(timed=False, inputs=None):
         src_bt, src_sl, src_cu = (bt, seq_lens, cu_new) if inputs is None else inputs[:3]
-        pkv.slot_mapping(src_bt, src_sl, src_cu, T, sh.block_size, sh.num_blocks, out=slots, err=err)
+        if has_pre or not fused:
+            pkv.slot_mapping(src_bt, src_sl, src_cu, T, sh.block_size, sh.num_blocks, out=slots,
+                             err=err)
         for li, lay in enumerate(L):
             q, k, v = (lay["q"], lay["k"], lay["v"]) if inputs is None else inputs[3][li]
-            pkv.kv_write(k, v, slots, lay["k_pool"], lay["v_pool"], err=err)
+            if not fused:
+                pkv.kv_write(k, v, slots, lay["k_pool"], lay["v_pool"], err=err)
+            elif has_pre:  # the prefill chunks' tokens follow the decode rows' tokens
+                pkv.kv_write(k[nd:], v[nd:], slots[nd:], lay["k_pool"], lay["v_pool"], err=err)
             if nd:
                 if timed:
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
-                pkv.paged_attention_decode(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd],
-                                           src_sl[:nd], sh.scale, max_dec, out=dec_out[li],
-                                           workspace=ws, err=err)
+                if fused:
+                    pkv.paged_attention_decode_append(
+                        q[:nd], k[:nd], v[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd],
+                        src_sl[:nd], sh.scale, max_dec, out=dec_out[li], workspace=ws, err=err)
+                else:
+                    pkv.paged_attention_decode(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd],
+                                               src_sl[:nd], sh.scale, max_dec, out=dec_out[li],
+                                               workspace=ws, err=err)
                 if timed:
                     e1.record(stream)
                     ev_dec.append((e0, e1))
@@ -378,7 +396,11 @@ def run_gb300(args, rank, world, local):
                     e3.record(stream)
                     ev_pre.append((e2, e3))
 
-    launches_per_step = 1 + n_layers * (1 + (3 if nd else 0) + (1 if has_pre else 0))
+    dec_launches = (2 if nd <= 2048 else 3) if nd else 0  # (plan above 2,048 sequences) + main + merge
+    if fused:
+        launches_per_step = (1 if has_pre else 0) + n_layers * (dec_launches + (2 if has_pre else 0))
+    else:
+        launches_per_step = 1 + n_layers * (1 + dec_launches + (1 if has_pre else 0))
 
     def decode_all():
         for li, lay in enumerate(L):
@@ -512,7 +534,7 @@ def run_gb300(args, rank, world, local):
     roof = None
     if dec_ms:
         ach = acc["decode_bytes"] / (dec_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "kernel": "paged_attention_decode (plan + split + merge)",
+        roof = {"bound": "hbm", "kernel": "paged_attention_decode (split kernel + merge)",
                 "timing": ("CUDA events around graph replays of one layer loop of decode calls, "
                            "after the step's timed region" if use_graph else
                            "CUDA events around every decode call inside the timed region"),
@@ -537,7 +559,10 @@ def run_gb300(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if sh.dtype == "bf16" else "f32",
-        "data": "synthetic (seeded; workloads/)", "config": workload_config(plan, n_layers, "cuda_graph" if use_graph else "eager"),
+        "data": "synthetic (seeded; workloads/)",
+        "config": workload_config(plan, n_layers, "cuda_graph" if use_graph else "eager"),
+        "decode_write": ("fused into the decode launch (decode_append)" if fused
+                         else "separate kv_write launch"),
         "decode_tokens_per_s": dec_tok_s,
         "decode_tokens_per_s_note": f"{nd} decode tokens per step of {sh.layers} layers, "
                                     f"{n_layers} timed layer(s) scaled by {sh.layers / n_layers:g}",

@@ -219,6 +219,36 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n
                                       int32_t* err_word, void* stream);
 
 /*
+ * pkv_paged_attention_decode_append - write this step's K/V and run decode
+ * attention, in one launch.
+ *
+ * "Day 16", What I added (append(layer, k, v) stores the step's K/V and
+ * returns the full history for attention) and "nano-vLLM", Where the time
+ * went (at small batches the step is dominated by per-operation launch
+ * cost; fusing operations removes it).  The result is exactly that of
+ *     pkv_kv_write(k_new, v_new, slots) ; pkv_paged_attention_decode(...)
+ * with slots[b] = block_tables[b][(seq_lens[b]-1) / bs] * bs
+ * + (seq_lens[b]-1) % bs: the pools receive the same bytes and the output
+ * is bit-identical to the two calls with the same max_ctas.  Sequences of
+ * length 0 write nothing; a sequence whose length is out of range (see the
+ * PKV_DEVERR_* bits) or whose last table entry is not a valid block id
+ * writes nothing either.  The new row reaches the attention straight from
+ * k_new / v_new; the pool copy is stored alongside.
+ *
+ *   k_new, v_new  [num_seqs, n_kv, head_dim] of pool->dtype, 16-byte aligned
+ *   k_pool, v_pool  written at each sequence's last position only
+ *   everything else as for pkv_paged_attention_decode (same workspace size)
+ */
+pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, const void* v_new,
+                                             int32_t num_seqs, int32_t n_heads, void* k_pool,
+                                             void* v_pool, const pkv_pool_desc* pool,
+                                             const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                             int32_t max_seq_len, float scale, int32_t max_ctas,
+                                             void* out, void* workspace, size_t workspace_bytes,
+                                             int32_t* err_word, void* stream);
+
+/*
  * pkv_paged_attention_prefill - causal attention of a query chunk over the
  * sequence's paged history (chunked prefill).
  *

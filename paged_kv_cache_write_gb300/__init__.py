@@ -72,6 +72,9 @@ def _load():
     L.pkv_paged_attention_decode.restype = _i32
     L.pkv_paged_attention_decode.argtypes = [_p, _i32, _i32, _p, _p, _desc, _p, _i32, _p, _i32,
                                              _f, _i32, _p, _p, _sz, _p, _p]
+    L.pkv_paged_attention_decode_append.restype = _i32
+    L.pkv_paged_attention_decode_append.argtypes = [_p, _p, _p, _i32, _i32, _p, _p, _desc, _p,
+                                                    _i32, _p, _i32, _f, _i32, _p, _p, _sz, _p, _p]
     L.pkv_prefill_workspace_bytes.restype = _sz
     L.pkv_prefill_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
     L.pkv_paged_attention_prefill.restype = _i32
@@ -223,6 +226,37 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, seq_lens, scale: flo
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check("pkv_paged_attention_decode", _load().pkv_paged_attention_decode(
         _dev(q, "q", k_pool.dtype), B, H, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+        ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32), W,
+        _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), float(scale), int(max_ctas),
+        _dev(out, "out", k_pool.dtype), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _opt(err, "err", torch.int32),
+        _stream(stream)))
+    return out
+
+
+def paged_attention_decode_append(q, k_new, v_new, k_pool, v_pool, block_tables, seq_lens,
+                                  scale: float, max_seq_len: int | None = None, *, out=None,
+                                  workspace=None, max_ctas: int = 0, err=None, stream=None):
+    """Store this step's ``k_new``/``v_new`` [B, n_kv, head_dim] at each
+    sequence's last position (``seq_lens[b] - 1``) and return decode
+    attention [B, n_heads, head_dim] over the updated pages, in one launch.
+    Same as ``kv_write`` at those slots followed by ``paged_attention_decode``.
+    """
+    desc = pool_desc(k_pool)
+    B, H, hd = q.shape
+    W = block_tables.shape[1]
+    if k_new.shape != (B, desc.n_kv, hd) or v_new.shape != k_new.shape:
+        raise ValueError(f"k_new/v_new must be {(B, desc.n_kv, hd)}")
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if B else 0
+    if out is None:
+        out = torch.empty_like(q)
+    need = decode_workspace_bytes(B, H, hd, max_seq_len, max_ctas, desc.block_size)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("pkv_paged_attention_decode_append", _load().pkv_paged_attention_decode_append(
+        _dev(q, "q", k_pool.dtype), _dev(k_new, "k_new", k_pool.dtype),
+        _dev(v_new, "v_new", k_pool.dtype), B, H, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
         ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32), W,
         _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), float(scale), int(max_ctas),
         _dev(out, "out", k_pool.dtype), _dev(workspace, "workspace"),

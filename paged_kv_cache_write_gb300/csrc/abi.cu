@@ -133,13 +133,15 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t hea
   return pkv::decode_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len, max_ctas);
 }
 
-pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n_heads,
-                                      const void* k_pool, const void* v_pool,
-                                      const pkv_pool_desc* pool, const int32_t* block_tables,
-                                      int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                                      int32_t max_seq_len, float scale, int32_t max_ctas,
-                                      void* out, void* workspace, size_t workspace_bytes,
-                                      int32_t* err_word, void* stream) {
+namespace {
+
+// Shared body of the decode entry points; k_new / v_new null: plain decode.
+pkv_status decode_entry(const void* q, const void* k_new, const void* v_new, int32_t num_seqs,
+                        int32_t n_heads, const void* k_pool, const void* v_pool,
+                        const pkv_pool_desc* pool, const int32_t* block_tables,
+                        int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+                        float scale, int32_t max_ctas, void* out, void* workspace,
+                        size_t workspace_bytes, int32_t* err_word, void* stream) {
   PoolShape shape;
   pkv_status st = check_attention(q, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
                                   max_blocks_per_seq, seq_lens, max_seq_len, scale, out, &shape);
@@ -147,6 +149,8 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n
   if (max_ctas < 0) return PKV_ERR_RANGE;
   if (!pkv::decode_supported(shape, n_heads)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_NULL;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_ALIGN;
   if (!workspace) return PKV_ERR_WORKSPACE;
   if (workspace_bytes < pkv::decode_workspace_bytes(num_seqs, n_heads, shape.head_dim,
                                                     max_seq_len, max_ctas))
@@ -171,8 +175,36 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n
   a.max_ctas = max_ctas;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
+  a.k_new = k_new;
+  a.v_new = v_new;
   a.err = err_word;
   return from_cuda(pkv::launch_decode(a, as_stream(stream)));
+}
+
+}  // namespace
+
+pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n_heads,
+                                      const void* k_pool, const void* v_pool,
+                                      const pkv_pool_desc* pool, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                      int32_t max_seq_len, float scale, int32_t max_ctas,
+                                      void* out, void* workspace, size_t workspace_bytes,
+                                      int32_t* err_word, void* stream) {
+  return decode_entry(q, nullptr, nullptr, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
+                      max_blocks_per_seq, seq_lens, max_seq_len, scale, max_ctas, out, workspace,
+                      workspace_bytes, err_word, stream);
+}
+
+pkv_status pkv_paged_attention_decode_append(
+    const void* q, const void* k_new, const void* v_new, int32_t num_seqs, int32_t n_heads,
+    void* k_pool, void* v_pool, const pkv_pool_desc* pool, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len, float scale,
+    int32_t max_ctas, void* out, void* workspace, size_t workspace_bytes, int32_t* err_word,
+    void* stream) {
+  if (num_seqs > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_NULL;
+  return decode_entry(q, k_new, v_new, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
+                      max_blocks_per_seq, seq_lens, max_seq_len, scale, max_ctas, out, workspace,
+                      workspace_bytes, err_word, stream);
 }
 
 size_t pkv_prefill_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }

@@ -403,10 +403,14 @@ __device__ __forceinline__ void ring_init(const Ring& r, int consumer_warps) {
 // next stage with rows [0, valid) of block `blk` (lane l < 16: K row l,
 // lane l >= 16: V row l-16), zero rows [valid, 16).  `k_src`/`v_src` point
 // at the first element of this CTA's heads in token row 0 of the block
-// (ignored when valid == 0).  Returns false if the wait timed out.
+// (ignored when valid == 0).  Row `new_row` (if in [0, valid)) is taken
+// from `k_new_src`/`v_new_src` instead.  Returns false if the wait timed
+// out.
 __device__ __forceinline__ bool ring_fill(const Ring& r, uint32_t it, const uint8_t* k_src,
                                           const uint8_t* v_src, int64_t src_row_pitch, int valid,
-                                          int32_t* err) {
+                                          int32_t* err, int new_row = -1,
+                                          const uint8_t* k_new_src = nullptr,
+                                          const uint8_t* v_new_src = nullptr) {
   const int lane = threadIdx.x & 31;
   const int st = static_cast<int>(it % r.nstages);
   const uint32_t use = it / r.nstages;
@@ -425,7 +429,8 @@ __device__ __forceinline__ bool ring_fill(const Ring& r, uint32_t it, const uint
   if (lane == 0) mbar_arrive_expect_tx(r.full + st, static_cast<uint32_t>(2 * valid * r.row_bytes));
   if (row < valid) {
     fence_proxy_async_smem();
-    const uint8_t* src = (is_v ? v_src : k_src) + row * src_row_pitch;
+    const uint8_t* src = row == new_row ? (is_v ? v_new_src : k_new_src)
+                                        : (is_v ? v_src : k_src) + row * src_row_pitch;
     bulk_copy_g2s(dst, src, static_cast<uint32_t>(r.row_bytes), r.full + st);
   }
   return true;
@@ -460,6 +465,8 @@ struct DecodeParams {
   void* out;
   const uint8_t* k_pool;
   const uint8_t* v_pool;
+  const uint8_t* k_new;  // append: this step's K/V per sequence [B, n_kv, HD], else null
+  const uint8_t* v_new;
   const int32_t* bt;
   const int32_t* seq_lens;
   int32_t* err;
@@ -784,12 +791,31 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
             valid = 0;
           }
           const int64_t off = int64_t(valid > 0 ? blk : 0) * kBS * token_pitch + head_off;
-          if (!ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err)) {
+          // append: the step's token is the last of the sequence; its row
+          // comes from k_new / v_new, which this CTA also stores to the pool
+          const bool fresh = p.k_new != nullptr && j == cur.nblk - 1 && valid > 0 &&
+                             __ldg(p.seq_lens + cur.b) == cur.L;  // not a clamped bad length
+          const int new_row = fresh ? cur.L - 1 - j * kBS : -1;
+          const int64_t new_off = int64_t(cur.b) * p.n_kv * HD * p.elem_bytes + head_off;
+          if (!ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err,
+                         new_row, p.k_new + new_off, p.v_new + new_off)) {
             *ring.abort_flag = 1;
             ok = false;
             break;
           }
           ++it;
+          if (fresh) {
+            const int nvec = ring.row_bytes / 16;  // 16-byte pieces of this group's row
+            const int64_t dst = off + int64_t(new_row) * token_pitch;
+            for (int i = lane; i < 2 * nvec; i += 32) {
+              const bool is_v = i >= nvec;
+              const int64_t o = int64_t(is_v ? i - nvec : i) * 16;
+              const uint4 x = __ldg(reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) +
+                                                                   new_off + o));
+              *reinterpret_cast<uint4*>(const_cast<uint8_t*>(is_v ? p.v_pool : p.k_pool) + dst +
+                                        o) = x;
+            }
+          }
         }
       }
       u += n;
@@ -1190,6 +1216,8 @@ struct DecodeLaunch {
     p.v_pool = static_cast<const uint8_t*>(a.v_pool);
     p.bt = a.block_tables;
     p.seq_lens = a.seq_lens;
+    p.k_new = static_cast<const uint8_t*>(a.k_new);
+    p.v_new = static_cast<const uint8_t*>(a.v_new);
     p.err = a.err;
     p.B = a.num_seqs;
     p.n_heads = a.n_heads;

@@ -43,6 +43,11 @@ struct AttnArgs {
   PoolShape pool;
   float scale;
   int32_t max_ctas;  // decode: persistent grid cap (0 = one full wave)
+  // decode with append: this step's K/V per sequence [num_seqs, n_kv,
+  // head_dim], stored at position seq_lens[b] - 1 (null: plain decode;
+  // then k_pool / v_pool are only read)
+  const void* k_new;
+  const void* v_new;
   void* workspace;
   size_t workspace_bytes;
   int32_t* err;

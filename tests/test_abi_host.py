@@ -108,6 +108,29 @@ def test_decode_host_checks(pkv):
     assert _decode(pkv, B=0) == 0
 
 
+def _append(pkv, **over):
+    a = dict(q=FAKE, kn=FAKE, vn=FAKE, B=2, H=8, k=FAKE, v=FAKE, desc=_desc(pkv), bt=FAKE, W=4,
+             sl=FAKE, maxlen=64, scale=0.125, max_ctas=0, out=FAKE, ws=FAKE, wsb=1 << 40, err=None)
+    a.update(over)
+    return pkv.lib.pkv_paged_attention_decode_append(
+        a["q"], a["kn"], a["vn"], a["B"], a["H"], a["k"], a["v"], ctypes.byref(a["desc"]), a["bt"],
+        a["W"], a["sl"], a["maxlen"], a["scale"], a["max_ctas"], a["out"], a["ws"], a["wsb"],
+        a["err"], None)
+
+
+def test_decode_append_host_checks(pkv):
+    assert _append(pkv, kn=None) == 1
+    assert _append(pkv, vn=None) == 1
+    assert _append(pkv, kn=FAKE + 8) == 4
+    assert _append(pkv, vn=FAKE + 4) == 4
+    assert _append(pkv, q=None) == 1
+    assert _append(pkv, H=7) == 2
+    assert _append(pkv, scale=0.0) == 5
+    assert _append(pkv, ws=None) == 6
+    assert _append(pkv, desc=_desc(pkv, head_dim=48)) == 7
+    assert _append(pkv, B=0, kn=None, vn=None) == 0
+
+
 def test_prefill_host_checks(pkv):
     lib = pkv.lib
     d = _desc(pkv)
