@@ -9,6 +9,8 @@ fallback, and this package shares no code, table or helper with it.
 The oracle is the plain definition of what the hot path computes, written
 in numpy with float64 arithmetic:
 
+* the copy-on-write block copy follows "Build a Mini vLLM", Key Takeaways
+  6 (prefix sharing with copy-on-write blocks);
 * slot mapping, the scatter write and the block-table gather follow
   "Build a Mini vLLM" section 2 (``BlockManager.append_slot``) and section 3
   (``gather_kv``), and "Day 16" (What I learned, item 3: write is a scatter,
@@ -29,6 +31,7 @@ from .paged import (  # noqa: F401
     slot_of,
     slot_mapping,
     kv_write,
+    copy_blocks,
     gather_kv,
     kv_head_of,
     causal_last_key,

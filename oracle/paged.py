@@ -101,6 +101,30 @@ def kv_write(k, v, slots, k_pool, v_pool):
     return k_pool, v_pool
 
 
+def copy_blocks(k_pool, v_pool, pairs):
+    """Return copies of the pools where, for each ``(src, dst)`` of
+    ``pairs``, physical block ``dst`` holds the contents of block ``src``.
+
+    This is the copy of copy-on-write prefix sharing ("Build a Mini vLLM",
+    Key Takeaways 6: real engines share prefix blocks and copy a shared
+    block before a sequence writes into it).  All copies read the pools as
+    they were before the call, so the result does not depend on the order
+    of the pairs.  A pair with an id outside ``[0, num_blocks)`` is skipped
+    (pages silent; the kernels report and skip it too).
+    """
+    src_k = np.array(k_pool, copy=True)
+    src_v = np.array(v_pool, copy=True)
+    k_out = np.array(k_pool, copy=True)
+    v_out = np.array(v_pool, copy=True)
+    nb = k_out.shape[0]
+    for s, d in np.asarray(pairs, dtype=np.int64).reshape(-1, 2):
+        if not (0 <= s < nb and 0 <= d < nb):
+            continue
+        k_out[d] = src_k[s]
+        v_out[d] = src_v[s]
+    return k_out, v_out
+
+
 # --------------------------------------------------------------------------
 # the block-table gather ("Build a Mini vLLM" section 3, gather_kv)
 # --------------------------------------------------------------------------

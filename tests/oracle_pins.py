@@ -111,6 +111,50 @@ def pin_write_gather_round_trip():
         assert len(set(sm.tolist())) == len(sm)
 
 
+def pin_copy_on_write_shared_prefix():
+    """Copy-on-write of a shared prefix block ("Build a Mini vLLM", Key
+    Takeaways 6): sequences A and B share physical block P holding the
+    first 6 tokens (block size 4: P is full, Q half full and also shared).
+    Before B writes its 7th token into the shared, half-full block Q, the
+    engine copies Q to a free block F, points B's table at F, then writes.
+    A must read back exactly what it had; B its prefix plus the new token."""
+    rng = np.random.default_rng(5)
+    bs, n_kv, hd, nb = 4, 2, 3, 8
+    kp = _rand_pool(rng, nb, bs, n_kv, hd)
+    vp = _rand_pool(rng, nb, bs, n_kv, hd)
+    P, Q, F = 3, 6, 1
+    table_a = np.array([P, Q])
+    a_k = oracle.gather_kv(kp, table_a, 6).copy()
+    a_v = oracle.gather_kv(vp, table_a, 6).copy()
+    kp2, vp2 = oracle.copy_blocks(kp, vp, np.array([[Q, F]]))
+    table_b = np.array([P, F])
+    new_k = rng.standard_normal((1, n_kv, hd)).astype(np.float32)
+    new_v = rng.standard_normal((1, n_kv, hd)).astype(np.float32)
+    sm = oracle.slot_mapping(table_b[None], np.array([7]), np.array([1]), bs)
+    assert sm.tolist() == [F * bs + 2]
+    kp3, vp3 = oracle.kv_write(new_k, new_v, sm, kp2, vp2)
+    assert np.array_equal(oracle.gather_kv(kp3, table_a, 6), a_k)
+    assert np.array_equal(oracle.gather_kv(vp3, table_a, 6), a_v)
+    assert np.array_equal(oracle.gather_kv(kp3, table_b, 7), np.concatenate([a_k, new_k]))
+    assert np.array_equal(oracle.gather_kv(vp3, table_b, 7), np.concatenate([a_v, new_v]))
+    # only block F changed, and F's first two rows are Q's
+    changed = [b for b in range(nb) if not np.array_equal(kp3[b], kp[b])]
+    assert changed == [F]
+    assert np.array_equal(kp3[F, :2], kp[Q, :2]) and np.array_equal(vp3[F, :2], vp[Q, :2])
+
+
+def pin_copy_blocks_reads_the_pools_before_the_call():
+    """Pairs chained through a block (0 -> 1, 1 -> 2) copy the old
+    contents: block 2 receives the old block 1, whatever the pair order;
+    a pair with an id outside the pool is skipped."""
+    blocks = np.arange(5, dtype=np.float32).reshape(5, 1, 1, 1) * np.ones((5, 2, 1, 2),
+                                                                      dtype=np.float32)
+    for pairs in ([[0, 1], [1, 2], [7, 3]], [[1, 2], [0, 1], [3, -1]]):
+        kp, vp = oracle.copy_blocks(blocks, -blocks, np.array(pairs))
+        assert [float(kp[b, 0, 0, 0]) for b in range(5)] == [0.0, 0.0, 1.0, 3.0, 4.0], pairs
+        assert np.array_equal(vp, -kp)
+
+
 def pin_negative_slot_skipped():
     pool = np.zeros((2, 2, 1, 1), dtype=np.float32)
     k = np.array([[[1.0]], [[2.0]]], dtype=np.float32)

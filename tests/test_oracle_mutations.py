@@ -6,6 +6,8 @@ import pytest
 import oracle.paged as op
 from oracle_pins import ALL_PINS
 
+_orig_copy = op.copy_blocks
+
 
 def _wrong_group(h, n_heads, n_kv):           # h % n_kv instead of h // rep
     return h % n_kv
@@ -56,6 +58,23 @@ def _bf16_truncated_bits(raw, dtype):
     return np.asarray(raw, dtype=np.float32).astype(np.float64)
 
 
+def _copy_reversed(k_pool, v_pool, pairs):      # dst copied onto src
+    return _orig_copy(k_pool, v_pool, np.asarray(pairs).reshape(-1, 2)[:, ::-1])
+
+
+def _copy_in_place(k_pool, v_pool, pairs):      # later pairs see earlier copies
+    k, v = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
+    for s, d in np.asarray(pairs).reshape(-1, 2):
+        if 0 <= s < k.shape[0] and 0 <= d < k.shape[0]:
+            k[d], v[d] = k[s], v[s]
+    return k, v
+
+
+def _copy_k_only(k_pool, v_pool, pairs):        # V left behind
+    k, _ = _orig_copy(k_pool, v_pool, pairs)
+    return k, np.array(v_pool, copy=True)
+
+
 MUTANTS = [
     ("kv_head_of", _wrong_group),
     ("slot_of", _slot_swapped),
@@ -67,6 +86,9 @@ MUTANTS = [
     ("gather_kv", _gather_off_by_one_len),
     ("merge_partials", _merge_no_rescale),
     ("to_float64", _bf16_truncated_bits),
+    ("copy_blocks", _copy_reversed),
+    ("copy_blocks", _copy_in_place),
+    ("copy_blocks", _copy_k_only),
 ]
 
 
