@@ -479,6 +479,36 @@ def run_gb300(args, rank, world, local):
     step_bytes = per_layer * n_layers
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
 
+    # ---- copy-on-write block copy: held blocks onto free ones of layer 0's
+    # pools (free blocks are outside every sequence, so the step is untouched)
+    cow = None
+    free = np.setdiff1d(np.arange(1 if sh.dummy_block0 else 0, sh.num_blocks), plan.held_blocks)
+    n_cow = int(min(4096, len(free), len(plan.held_blocks)))
+    if n_cow > 0:
+        crng = np.random.default_rng(99)
+        pairs = np.stack([crng.choice(plan.held_blocks, n_cow, replace=False),
+                          crng.choice(free, n_cow, replace=False)], axis=1).astype(np.int32)
+        pairs_d = torch.from_numpy(pairs).to(dev)
+
+        def cow_call():
+            pkv.copy_blocks(L[0]["k_pool"], L[0]["v_pool"], pairs_d, err=err)
+
+        for _ in range(3):
+            cow_call()
+        reps = 20
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(reps):
+            cow_call()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        cow_ms = c0.elapsed_time(c1) / reps
+        block_bytes = sh.block_size * sh.n_kv * sh.head_dim * sh.itemsize
+        cow_bytes = 2 * 2 * n_cow * block_bytes  # K and V, read and written
+        cow = {"pairs": n_cow, "bytes_per_launch": cow_bytes, "ms_per_launch": cow_ms,
+               "achieved": cow_bytes / (cow_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "timing": "CUDA events around 20 back-to-back launches after 3 warm-up launches"}
+
     # ---- end to end: step inputs from pinned host memory, outputs back
     e2e = None
     if not args.no_e2e:
@@ -571,6 +601,8 @@ def run_gb300(args, rank, world, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "bytes_per_step": step_bytes,
+        "copy_blocks": (dict(cow, peak=hbm, frac=cow["achieved"] / hbm,
+                             peak_source=f"hbm_gbs of {src}") if cow else None),
     }
     print(json.dumps(line), flush=True)
     if world > 1:

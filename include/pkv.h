@@ -168,6 +168,30 @@ pkv_status pkv_kv_gather(const void* k_pool, const void* v_pool, const pkv_pool_
                          void* k_out, void* v_out, int32_t* err_word, void* stream);
 
 /*
+ * pkv_copy_blocks - copy whole physical blocks of both pools (the copy of
+ * copy-on-write prefix sharing).
+ *
+ * "Build a Mini vLLM", Key Takeaways 6: real engines share the blocks of a
+ * common prefix between sequences and copy a shared block before one of
+ * them writes into it.  For every pair i:
+ *     k_pool[block_pairs[i][1]] = k_pool[block_pairs[i][0]]  (all
+ *     block_size x n_kv x head_dim elements, bit for bit), and the same for v_pool
+ * The caller then points the writing sequence's table entry at the
+ * destination.  Destinations must be distinct and must not be the source
+ * of any pair in the same call (then the result is that of copying from
+ * the pools as they were before the call); otherwise which bytes land is
+ * unspecified.  A pair with an id outside [0, num_blocks) is skipped and
+ * reported as PKV_DEVERR_BLOCK_ID.
+ *
+ *   block_pairs  int32 [num_pairs][2] (source, destination), device memory
+ *   k_pool, v_pool  16-byte aligned; n_kv * head_dim * sizeof(dtype) a
+ *                   multiple of 16 bytes
+ */
+pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const pkv_pool_desc* pool,
+                           const int32_t* block_pairs, int32_t num_pairs, int32_t* err_word,
+                           void* stream);
+
+/*
  * Workspace for pkv_paged_attention_decode, in bytes (never 0): room for
  * a per-sequence work prefix and two partial results per CTA of the
  * largest grid the current device can run.  max_seq_len and max_ctas are

@@ -65,6 +65,8 @@ def _load():
     L.pkv_slot_mapping.argtypes = [_p, _i32, _p, _p, _i32, _i32, _i32, _i32, _p, _p, _p]
     L.pkv_kv_write.restype = _i32
     L.pkv_kv_write.argtypes = [_p, _p, _p, _i32, _p, _p, _desc, _p, _p]
+    L.pkv_copy_blocks.restype = _i32
+    L.pkv_copy_blocks.argtypes = [_p, _p, _desc, _p, _i32, _p, _p]
     L.pkv_kv_gather.restype = _i32
     L.pkv_kv_gather.argtypes = [_p, _p, _desc, _p, _i32, _p, _p, _i32, _i32, _p, _p, _p, _p]
     L.pkv_decode_workspace_bytes.restype = _sz
@@ -178,6 +180,19 @@ def kv_write(k, v, slot_mapping, k_pool, v_pool, *, err=None, stream=None):
         _dev(slot_mapping, "slot_mapping", torch.int64), T, _dev(k_pool, "k_pool"),
         _dev(v_pool, "v_pool"), ctypes.byref(desc), _opt(err, "err", torch.int32),
         _stream(stream)))
+
+
+def copy_blocks(k_pool, v_pool, block_pairs, *, err=None, stream=None):
+    """Copy whole blocks of both pools: for each row (src, dst) of the
+    int32 [n, 2] ``block_pairs``, block dst becomes a copy of block src
+    (copy-on-write).  Destinations must be distinct and not sources."""
+    desc = pool_desc(k_pool)
+    if block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be [n, 2]")
+    _check("pkv_copy_blocks", _load().pkv_copy_blocks(
+        _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), ctypes.byref(desc),
+        _dev(block_pairs, "block_pairs", torch.int32), int(block_pairs.shape[0]),
+        _opt(err, "err", torch.int32), _stream(stream)))
 
 
 def kv_gather(k_pool, v_pool, block_tables, seq_lens, cu_seq_lens, total_tokens: int, *,

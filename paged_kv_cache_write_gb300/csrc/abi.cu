@@ -103,6 +103,20 @@ pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mappin
                                         err_word, as_stream(stream)));
 }
 
+pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const pkv_pool_desc* pool,
+                          const int32_t* block_pairs, int32_t num_pairs, int32_t* err_word,
+                          void* stream) {
+  PoolShape shape;
+  pkv_status st = check_pool(pool, &shape);
+  if (st != PKV_OK) return st;
+  if (num_pairs < 0) return PKV_ERR_SHAPE;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !block_pairs) return PKV_ERR_NULL;
+  if (!aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_ALIGN;
+  return from_cuda(pkv::launch_copy_blocks(k_pool, v_pool, shape, block_pairs, num_pairs,
+                                           err_word, as_stream(stream)));
+}
+
 pkv_status pkv_kv_gather(const void* k_pool, const void* v_pool, const pkv_pool_desc* pool,
                          const int32_t* block_tables, int32_t max_blocks_per_seq,
                          const int32_t* seq_lens, const int32_t* cu_seq_lens, int32_t num_seqs,

@@ -81,6 +81,47 @@ __global__ void kv_write_kernel(const uint4* __restrict__ k, const uint4* __rest
   }
 }
 
+// Copy-on-write block copy: CTA i copies block pairs[i][0] onto block
+// pairs[i][1] in both pools.  The K and V blocks are one run of 16-byte
+// words (K first, then V); each thread moves kCopyUnroll words per pass
+// with all loads issued before any store, streaming past the caches (the
+// copied data is not read again by this kernel).
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 8;
+
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                       const int32_t* __restrict__ pairs, int64_t words_per_block,
+                       int num_blocks, int32_t* err) {
+  const int src = __ldg(pairs + 2 * int64_t(blockIdx.x));
+  const int dst = __ldg(pairs + 2 * int64_t(blockIdx.x) + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0) report(err, PKV_DEVERR_BLOCK_ID);
+    return;
+  }
+  const int64_t n = 2 * words_per_block;
+  const uint4* ks = k_pool + src * words_per_block;
+  const uint4* vs = v_pool + src * words_per_block;
+  uint4* kd = k_pool + dst * words_per_block;
+  uint4* vd = v_pool + dst * words_per_block;
+  for (int64_t base = threadIdx.x; base < n; base += int64_t(kCopyThreads) * kCopyUnroll) {
+    uint4 x[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t i = base + int64_t(u) * kCopyThreads;
+      if (i < n) x[u] = i < words_per_block ? __ldcs(ks + i) : __ldcs(vs + (i - words_per_block));
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t i = base + int64_t(u) * kCopyThreads;
+      if (i < n) {
+        if (i < words_per_block) __stcs(kd + i, x[u]);
+        else __stcs(vd + (i - words_per_block), x[u]);
+      }
+    }
+  }
+}
+
 __global__ void kv_gather_kernel(const uint4* __restrict__ k_pool, const uint4* __restrict__ v_pool,
                                  int words_per_row, int bs, int num_blocks,
                                  const int32_t* __restrict__ block_tables, int W,
@@ -153,6 +194,17 @@ cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_ma
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, num_tokens, words,
       static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
       int64_t(pool.num_blocks) * pool.block_size, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const PoolShape& pool,
+                               const int32_t* pairs, int32_t num_pairs, int32_t* err,
+                               cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  const int64_t words = int64_t(pool.block_size) * pool.row_bytes() / 16;
+  copy_blocks_kernel<<<num_pairs, kCopyThreads, 0, stream>>>(
+      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), pairs, words, pool.num_blocks,
+      err);
   return cudaGetLastError();
 }
 

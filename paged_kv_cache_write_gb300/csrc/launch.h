@@ -24,6 +24,10 @@ cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_ma
                             int32_t num_tokens, void* k_pool, void* v_pool, const PoolShape& pool,
                             int32_t* err, cudaStream_t stream);
 
+cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const PoolShape& pool,
+                               const int32_t* pairs, int32_t num_pairs, int32_t* err,
+                               cudaStream_t stream);
+
 cudaError_t launch_kv_gather(const void* k_pool, const void* v_pool, const PoolShape& pool,
                              const int32_t* block_tables, int32_t max_blocks_per_seq,
                              const int32_t* seq_lens, const int32_t* cu_seq_lens, int32_t num_seqs,

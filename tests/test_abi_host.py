@@ -72,6 +72,18 @@ def test_kv_write_host_checks(pkv):
                             None, None) == 2
 
 
+def test_copy_blocks_host_checks(pkv):
+    lib = pkv.lib
+    d = _desc(pkv)
+    by = ctypes.byref
+    assert lib.pkv_copy_blocks(FAKE, FAKE, None, FAKE, 3, None, None) == 1
+    assert lib.pkv_copy_blocks(FAKE, FAKE, by(d), FAKE, -1, None, None) == 2
+    assert lib.pkv_copy_blocks(FAKE, FAKE, by(d), None, 3, None, None) == 1
+    assert lib.pkv_copy_blocks(FAKE + 8, FAKE, by(d), FAKE, 3, None, None) == 4
+    assert lib.pkv_copy_blocks(FAKE, FAKE, by(_desc(pkv, dtype=9)), FAKE, 3, None, None) == 3
+    assert lib.pkv_copy_blocks(None, None, by(d), None, 0, None, None) == 0
+
+
 def test_slot_mapping_host_checks(pkv):
     lib = pkv.lib
     assert lib.pkv_slot_mapping(FAKE, 4, FAKE, FAKE, -1, 3, 16, 8, FAKE, None, None) == 2
