@@ -50,6 +50,13 @@ sys.path.insert(0, ROOT)
 METRIC = ("paged decode attn: KV GB/s read (% of GB300 HBM peak), decode tokens/s per step")
 WORKLOAD = "llama2-70b-mixed"
 WORKLOAD_LABEL = "llama2-70b-gqa8-mixed-decode256-prefill4x512"
+# DRAM bytes (read + written) per KV byte touched by the decode kernel,
+# measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
+# llama2-70b-decode64 workload (70B shape) and one layer of the
+# llama-3.2-1b workload; keyed by (dtype, n_heads, n_kv, head_dim).  Valid
+# only for the decode kernel as it was captured: drop the entries when the
+# kernel changes and capture again.
+DECODE_DRAM_PER_KV_BYTE = {("bf16", 64, 8, 128): 1.01459, ("bf16", 32, 8, 64): 1.02249}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit -> name
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -564,12 +571,18 @@ def run_gb300(args, rank, world, local):
     roof = None
     if dec_ms:
         ach = acc["decode_bytes"] / (dec_ms * 1e-3) / 1e9
+        ratio = DECODE_DRAM_PER_KV_BYTE.get((sh.dtype, sh.n_heads, sh.n_kv, sh.head_dim))
+        traffic = ratio * acc["decode_kv_bytes"] if ratio else None
         roof = {"bound": "hbm", "kernel": "paged_attention_decode (split kernel + merge)",
                 "timing": ("CUDA events around graph replays of one layer loop of decode calls, "
                            "after the step's timed region" if use_graph else
                            "CUDA events around every decode call inside the timed region"),
                 "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "peak_source": f"hbm_gbs of {src}", "traffic": None,
+                "peak_source": f"hbm_gbs of {src}", "traffic": traffic,
+                "traffic_note": ("dram__bytes_read.sum + dram__bytes_write.sum of the decode "
+                                 "kernel per KV byte, from one ncu capture of this shape, "
+                                 "times this call's KV bytes"
+                                 if traffic else "no capture of this shape's current kernel"),
                 "algorithmic_bytes_per_launch": acc["decode_bytes"], "ms_per_launch": dec_ms}
     pre_roof = None
     if pre_ms:
@@ -580,11 +593,24 @@ def run_gb300(args, rank, world, local):
                     "ms_per_launch": pre_ms}
     cpu = None
     if not args.no_cpu_baseline and layers_cpu:
-        secs, nbytes, nr, npq = oracle_sample(plan, layers_cpu[0], 48 if nd >= 48 else nd, 16)
+        # passes over layer 0 (every decode sequence, 64 prefill queries
+        # per pass, rotating) until about 10 s of CPU work are done
+        secs = nbytes = nr = npq = passes = 0
+        while secs < 10.0 and passes < 50:
+            s_, b_, r_, p_ = oracle_sample(plan, layers_cpu[0], nd, 64, offset=passes * 64)
+            secs, nbytes, nr, npq, passes = secs + s_, nbytes + b_, nr + r_, npq + p_, passes + 1
         cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{nr} decode sequences + {npq} prefill queries of layer 0 "
-                         f"({nbytes / 1e6:.0f} MB of KV), float64 numpy oracle, {secs:.1f} s"}
+               "sample": f"{passes} passes over layer 0: {nr} decode sequences + {npq} prefill "
+                         f"queries in all ({nbytes / 1e6:.0f} MB of KV), float64 numpy oracle, "
+                         f"{secs:.1f} s on one core"}
     dec_tok_s = world * nd / (ms_step * 1e-3 * (sh.layers / n_layers)) if nd else None
+    n_pre_tok = int(plan.new_lens[nd:].sum())
+    pre_tok_s = (world * n_pre_tok / (ms_step * 1e-3 * (sh.layers / n_layers))
+                 if has_pre else None)
+    # the roofline object describes the step's dominant kernel
+    dominant = roof
+    if pre_roof and (roof is None or pre_ms > dec_ms):
+        dominant = pre_roof
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -597,7 +623,9 @@ def run_gb300(args, rank, world, local):
         "decode_tokens_per_s_note": f"{nd} decode tokens per step of {sh.layers} layers, "
                                     f"{n_layers} timed layer(s) scaled by {sh.layers / n_layers:g}",
         "percent_of_hbm_peak_step": 100.0 * value / world / hbm,
-        "roofline": roof, "prefill_roofline": pre_roof, "cpu_baseline": cpu, "e2e": e2e,
+        "prefill_tokens_per_s": pre_tok_s,
+        "roofline": dominant, "decode_roofline": roof, "prefill_roofline": pre_roof,
+        "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "bytes_per_step": step_bytes,

@@ -66,7 +66,7 @@ def test_copy_blocks_bad_ids_skipped():
 
 
 def test_copy_blocks_many_pairs_workload_block():
-    """4,096 pairs of LLaMA-2-70B-shaped blocks (16 KB of K and of V each)."""
+    """4,096 pairs of LLaMA-2-70B-shaped blocks (32 KB of K and 32 KB of V each)."""
     nb, n = 10000, 4096
     g = torch.Generator(device="cuda").manual_seed(3)
     kp = torch.randn((nb, 16, 8, 128), generator=g, device="cuda").to(torch.bfloat16)

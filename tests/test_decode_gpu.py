@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 # (shape, layers checked).  All layers of the toy and SmolLM2 steps; three
 # layers of Llama-3.2-1B; first and last layer of LLaMA-7B; the one 70B layer.
 CASES = [("toy", [0]), ("smollm2-135m", list(range(30))), ("llama-3.2-1b", [0, 7, 15]),
-         ("llama-7b", [0, 31]), ("llama2-70b-mixed", [0])]
+         ("llama-7b", [0, 31]), ("llama2-70b-mixed", [0]), ("llama2-70b-decode64", [0])]
 
 
 def _sample_rows(plan, n=24):
@@ -37,7 +37,7 @@ def test_decode_matches_oracle(name, layers):
         g, o = GpuStep(plan, layer), OracleStep(plan, layer)
         o.run_write()
         _, dec, _ = g.run()
-        rows = _sample_rows(plan) if name == "llama2-70b-mixed" else None
+        rows = _sample_rows(plan) if name.startswith("llama2-70b") else None
         ref = o.decode(rows=rows)
         rows = rows if rows is not None else list(range(plan.n_decode))
         assert_close(f64(dec)[rows], ref[rows], plan.shape.dtype, f"{name} layer {layer_id}")

@@ -30,6 +30,28 @@ def test_prefill_70b_mixed_step_sampled():
     assert int(g.err.item()) == 0
 
 
+@pytest.mark.parametrize("name", ["smollm2-135m-prompts", "llama-3.2-1b-prompts"])
+def test_batched_full_prompt_prefill_sampled(name):
+    """Batched full-prompt prefill (history 0): every prompt of a batch of
+    users arriving together in one launch; sampled queries of every prompt
+    (first, block edges, last, random) against the oracle."""
+    plan = draw_plan(name)
+    assert plan.n_decode == 0 and np.array_equal(plan.new_lens, plan.seq_lens)
+    layer = make_layer(plan, 0, fill=1e30)
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.run_write()
+    _, _, pre = g.run()
+    got = f64(pre)
+    rng = np.random.default_rng(5)
+    for b in range(plan.num_seqs):
+        c = int(plan.new_lens[b])
+        base = int(plan.cu_new_lens[b])
+        qs = sorted({0, 1, 15, 16, 17, c - 1} | set(rng.choice(c, 4, replace=False).tolist()))
+        ref = np.stack([o.prefill_row(b, i) for i in qs])
+        assert_close(got[[base + i for i in qs]], ref, "bf16", f"{name} prompt {b}")
+    assert int(g.err.item()) == 0
+
+
 SMALL = [(8, 4, 16, "f32"), (16, 2, 64, "f32"), (9, 3, 64, "bf16"), (32, 8, 64, "bf16"),
          (64, 8, 128, "bf16"), (8, 8, 128, "bf16"), (16, 1, 64, "bf16"), (4, 2, 32, "bf16")]
 

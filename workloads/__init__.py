@@ -74,15 +74,24 @@ SHAPES = {
     "llama2-70b-mixed": Shape("llama2-70b-mixed", "bf16", 80, 64, 8, 128, 16, 65536, True),
     # the prefill half of the 70B mixed step alone, in a small pool (profiling)
     "llama2-70b-prefill": Shape("llama2-70b-prefill", "bf16", 80, 64, 8, 128, 16, 2048, True),
+    # 64 of the 70B step's decode sequences in an 8,192-block pool (profiling)
+    "llama2-70b-decode64": Shape("llama2-70b-decode64", "bf16", 80, 64, 8, 128, 16, 8192, True),
+    # batched full-prompt prefill: every user arriving together is prefilled
+    # in one pass (history 0), the SmolLM2 server's 30 users and a
+    # Llama-3.2-1B batch of 32 prompts
+    "smollm2-135m-prompts": Shape("smollm2-135m-prompts", "bf16", 30, 9, 3, 64, 16, 1024, True),
+    "llama-3.2-1b-prompts": Shape("llama-3.2-1b-prompts", "bf16", 16, 32, 8, 64, 16, 8192, True),
 }
 CONFIG_IDS = {"toy": 1, "smollm2-135m": 2, "llama-3.2-1b": 3, "llama-7b": 4, "llama2-70b-mixed": 5,
-              "llama2-70b-prefill": 6}
+              "llama2-70b-prefill": 6, "llama2-70b-decode64": 7, "smollm2-135m-prompts": 8,
+              "llama-3.2-1b-prompts": 9}
 
 # Layers materialised (each with its own pool) in one timed step.  The toy
 # step is one layer.  One 70B pool of 65,536 blocks is 4.3 GB, so that step
 # is timed on one layer and per-step token rates are scaled by its 80 layers.
 TIMED_LAYERS = {"toy": 1, "smollm2-135m": 30, "llama-3.2-1b": 16, "llama-7b": 32, "llama2-70b-mixed": 1,
-                "llama2-70b-prefill": 1}
+                "llama2-70b-prefill": 1, "llama2-70b-decode64": 1, "smollm2-135m-prompts": 30,
+                "llama-3.2-1b-prompts": 16}
 
 
 @dataclass
@@ -151,6 +160,20 @@ def draw_plan(name: str, *, num_seqs: int | None = None) -> Plan:
     elif name == "llama2-70b-prefill":
         lens = np.array([0, 1365, 2731, 4096], dtype=np.int64) + 512
         n_decode = 0
+    elif name == "llama2-70b-decode64":
+        b = 64 if num_seqs is None else num_seqs
+        raw = rng.lognormal(mean=math.log(1024.0), sigma=1.0, size=b)
+        lens = np.clip(np.rint(raw), 16, 8192).astype(np.int64)
+    elif name == "smollm2-135m-prompts":
+        # the SmolLM2 server's prompts (system prompt + question) of 30 users
+        # arriving together, each prefilled whole
+        b = 30 if num_seqs is None else num_seqs
+        lens = rng.integers(33, 613, size=b)
+        n_decode = 0
+    elif name == "llama-3.2-1b-prompts":
+        b = 32 if num_seqs is None else num_seqs
+        lens = rng.integers(128, 2049, size=b)
+        n_decode = 0
     else:
         raise KeyError(name)
 
@@ -159,6 +182,8 @@ def draw_plan(name: str, *, num_seqs: int | None = None) -> Plan:
         n_decode = B
     new_lens = np.ones(B, dtype=np.int64)
     new_lens[n_decode:] = 512
+    if name.endswith("-prompts"):
+        new_lens[:] = lens  # the whole prompt is this step's chunk (history 0)
 
     first_free = 1 if sh.dummy_block0 else 0
     first_private = first_free + len(shared)
