@@ -80,6 +80,9 @@ def parse_args(argv=None):
     ap.add_argument("--separate-write", action="store_true",
                     help="write every new token with kv_write, then run plain decode "
                          "(instead of the fused decode-with-append launch)")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="decode with the shared-prefix entry point (the workload's common "
+                         "prompt blocks read once per step); the K/V write is then separate")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers materialised per step (0 = the workload's own count)")
     return ap.parse_args(argv)
@@ -354,8 +357,10 @@ def run_gb300(args, rank, world, local):
         max_q = int(plan.new_lens[nd:].max())
         max_pre = int(plan.seq_lens[nd:].max())
     slots = torch.empty(T, dtype=torch.int64, device=dev)
-    ws = torch.empty(pkv.decode_workspace_bytes(nd, sh.n_heads, sh.head_dim, max_dec), dtype=torch.uint8,
-                     device=dev)
+    P = len(plan.shared_prefix_blocks) if args.shared_prefix else 0
+    ws_bytes = (pkv.decode_shared_prefix_workspace_bytes(nd, sh.n_heads, sh.head_dim, max_dec, P)
+                if P else pkv.decode_workspace_bytes(nd, sh.n_heads, sh.head_dim, max_dec))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     dec_out = [torch.empty((nd, sh.n_heads, sh.head_dim), dtype=sh.torch_dtype, device=dev) for _ in L]
     pre_out = [torch.empty((T - nd, sh.n_heads, sh.head_dim), dtype=sh.torch_dtype, device=dev)
                for _ in L] if has_pre else None
@@ -364,7 +369,15 @@ def run_gb300(args, rank, world, local):
 
     ev_dec, ev_pre = [], []
 
-    fused = not args.separate_write
+    fused = not args.separate_write and P == 0
+
+    def decode_call(q, k_pool, v_pool, bt_, sl_, out):
+        if P:
+            pkv.paged_attention_decode_shared_prefix(q, k_pool, v_pool, bt_, sl_, sh.scale, P,
+                                                     max_dec, out=out, workspace=ws, err=err)
+        else:
+            pkv.paged_attention_decode(q, k_pool, v_pool, bt_, sl_, sh.scale, max_dec, out=out,
+                                       workspace=ws, err=err)
 
     def step(timed=False, inputs=None):
         src_bt, src_sl, src_cu = (bt, seq_lens, cu_new) if inputs is None else inputs[:3]
@@ -386,9 +399,8 @@ def run_gb300(args, rank, world, local):
                         q[:nd], k[:nd], v[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd],
                         src_sl[:nd], sh.scale, max_dec, out=dec_out[li], workspace=ws, err=err)
                 else:
-                    pkv.paged_attention_decode(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd],
-                                               src_sl[:nd], sh.scale, max_dec, out=dec_out[li],
-                                               workspace=ws, err=err)
+                    decode_call(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
+                                dec_out[li])
                 if timed:
                     e1.record(stream)
                     ev_dec.append((e0, e1))
@@ -403,7 +415,8 @@ def run_gb300(args, rank, world, local):
                     e3.record(stream)
                     ev_pre.append((e2, e3))
 
-    dec_launches = (2 if nd <= 2048 else 3) if nd else 0  # (plan above 2,048 sequences) + main + merge
+    # (prefix runs + their combine) + (plan above 2,048 sequences) + main + merge
+    dec_launches = ((2 if nd <= 2048 else 3) + (2 if P else 0)) if nd else 0
     if fused:
         launches_per_step = (1 if has_pre else 0) + n_layers * (dec_launches + (2 if has_pre else 0))
     else:
@@ -411,9 +424,8 @@ def run_gb300(args, rank, world, local):
 
     def decode_all():
         for li, lay in enumerate(L):
-            pkv.paged_attention_decode(lay["q"][:nd], lay["k_pool"], lay["v_pool"], bt[:nd],
-                                       seq_lens[:nd], sh.scale, max_dec, out=dec_out[li],
-                                       workspace=ws, err=err)
+            decode_call(lay["q"][:nd], lay["k_pool"], lay["v_pool"], bt[:nd], seq_lens[:nd],
+                        dec_out[li])
 
     def prefill_all():
         for li, lay in enumerate(L):
@@ -573,7 +585,9 @@ def run_gb300(args, rank, world, local):
         ach = acc["decode_bytes"] / (dec_ms * 1e-3) / 1e9
         ratio = DECODE_DRAM_PER_KV_BYTE.get((sh.dtype, sh.n_heads, sh.n_kv, sh.head_dim))
         traffic = ratio * acc["decode_kv_bytes"] if ratio else None
-        roof = {"bound": "hbm", "kernel": "paged_attention_decode (split kernel + merge)",
+        roof = {"bound": "hbm", "kernel": ("paged_attention_decode_shared_prefix (prefix + split "
+                                           "kernel + merge)" if P else
+                                           "paged_attention_decode (split kernel + merge)"),
                 "timing": ("CUDA events around graph replays of one layer loop of decode calls, "
                            "after the step's timed region" if use_graph else
                            "CUDA events around every decode call inside the timed region"),
@@ -619,6 +633,7 @@ def run_gb300(args, rank, world, local):
         "config": workload_config(plan, n_layers, "cuda_graph" if use_graph else "eager"),
         "decode_write": ("fused into the decode launch (decode_append)" if fused
                          else "separate kv_write launch"),
+        "decode_shared_prefix_blocks": P,
         "decode_tokens_per_s": dec_tok_s,
         "decode_tokens_per_s_note": f"{nd} decode tokens per step of {sh.layers} layers, "
                                     f"{n_layers} timed layer(s) scaled by {sh.layers / n_layers:g}",

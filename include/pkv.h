@@ -91,6 +91,7 @@ typedef enum pkv_dtype {
 #define PKV_DEVERR_TABLE_WIDTH 4  /* a length needs more blocks than a table row has */
 #define PKV_DEVERR_LENGTH      8  /* a length < 0, > max_seq_len, or < its chunk      */
 #define PKV_DEVERR_TIMEOUT    16  /* a pipeline wait gave up (kernel returned early) */
+#define PKV_DEVERR_PREFIX     32  /* a table does not start with the declared shared prefix */
 
 /* Shape of one layer's K pool (the V pool has the same shape). */
 typedef struct pkv_pool_desc {
@@ -192,9 +193,10 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const pkv_pool_desc* pool
                            void* stream);
 
 /*
- * Workspace for pkv_paged_attention_decode, in bytes (never 0): room for
- * a per-sequence work prefix and two partial results per CTA of the
- * largest grid the current device can run.  max_seq_len and max_ctas are
+ * Workspace for pkv_paged_attention_decode and
+ * pkv_paged_attention_decode_append, in bytes (never 0): room for a
+ * per-sequence work prefix and two partial results per CTA of the largest
+ * grid the current device can run.  max_seq_len and max_ctas are
  * accepted for forward compatibility; block_size must be 16.
  */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim,
@@ -241,6 +243,49 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n
                                       float scale, int32_t max_ctas, void* out,
                                       void* workspace, size_t workspace_bytes,
                                       int32_t* err_word, void* stream);
+
+/*
+ * pkv_paged_attention_decode_shared_prefix - decode attention that reads a
+ * prefix shared by every sequence once per step.
+ *
+ * "nano-vLLM", Where the time went and Next steps 3: with a common prompt,
+ * gathering per user reads the shared prefix blocks once per user; a kernel
+ * that reads blocks in place should read them once.  The caller declares
+ * that the first shared_prefix_blocks entries of every row of
+ * block_tables are the same blocks (row 0's entries are used).  Each KV
+ * head's prefix keys are read once for all sequences and every sequence's
+ * query rows attend over the prefix tokens they can see (min(seq_lens[b],
+ * shared_prefix_blocks * bs)) in runs of the prefix blocks, several
+ * sequences' rows sharing each tensor-core tile; the blocks after the
+ * prefix are walked as in pkv_paged_attention_decode, continuing each
+ * sequence's softmax from its combined prefix runs.  The output is the same attention as
+ * pkv_paged_attention_decode (within the dtype's tolerance; not bit-equal:
+ * the sums are taken in another order).  A row whose first entries differ
+ * from row 0's, where the sequence reaches them, is reported as
+ * PKV_DEVERR_PREFIX.  shared_prefix_blocks = 0 is plain decode.
+ *
+ *   shared_prefix_blocks  0 .. max_blocks_per_seq (else PKV_ERR_RANGE)
+ *   workspace   at least pkv_decode_shared_prefix_workspace_bytes(...)
+ *               (the decode workspace plus up to 16 prefix partials per
+ *               query row, at most 1,024 per query head)
+ *   everything else as for pkv_paged_attention_decode
+ */
+size_t pkv_decode_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t n_heads,
+                                                int32_t head_dim, int32_t max_seq_len,
+                                                int32_t shared_prefix_blocks, int32_t max_ctas,
+                                                int32_t block_size);
+
+pkv_status pkv_paged_attention_decode_shared_prefix(const void* q, int32_t num_seqs,
+                                                    int32_t n_heads, const void* k_pool,
+                                                    const void* v_pool,
+                                                    const pkv_pool_desc* pool,
+                                                    const int32_t* block_tables,
+                                                    int32_t max_blocks_per_seq,
+                                                    const int32_t* seq_lens, int32_t max_seq_len,
+                                                    int32_t shared_prefix_blocks, float scale,
+                                                    int32_t max_ctas, void* out, void* workspace,
+                                                    size_t workspace_bytes, int32_t* err_word,
+                                                    void* stream);
 
 /*
  * pkv_paged_attention_decode_append - write this step's K/V and run decode

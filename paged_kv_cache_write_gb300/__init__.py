@@ -74,6 +74,12 @@ def _load():
     L.pkv_paged_attention_decode.restype = _i32
     L.pkv_paged_attention_decode.argtypes = [_p, _i32, _i32, _p, _p, _desc, _p, _i32, _p, _i32,
                                              _f, _i32, _p, _p, _sz, _p, _p]
+    L.pkv_decode_shared_prefix_workspace_bytes.restype = _sz
+    L.pkv_decode_shared_prefix_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32]
+    L.pkv_paged_attention_decode_shared_prefix.restype = _i32
+    L.pkv_paged_attention_decode_shared_prefix.argtypes = [_p, _i32, _i32, _p, _p, _desc, _p, _i32,
+                                                           _p, _i32, _i32, _f, _i32, _p, _p, _sz,
+                                                           _p, _p]
     L.pkv_paged_attention_decode_append.restype = _i32
     L.pkv_paged_attention_decode_append.argtypes = [_p, _p, _p, _i32, _i32, _p, _p, _desc, _p,
                                                     _i32, _p, _i32, _f, _i32, _p, _p, _sz, _p, _p]
@@ -246,6 +252,42 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, seq_lens, scale: flo
         _dev(out, "out", k_pool.dtype), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _opt(err, "err", torch.int32),
         _stream(stream)))
+    return out
+
+
+def decode_shared_prefix_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len,
+                                         shared_prefix_blocks, max_ctas=0, block_size=16):
+    return int(_load().pkv_decode_shared_prefix_workspace_bytes(
+        num_seqs, n_heads, head_dim, max_seq_len, shared_prefix_blocks, max_ctas, block_size))
+
+
+def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
+                                         shared_prefix_blocks: int,
+                                         max_seq_len: int | None = None, *, out=None,
+                                         workspace=None, max_ctas: int = 0, err=None,
+                                         stream=None):
+    """Decode attention where the first ``shared_prefix_blocks`` table
+    entries of every sequence are the same blocks, read once per step."""
+    desc = pool_desc(k_pool)
+    B, H, hd = q.shape
+    W = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if B else 0
+    if out is None:
+        out = torch.empty_like(q)
+    need = decode_shared_prefix_workspace_bytes(B, H, hd, max_seq_len, shared_prefix_blocks,
+                                                max_ctas, desc.block_size)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("pkv_paged_attention_decode_shared_prefix",
+           _load().pkv_paged_attention_decode_shared_prefix(
+               _dev(q, "q", k_pool.dtype), B, H, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+               ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32), W,
+               _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len),
+               int(shared_prefix_blocks), float(scale), int(max_ctas),
+               _dev(out, "out", k_pool.dtype), _dev(workspace, "workspace"),
+               workspace.numel() * workspace.element_size(), _opt(err, "err", torch.int32),
+               _stream(stream)))
     return out
 
 

@@ -144,18 +144,33 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t hea
   if (num_seqs < 0) num_seqs = 0;
   if (n_heads < 1) n_heads = 1;
   if (head_dim < 1) head_dim = 1;
-  return pkv::decode_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len, max_ctas);
+  return pkv::decode_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len, max_ctas, 0);
+}
+
+size_t pkv_decode_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t n_heads,
+                                                int32_t head_dim, int32_t max_seq_len,
+                                                int32_t shared_prefix_blocks, int32_t max_ctas,
+                                                int32_t block_size) {
+  (void)block_size;
+  if (num_seqs < 0) num_seqs = 0;
+  if (n_heads < 1) n_heads = 1;
+  if (head_dim < 1) head_dim = 1;
+  if (shared_prefix_blocks < 0) shared_prefix_blocks = 0;
+  return pkv::decode_workspace_bytes(num_seqs, n_heads, head_dim, max_seq_len, max_ctas,
+                                     shared_prefix_blocks);
 }
 
 namespace {
 
-// Shared body of the decode entry points; k_new / v_new null: plain decode.
+// Shared body of the decode entry points; k_new / v_new null: plain
+// decode; prefix_blocks > 0: the leading table entries are shared.
 pkv_status decode_entry(const void* q, const void* k_new, const void* v_new, int32_t num_seqs,
                         int32_t n_heads, const void* k_pool, const void* v_pool,
                         const pkv_pool_desc* pool, const int32_t* block_tables,
                         int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
-                        float scale, int32_t max_ctas, void* out, void* workspace,
-                        size_t workspace_bytes, int32_t* err_word, void* stream) {
+                        int32_t prefix_blocks, float scale, int32_t max_ctas, void* out,
+                        void* workspace, size_t workspace_bytes, int32_t* err_word,
+                        void* stream) {
   PoolShape shape;
   pkv_status st = check_attention(q, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
                                   max_blocks_per_seq, seq_lens, max_seq_len, scale, out, &shape);
@@ -165,9 +180,10 @@ pkv_status decode_entry(const void* q, const void* k_new, const void* v_new, int
   if (num_seqs == 0) return PKV_OK;
   if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_NULL;
   if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_ALIGN;
+  if (prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq) return PKV_ERR_RANGE;
   if (!workspace) return PKV_ERR_WORKSPACE;
   if (workspace_bytes < pkv::decode_workspace_bytes(num_seqs, n_heads, shape.head_dim,
-                                                    max_seq_len, max_ctas))
+                                                    max_seq_len, max_ctas, prefix_blocks))
     return PKV_ERR_WORKSPACE;
   if (!aligned16(workspace)) return PKV_ERR_ALIGN;
   pkv::AttnArgs a{};
@@ -191,6 +207,7 @@ pkv_status decode_entry(const void* q, const void* k_new, const void* v_new, int
   a.workspace_bytes = workspace_bytes;
   a.k_new = k_new;
   a.v_new = v_new;
+  a.prefix_blocks = prefix_blocks;
   a.err = err_word;
   return from_cuda(pkv::launch_decode(a, as_stream(stream)));
 }
@@ -205,8 +222,19 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n
                                       void* out, void* workspace, size_t workspace_bytes,
                                       int32_t* err_word, void* stream) {
   return decode_entry(q, nullptr, nullptr, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
-                      max_blocks_per_seq, seq_lens, max_seq_len, scale, max_ctas, out, workspace,
-                      workspace_bytes, err_word, stream);
+                      max_blocks_per_seq, seq_lens, max_seq_len, 0, scale, max_ctas, out,
+                      workspace, workspace_bytes, err_word, stream);
+}
+
+pkv_status pkv_paged_attention_decode_shared_prefix(
+    const void* q, int32_t num_seqs, int32_t n_heads, const void* k_pool, const void* v_pool,
+    const pkv_pool_desc* pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens, int32_t max_seq_len, int32_t shared_prefix_blocks, float scale,
+    int32_t max_ctas, void* out, void* workspace, size_t workspace_bytes, int32_t* err_word,
+    void* stream) {
+  return decode_entry(q, nullptr, nullptr, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
+                      max_blocks_per_seq, seq_lens, max_seq_len, shared_prefix_blocks, scale,
+                      max_ctas, out, workspace, workspace_bytes, err_word, stream);
 }
 
 pkv_status pkv_paged_attention_decode_append(
@@ -217,8 +245,8 @@ pkv_status pkv_paged_attention_decode_append(
     void* stream) {
   if (num_seqs > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_NULL;
   return decode_entry(q, k_new, v_new, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
-                      max_blocks_per_seq, seq_lens, max_seq_len, scale, max_ctas, out, workspace,
-                      workspace_bytes, err_word, stream);
+                      max_blocks_per_seq, seq_lens, max_seq_len, 0, scale, max_ctas, out,
+                      workspace, workspace_bytes, err_word, stream);
 }
 
 size_t pkv_prefill_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }

@@ -38,6 +38,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include <type_traits>
 
 #include "device.cuh"
@@ -92,6 +94,30 @@ struct MmaRows {
     }
 #pragma unroll
     for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  }
+
+  // Continue from a partial result instead of from nothing (call after
+  // begin): part_row(r) -> the row's normalised output (fp32, nullptr =
+  // inactive row), ml_row(r) -> its max (log2 units) and exp-sum.
+  template <typename PartRow, typename MlRow>
+  __device__ __forceinline__ void seed(PartRow part_row, MlRow ml_row) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float* pp = part_row(g + 8 * h);
+      if (!pp) continue;
+      const float* ml = ml_row(g + 8 * h);
+      const float lsum = ml[1];
+      m[h] = ml[0];
+      l[h] = c == 0 ? lsum : 0.f;  // the four lanes of a row are summed at the end
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        const float2 x = *reinterpret_cast<const float2*>(pp + i * 8 + 2 * c);
+        o[i][2 * h] = x.x * lsum;
+        o[i][2 * h + 1] = x.y * lsum;
+      }
+    }
   }
 
   // One 16-token block.  k_tile / v_tile point at token 0 of this warp's KV
@@ -261,6 +287,23 @@ struct SimtRows {
       for (int i = 0; i < HD / 16; ++i) o[k][i] = 0.f;
     }
     __syncwarp();
+  }
+
+  // Continue from a partial result (see MmaRows::seed).
+  template <typename PartRow, typename MlRow>
+  __device__ __forceinline__ void seed(PartRow part_row, MlRow ml_row) {
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 15, hw = lane >> 4;
+#pragma unroll
+    for (int k = 0; k < RPH; ++k) {
+      const float* pp = part_row(hw + 2 * k);
+      if (!pp) continue;
+      const float* ml = ml_row(hw + 2 * k);
+      m[k] = ml[0];
+      l[k] = ml[1];
+#pragma unroll
+      for (int i = 0; i < HD / 16; ++i) o[k][i] = pp[t + 16 * i] * ml[1];
+    }
   }
 
   __device__ __forceinline__ void block(const uint8_t* k_tile, const uint8_t* v_tile, int stride,
@@ -479,6 +522,15 @@ struct DecodeParams {
   float* ws_ml;       // [2 * grid][HG * rep][2] partial max (log2 units) and exp-sum
   int B, n_heads, n_kv, rep, hg_size, n_groups, W, num_blocks, max_len, max_seq_len, head_dim;
   int elem_bytes, nstages, grid;
+  // shared prefix: every sequence's first prefix_blocks table entries are
+  // the same blocks; the prefix kernel attends over them in prefix_chunks
+  // runs of prefix_bpc blocks and leaves per-row partials in pre_o /
+  // pre_ml, and units here cover only the blocks after the prefix (0: no
+  // shared prefix)
+  int prefix_blocks, prefix_chunks, prefix_bpc;
+  int prefix_seed_run;  // run slot holding the combined prefix partials
+  float* pre_o;   // [chunks][B][n_heads][HD] normalised prefix outputs
+  float* pre_ml;  // [chunks][B][n_heads][2] prefix max (log2 units) and exp-sum
   int plan_in_kernel;  // 1: each CTA scans the lengths itself (no plan kernel)
   float scale_log2;
 };
@@ -549,9 +601,16 @@ constexpr int kPlanSmemSeqs = 8191;
 // Batches up to this size are planned by every main-kernel CTA itself.
 constexpr int kKernelPlanSeqs = 2048;
 
+// Blocks of a sequence of L tokens that this kernel walks (those after the
+// shared prefix).
+__device__ __forceinline__ int walked_blocks(const DecodeParams& p, int L) {
+  const int n = (L + kBS - 1) / kBS - p.prefix_blocks;
+  return n > 0 ? n : 0;
+}
+
 // Units (16-token blocks x head groups) of sequence b.
 __device__ __forceinline__ int units_of(const DecodeParams& p, int b) {
-  return p.n_groups * ((used_len(p, b) + kBS - 1) / kBS);
+  return p.n_groups * walked_blocks(p, used_len(p, b));
 }
 
 __device__ __forceinline__ void check_length(const DecodeParams& p, int b) {
@@ -641,17 +700,20 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     int4 st = make_int4(0, 0, 0, 0);
     if (r0 < range_begin(c + 1, U, p.grid)) {
       const int b = seq_of_unit(cu, p.B, r0);
-      const int nblk = (used_len(p, b) + kBS - 1) / kBS;
+      const int nblk = walked_blocks(p, used_len(p, b));
       const int grp = (r0 - cu[b]) / nblk;
       st = make_int4(b, grp, (r0 - cu[b]) - grp * nblk, 0);
     }
     p.starts[c] = st;
   }
-  zero_empty<T, HD>(p, 0, 1, [&](int b) { return used_len(p, b) == 0; });
+  if (p.prefix_blocks == 0)  // with a prefix, the prefix kernel writes them
+    zero_empty<T, HD>(p, 0, 1, [&](int b) { return used_len(p, b) == 0; });
 }
 
 // Walks this CTA's contiguous range of units segment by segment: a segment
 // is the run of units of one (sequence, head group) inside the range.
+// j counts the walked blocks of the group (block prefix_blocks + j of the
+// table); nblk is how many there are.
 struct Cursor {
   int b, grp, j, L, nblk;
 
@@ -660,7 +722,7 @@ struct Cursor {
     grp = st.y;
     j = st.z;
     L = used_len(p, b);
-    nblk = (L + kBS - 1) / kBS;
+    nblk = walked_blocks(p, L);
   }
   // advance past n units of the current group
   __device__ __forceinline__ void advance(const DecodeParams& p, int n) {
@@ -670,10 +732,13 @@ struct Cursor {
     if (++grp < p.n_groups) return;
     grp = 0;
     do {
-      ++b;
-      L = b < p.B ? used_len(p, b) : 1;
-    } while (L == 0);
-    nblk = (L + kBS - 1) / kBS;
+      if (++b >= p.B) {  // past the last unit: never used
+        nblk = 1;
+        return;
+      }
+      L = used_len(p, b);
+      nblk = walked_blocks(p, L);
+    } while (nblk == 0);
   }
 };
 
@@ -751,11 +816,12 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
     const int r0 = range_begin(blockIdx.x, U, G);
     if (r0 < range_begin(blockIdx.x + 1, U, G)) {
       const int b = seq_of_unit(cu_s, p.B, r0);
-      const int nblk = (used_len(p, b) + kBS - 1) / kBS;
+      const int nblk = walked_blocks(p, used_len(p, b));
       const int grp = (r0 - cu_s[b]) / nblk;
       st = make_int4(b, grp, (r0 - cu_s[b]) - grp * nblk, 0);
     }
-    zero_empty<T, HD>(p, blockIdx.x, G, [&](int b) { return cu_s[b + 1] == cu_s[b]; });
+    if (p.prefix_blocks == 0)  // with a prefix, the prefix kernel writes them
+      zero_empty<T, HD>(p, blockIdx.x, G, [&](int b) { return cu_s[b + 1] == cu_s[b]; });
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.total_units = U;
     fence_proxy_async_smem();  // the scan's stores come before the ring's copies
     __syncthreads();
@@ -779,12 +845,12 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
       const int32_t* row = p.bt + int64_t(cur.b) * p.W;
       const int64_t head_off = int64_t(cur.grp) * p.hg_size * HD * p.elem_bytes;
       for (int jj = 0; jj < n && ok; jj += 32) {
-        int id = (jj + lane < n) ? __ldg(row + cur.j + jj + lane) : 0;
+        int id = (jj + lane < n) ? __ldg(row + p.prefix_blocks + cur.j + jj + lane) : 0;
         const int n_here = min(32, n - jj);
         for (int k = 0; k < n_here; ++k) {
           if (*ring.abort_flag) { ok = false; break; }
           const int blk = __shfl_sync(0xffffffffu, id, k);
-          const int j = cur.j + jj + k;
+          const int j = p.prefix_blocks + cur.j + jj + k;  // table index
           int valid = min(kBS, cur.L - j * kBS);
           if (blk < 0 || blk >= p.num_blocks) {
             if (lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
@@ -793,7 +859,7 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
           const int64_t off = int64_t(valid > 0 ? blk : 0) * kBS * token_pitch + head_off;
           // append: the step's token is the last of the sequence; its row
           // comes from k_new / v_new, which this CTA also stores to the pool
-          const bool fresh = p.k_new != nullptr && j == cur.nblk - 1 && valid > 0 &&
+          const bool fresh = p.k_new != nullptr && j == p.prefix_blocks + cur.nblk - 1 && valid > 0 &&
                              __ldg(p.seq_lens + cur.b) == cur.L;  // not a clamped bad length
           const int new_row = fresh ? cur.L - 1 - j * kBS : -1;
           const int64_t new_off = int64_t(cur.b) * p.n_kv * HD * p.elem_bytes + head_off;
@@ -825,7 +891,7 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
     // the split group this CTA merges (read by the merge kernel)
     if (lane == 0) {
       p.splits[blockIdx.x] = r0 < r1 ? split_entry(blockIdx.x, G, U, st.x, st.y, st.z,
-                                                   (used_len(p, st.x) + kBS - 1) / kBS)
+                                                   walked_blocks(p, used_len(p, st.x)))
                                      : make_int4(-1, 0, 0, 0);
     }
   } else if (warp < consumers) {
@@ -850,6 +916,13 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
             return r < p.rep ? q + (int64_t(b) * p.n_heads + head0 + r) * HD : nullptr;
           },
           [&](int) { return last; });
+      if (p.prefix_blocks > 0 && cur.j == 0) {
+        // the group's first walked block: continue from the shared prefix
+        const int64_t prow = int64_t(p.prefix_seed_run) * p.B * p.n_heads +
+                             int64_t(b) * p.n_heads + head0;
+        rows.seed([&](int r) -> const float* { return r < p.rep ? p.pre_o + (prow + r) * HD : nullptr; },
+                  [&](int r) -> const float* { return p.pre_ml + (prow + r) * 2; });
+      }
       for (int k = 0; k < n; ++k) {
         if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
           *ring.abort_flag = 1;
@@ -859,7 +932,7 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
         const int st = static_cast<int>(it % ring.nstages);
         const int hoff = warp * HD * p.elem_bytes;
         rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride,
-                   (cur.j + k) * kBS, p.scale_log2);
+                   (p.prefix_blocks + cur.j + k) * kBS, p.scale_log2);
         ring_release(ring, it);
         ++it;
       }
@@ -880,6 +953,164 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
       u += n;
       cur.advance(p, n);
     }
+  }
+}
+
+// Shared-prefix attention: the first prefix_blocks table entries are the
+// same blocks for every sequence (a common prompt), so they are read once
+// for a whole chunk of sequences instead of once per sequence.  The prefix
+// is cut into prefix_chunks runs of prefix_bpc blocks.  CTA (head group g,
+// key run kc; sequences s0 ..): a producer warp streams run kc's blocks
+// (row 0's table, the group's heads of each token, as in the main kernel)
+// through the shared-memory ring; consumer warp w (KV head g*hg + w) packs
+// the query rows of several sequences into one set of rows (sequence
+// s0 + r / rep, query head r % rep), all of which see the same keys, and
+// leaves a normalised partial per row and run.  The main kernel combines a
+// sequence's runs when it starts the sequence's first walked block; a
+// sequence wholly inside the prefix gets its output from the main kernel's
+// end.  Consumer warp 0 also checks that each sequence's table starts with
+// row 0's blocks in this run.
+template <typename T, int HD, int MAXR, bool MMA>
+__global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_prefix_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using Rows = typename RowsOf<T, HD, MAXR, MMA>::type;
+  constexpr int R = MMA ? 16 : MAXR;  // rows one warp carries
+  const int consumers = p.hg_size;
+  const int row_bytes = p.hg_size * HD * p.elem_bytes;
+  Ring ring = make_ring(smem, p.nstages, row_bytes);
+  ring_init(ring, consumers);
+  pdl_wait();  // inputs written by the preceding kernel
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.prefix_chunks;
+  const int g = blockIdx.x / K, kc = blockIdx.x - (blockIdx.x / K) * K;
+  const int j0 = kc * p.prefix_bpc;
+  const int j1 = min(p.prefix_blocks, j0 + p.prefix_bpc);
+  const int pre_len = p.prefix_blocks * kBS;
+  const int spc = R / p.rep;  // sequences per CTA
+  const int s0 = blockIdx.y * spc;
+  const int64_t token_pitch = int64_t(p.n_kv) * HD * p.elem_bytes;
+  const int64_t head_off = int64_t(g) * p.hg_size * HD * p.elem_bytes;
+  if (warp == consumers) {
+    // ------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int jb = j0; jb < j1 && ok; jb += 32) {
+      const int id = jb + lane < j1 ? __ldg(p.bt + jb + lane) : 0;  // row 0's table
+      for (int k = 0; k < min(32, j1 - jb); ++k) {
+        if (*ring.abort_flag) { ok = false; break; }
+        const int blk = __shfl_sync(0xffffffffu, id, k);
+        int valid = kBS;
+        if (blk < 0 || blk >= p.num_blocks) {
+          if (lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
+          valid = 0;
+        }
+        const int64_t off = int64_t(valid > 0 ? blk : 0) * kBS * token_pitch + head_off;
+        if (!ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err)) {
+          *ring.abort_flag = 1;
+          ok = false;
+          break;
+        }
+        ++it;
+      }
+    }
+    if (!ok) ring_drain(ring, it);
+    return;
+  }
+  if (warp > consumers) return;
+  // ------------------------------------------------------ consumers
+  if (warp == 0) {
+    for (int s = 0; s < spc && s0 + s < p.B; ++s) {
+      const int b = s0 + s;
+      const int vis = min(used_len(p, b), pre_len);
+      for (int j = j0 + lane; j < min(j1, (vis + kBS - 1) / kBS); j += 32)
+        if (__ldg(p.bt + int64_t(b) * p.W + j) != __ldg(p.bt + j)) report(p.err, PKV_DEVERR_PREFIX);
+    }
+  }
+  Rows rows;
+  if constexpr (!MMA) {
+    float* scratch = reinterpret_cast<float*>(ring.stages + p.nstages * ring.stage_bytes);
+    rows.bind(scratch + warp * RowsOf<T, HD, MAXR, MMA>::kScratch);
+  }
+  const T* q = static_cast<const T*>(p.q);
+  const int head0 = (g * p.hg_size + warp) * p.rep;  // first query head of this KV head
+  auto seq_of = [&](int r) { return s0 + r / p.rep; };
+  auto active = [&](int r) { return r < spc * p.rep && seq_of(r) < p.B; };
+  auto row_of = [&](int r) { return int64_t(seq_of(r)) * p.n_heads + head0 + r % p.rep; };
+  rows.begin([&](int r) -> const T* { return active(r) ? q + row_of(r) * HD : nullptr; },
+             [&](int r) { return active(r) ? min(used_len(p, seq_of(r)), pre_len) - 1 : -1; });
+  const int hoff = warp * HD * p.elem_bytes;
+  for (uint32_t it = 0; it < static_cast<uint32_t>(j1 - j0); ++it) {
+    if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
+      *ring.abort_flag = 1;
+      return;
+    }
+    const int st = static_cast<int>(it % ring.nstages);
+    rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride,
+               (j0 + static_cast<int>(it)) * kBS, p.scale_log2);
+    ring_release(ring, it);
+  }
+  const int64_t part = int64_t(kc) * p.B * p.n_heads;  // run kc's rows
+  rows.store_partial(
+      [&](int r) -> float* { return active(r) ? p.pre_o + (part + row_of(r)) * HD : nullptr; },
+      [&](int r) -> float* { return p.pre_ml + (part + row_of(r)) * 2; });
+}
+
+// Combine the prefix runs of every (sequence, query head) row with
+// log-sum-exp weights: one thread per 4 output dims of a row.  Rows of a
+// sequence that lies wholly inside the prefix (length 0 included) get the
+// final output; the others a normalised partial in run slot prefix_chunks,
+// which the main kernel continues from.
+constexpr int kMaxPrefixRuns = 16;
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) decode_prefix_combine_kernel(DecodeParams p) {
+  pdl_wait();  // the prefix runs
+  pdl_launch_dependents();
+  constexpr int V = HD / 4;
+  const int64_t rows = int64_t(p.B) * p.n_heads;
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows * V) return;
+  const int64_t row = i / V;
+  const int e = static_cast<int>(i - row * V) * 4;
+  const int K = p.prefix_chunks;
+  float mk[kMaxPrefixRuns], lk[kMaxPrefixRuns];
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kMaxPrefixRuns; ++k) {
+    mk[k] = -INFINITY;
+    lk[k] = 0.f;
+    if (k < K) {
+      const float2 x = *reinterpret_cast<const float2*>(p.pre_ml + (k * rows + row) * 2);
+      mk[k] = x.x;
+      lk[k] = x.y;
+    }
+    if (lk[k] > 0.f) M = fmaxf(M, mk[k]);  // a run that saw no key has no weight
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxPrefixRuns; ++k) {
+    if (k < K) {
+      const float w = lk[k] > 0.f ? fast_exp2(mk[k] - M) * lk[k] : 0.f;
+      den += w;
+      const float4 o = *reinterpret_cast<const float4*>(p.pre_o + (k * rows + row) * HD + e);
+      acc = make_float4(fmaf(w, o.x, acc.x), fmaf(w, o.y, acc.y), fmaf(w, o.z, acc.z),
+                        fmaf(w, o.w, acc.w));
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const int b = static_cast<int>(row / p.n_heads);
+  if (used_len(p, b) <= p.prefix_blocks * kBS) {
+    T* out = static_cast<T*>(p.out) + row * HD + e;
+    out[0] = Elem<T>::from_f(acc.x * inv);
+    out[1] = Elem<T>::from_f(acc.y * inv);
+    out[2] = Elem<T>::from_f(acc.z * inv);
+    out[3] = Elem<T>::from_f(acc.w * inv);
+  } else {
+    *reinterpret_cast<float4*>(p.pre_o + (K * rows + row) * HD + e) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (e == 0) *reinterpret_cast<float2*>(p.pre_ml + (K * rows + row) * 2) = make_float2(M, den);
   }
 }
 
@@ -1165,12 +1396,35 @@ size_t merge_smem_bytes(int rows, int hd) {
   return size_t(merge_head_bytes(rows, P)) + size_t(P) * rows * hd * 4;
 }
 
+// Runs the shared prefix is cut into for the prefix kernel: enough CTAs
+// (head groups x sequence chunks x runs) to fill about two per SM, at most
+// kMaxPrefixRuns runs and at most 1,024 run-rows per query head (which
+// bounds the partials' workspace), at least one block per run.  *bpc =
+// blocks per run.  One more slot holds the combined partials.
+int max_prefix_runs(int num_seqs, int prefix_blocks) {
+  const int k = 1024 / (num_seqs > 0 ? num_seqs : 1);
+  return std::max(1, std::min({kMaxPrefixRuns, prefix_blocks, std::max(1, k)}));
+}
+int prefix_slots(int runs) { return runs > 0 ? runs + 1 : 0; }
+
+int prefix_runs(int num_seqs, int n_groups, int seqs_per_cta, int prefix_blocks, int* bpc) {
+  const int base = n_groups * ((num_seqs + seqs_per_cta - 1) / seqs_per_cta);
+  int k = (2 * sm_count() + base - 1) / base;
+  k = std::max(1, std::min(k, max_prefix_runs(num_seqs, prefix_blocks)));
+  *bpc = (prefix_blocks + k - 1) / k;
+  return (prefix_blocks + *bpc - 1) / *bpc;
+}
+
 // Decode workspace layout: cu_units [B+1] | starts [G] | splits [G] |
 // total units | partial max/sum [2G][rows][2] | partial outputs
-// [2G][rows][HD], each region 256-byte aligned.
+// [2G][rows][HD] | with a shared prefix: prefix partial outputs
+// [runs][B][n_heads][HD] and max/sum [runs][B][n_heads][2]; each region
+// 256-byte aligned.
 struct DecodeWs {
-  size_t cu, starts, splits, total_units, ml, o, total;
-  DecodeWs(int num_seqs, size_t G, size_t rows_per_group, int head_dim) {
+  size_t cu, starts, splits, total_units, ml, o, pre_o, pre_ml, total;
+  // prefix_heads: runs x n_heads with a shared prefix (its partials
+  // follow), else 0
+  DecodeWs(int num_seqs, size_t G, size_t rows_per_group, int head_dim, int prefix_heads = 0) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     cu = 0;
     starts = up(size_t(num_seqs + 1) * 4);
@@ -1178,12 +1432,15 @@ struct DecodeWs {
     total_units = splits + up(G * 16);
     ml = total_units + 256;
     o = ml + up(2 * G * rows_per_group * 2 * 4);
-    total = o + 2 * G * rows_per_group * size_t(head_dim) * 4;
+    pre_o = o + up(2 * G * rows_per_group * size_t(head_dim) * 4);
+    pre_ml = pre_o + up(size_t(num_seqs) * prefix_heads * head_dim * 4);
+    total = pre_ml + size_t(num_seqs) * prefix_heads * 2 * 4;
   }
 };
 
 template <typename T, int HD, int MAXR, bool MMA>
 struct DecodeLaunch {
+  static constexpr int kRowsPerWarp = MMA ? 16 : MAXR;  // query rows one consumer warp carries
   static size_t scratch_bytes(int warps) {
     return MMA ? 0 : size_t(warps) * RowsOf<T, HD, MAXR, MMA>::kScratch * sizeof(float);
   }
@@ -1238,7 +1495,14 @@ struct DecodeLaunch {
     if (e != cudaSuccess) return e;
     if (G > 65535) return cudaErrorInvalidValue;  // split entries pack CTA indices in 16 bits
     p.grid = G;
-    const DecodeWs L(a.num_seqs, G, size_t(hg) * p.rep, HD);
+    p.prefix_blocks = a.prefix_blocks;
+    p.prefix_chunks = 0;
+    if (p.prefix_blocks > 0)
+      p.prefix_chunks = prefix_runs(p.B, p.n_groups, kRowsPerWarp / p.rep, p.prefix_blocks,
+                                    &p.prefix_bpc);
+    p.prefix_seed_run = p.prefix_chunks;
+    const DecodeWs L(a.num_seqs, G, size_t(hg) * p.rep, HD,
+                     prefix_slots(p.prefix_chunks) * a.n_heads);
     if (L.total > a.workspace_bytes) return cudaErrorInvalidValue;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     p.cu_units = reinterpret_cast<int32_t*>(ws + L.cu);
@@ -1247,6 +1511,35 @@ struct DecodeLaunch {
     p.total_units = reinterpret_cast<int32_t*>(ws + L.total_units);
     p.ws_ml = reinterpret_cast<float*>(ws + L.ml);
     p.ws_o = reinterpret_cast<float*>(ws + L.o);
+    p.pre_o = reinterpret_cast<float*>(ws + L.pre_o);
+    p.pre_ml = reinterpret_cast<float*>(ws + L.pre_ml);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (p.prefix_blocks > 0) {
+      // the shared prefix: runs of its blocks, each read once per head group
+      // for a chunk of sequences (same ring and shared memory as below)
+      static KernelSetup prefix_setup;
+      e = kernel_setup(prefix_setup, decode_prefix_kernel<T, HD, MAXR, MMA>,
+                       static_cast<int>(smem), (hg + 1) * 32, nullptr);
+      if (e != cudaSuccess) return e;
+      const int spc = kRowsPerWarp / p.rep;
+      cudaLaunchConfig_t pcfg = {};
+      pcfg.gridDim = dim3(p.n_groups * p.prefix_chunks, (p.B + spc - 1) / spc);
+      pcfg.blockDim = dim3((hg + 1) * 32);
+      pcfg.dynamicSmemBytes = smem;
+      pcfg.stream = stream;
+      pcfg.attrs = attr;
+      pcfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&pcfg, decode_prefix_kernel<T, HD, MAXR, MMA>, p);
+      if (e != cudaSuccess) return e;
+      const int64_t threads = int64_t(p.B) * p.n_heads * (HD / 4);
+      pcfg.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
+      pcfg.blockDim = dim3(256);
+      pcfg.dynamicSmemBytes = 0;
+      e = cudaLaunchKernelEx(&pcfg, decode_prefix_combine_kernel<T, HD>, p);
+      if (e != cudaSuccess) return e;
+    }
     // small batches: every CTA scans the lengths in its ring stages
     const size_t ring_bytes = smem - kBarrierBytes - scratch_bytes(hg);
     p.plan_in_kernel =
@@ -1262,9 +1555,6 @@ struct DecodeLaunch {
     cfg.blockDim = dim3((hg + 1) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, decode_kernel<T, HD, MAXR, MMA>, p);
@@ -1291,7 +1581,14 @@ size_t decode_exact_workspace(const AttnArgs& a, int hg) {
   int G = 0, nstages = 0;
   size_t smem = 0;
   if (DecodeLaunch<T, HD, MAXR, MMA>::grid(a, hg, &G, &smem, &nstages) != cudaSuccess) return 0;
-  return DecodeWs(a.num_seqs, G, size_t(hg) * (a.n_heads / a.pool.n_kv), HD).total;
+  int runs = 0, bpc = 0;
+  if (a.prefix_blocks > 0)
+    runs = prefix_runs(a.num_seqs, a.pool.n_kv / hg,
+                       DecodeLaunch<T, HD, MAXR, MMA>::kRowsPerWarp / (a.n_heads / a.pool.n_kv),
+                       a.prefix_blocks, &bpc);
+  return DecodeWs(a.num_seqs, G, size_t(hg) * (a.n_heads / a.pool.n_kv), HD,
+                  prefix_slots(runs) * a.n_heads)
+      .total;
 }
 
 template <typename T, int HD, int MAXR, bool MMA>
@@ -1366,9 +1663,14 @@ bool prefill_supported(const PoolShape& pool, int32_t n_heads) { return decode_s
 int32_t decode_default_partition(int32_t, int32_t, int32_t, int32_t) { return 0; }
 
 // Upper bound of the decode workspace over every grid this device can run.
-size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim, int32_t, int32_t) {
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim, int32_t, int32_t,
+                              int32_t shared_prefix_blocks) {
   // rows per head group <= n_heads; at most 16 resident CTAs per SM
-  return DecodeWs(num_seqs, size_t(sm_count()) * 16, size_t(n_heads), head_dim).total;
+  return DecodeWs(num_seqs, size_t(sm_count()) * 16, size_t(n_heads), head_dim,
+                  shared_prefix_blocks > 0
+                      ? prefix_slots(max_prefix_runs(num_seqs, shared_prefix_blocks)) * n_heads
+                      : 0)
+      .total;
 }
 
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s) {

@@ -52,6 +52,8 @@ struct AttnArgs {
   // then k_pool / v_pool are only read)
   const void* k_new;
   const void* v_new;
+  // decode: leading table entries shared by every sequence (0: none)
+  int32_t prefix_blocks;
   void* workspace;
   size_t workspace_bytes;
   int32_t* err;
@@ -62,7 +64,8 @@ bool decode_supported(const PoolShape& pool, int32_t n_heads);
 int32_t decode_default_partition(int32_t num_seqs, int32_t n_kv, int32_t max_seq_len,
                                  int32_t block_size);
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim,
-                              int32_t max_seq_len, int32_t partition_tokens);
+                              int32_t max_seq_len, int32_t partition_tokens,
+                              int32_t shared_prefix_blocks);
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream);
 // Workspace the decode launch for `a` needs on the current device (0 on error).
 size_t decode_workspace_bytes_exact(const AttnArgs& a);

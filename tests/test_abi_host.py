@@ -120,6 +120,26 @@ def test_decode_host_checks(pkv):
     assert _decode(pkv, B=0) == 0
 
 
+def _prefix(pkv, P, **over):
+    a = dict(q=FAKE, B=2, H=8, k=FAKE, v=FAKE, desc=_desc(pkv), bt=FAKE, W=4, sl=FAKE, maxlen=64,
+             scale=0.125, max_ctas=0, out=FAKE, ws=FAKE, wsb=1 << 40, err=None)
+    a.update(over)
+    return pkv.lib.pkv_paged_attention_decode_shared_prefix(
+        a["q"], a["B"], a["H"], a["k"], a["v"], ctypes.byref(a["desc"]), a["bt"], a["W"], a["sl"],
+        a["maxlen"], P, a["scale"], a["max_ctas"], a["out"], a["ws"], a["wsb"], a["err"], None)
+
+
+def test_decode_shared_prefix_host_checks(pkv):
+    assert _prefix(pkv, -1) == 5
+    assert _prefix(pkv, 5) == 5                        # more shared blocks than a table row has
+    assert _prefix(pkv, 2, q=None) == 1
+    assert _prefix(pkv, 2, H=7) == 2
+    assert _prefix(pkv, 2, ws=None) == 6
+    assert _prefix(pkv, 2, wsb=16) == 6
+    assert _prefix(pkv, 2, desc=_desc(pkv, head_dim=48)) == 7
+    assert _prefix(pkv, 2, B=0) == 0
+
+
 def _append(pkv, **over):
     a = dict(q=FAKE, kn=FAKE, vn=FAKE, B=2, H=8, k=FAKE, v=FAKE, desc=_desc(pkv), bt=FAKE, W=4,
              sl=FAKE, maxlen=64, scale=0.125, max_ctas=0, out=FAKE, ws=FAKE, wsb=1 << 40, err=None)

@@ -1,0 +1,107 @@
+"""Shared-prefix decode on the GPU, through the C ABI: the prefix blocks
+every sequence's table starts with are read once per step, and the result
+must match the float64 oracle (plain decode over each sequence's own
+table) and the plain GPU decode within the dtype's tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_write_gb300 as pkv
+from gpu_step import GpuStep, OracleStep, assert_close, f64
+from workloads import draw_plan, make_layer, make_tiny_layer, tiny_plan
+
+pytestmark = pytest.mark.gpu
+
+PKV_DEVERR_PREFIX = 32
+
+
+def _prefix_decode(g, P, max_ctas=0):
+    t = g.t
+    nd = g.nd
+    return pkv.paged_attention_decode_shared_prefix(
+        t["q"][:nd], t["k_pool"], t["v_pool"], g.bt[:nd], g.seq_lens[:nd], g.sh.scale, P,
+        g.max_dec, max_ctas=max_ctas, err=g.err)
+
+
+WORKLOADS = [("smollm2-135m", 0), ("smollm2-135m", 29), ("llama-3.2-1b-sharedprompt", 0),
+             ("llama-3.2-1b-sharedprompt", 15)]
+
+
+@pytest.mark.parametrize("name,layer_id", WORKLOADS, ids=[f"{n}-L{l}" for n, l in WORKLOADS])
+def test_shared_prefix_workloads(name, layer_id):
+    """SmolLM2 step: 30 sequences share a 2-block (32-token) system prompt;
+    Llama-3.2-1B: 64 sequences behind a 64-block (1,024-token) prompt."""
+    plan = draw_plan(name)
+    P = len(plan.shared_prefix_blocks)
+    assert P > 0 and np.all(plan.block_tables[:, :P] == np.array(plan.shared_prefix_blocks))
+    layer = make_layer(plan, layer_id, fill=1e30)
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.run_write()
+    g.write(g.slots())
+    plain = g.decode()
+    shared = _prefix_decode(g, P)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    ref = o.decode()
+    assert_close(f64(shared), ref, "bf16", f"{name} layer {layer_id}")
+    assert_close(f64(shared), f64(plain), "bf16", "vs plain decode")
+
+
+def _plan_with_prefix(lens, P, H, K, D, dt, seed):
+    shared = tuple(range(1, 1 + P))
+    plan = tiny_plan(lens, [1] * len(lens), n_heads=H, n_kv=K, head_dim=D, block_size=16,
+                     num_blocks=160, dtype=dt, seed=seed, shared=shared)
+    bt = plan.block_tables.copy()
+    if bt.shape[1] < P:
+        bt = np.concatenate([bt, np.zeros((bt.shape[0], P - bt.shape[1]), bt.dtype)], axis=1)
+    bt[:, :P] = shared  # every row starts with the shared blocks, short ones too
+    plan.block_tables = bt
+    return plan
+
+
+SMALL = [  # (n_heads, n_kv, head_dim, dtype)
+    (9, 3, 64, "bf16"), (32, 8, 64, "bf16"), (64, 8, 128, "bf16"), (16, 1, 64, "bf16"),
+    (8, 4, 16, "f32"), (12, 4, 128, "f32"), (4, 2, 32, "bf16"),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[f"{h}x{k}x{d}-{t}" for h, k, d, t in SMALL])
+@pytest.mark.parametrize("P", [1, 2, 5])
+def test_shared_prefix_small_ragged(shape, P):
+    """Lengths inside, at the end of and past the prefix, empty sequences,
+    several grid sizes."""
+    H, K, D, dt = shape
+    lens = [0, 1, 5, 16, 17, 31, 32, 33, 48, 79, 80, 81, 100, 300, 700]
+    plan = _plan_with_prefix(lens, P, H, K, D, dt, seed=H + D + P)
+    layer = make_tiny_layer(plan, seed=D + P, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    # the pools are read as generated (no write step: a length-0 row has no slot)
+    o.kp, o.vp = o.raw["k_pool"], o.raw["v_pool"]
+    ref = o.decode()
+    for max_ctas in (0, 1, 3, 16):
+        out = _prefix_decode(g, P, max_ctas)
+        torch.cuda.synchronize()
+        assert int(g.err.item()) == 0, max_ctas
+        assert_close(f64(out), ref, dt, f"P={P} max_ctas={max_ctas}")
+        assert torch.count_nonzero(out[0].float()) == 0  # length 0
+
+
+def test_shared_prefix_zero_blocks_is_plain_decode():
+    plan = _plan_with_prefix([3, 40, 200], 2, 32, 8, 64, "bf16", seed=1)
+    layer = make_tiny_layer(plan, seed=1)
+    g = GpuStep(plan, layer)
+    plain = g.decode()
+    zero = _prefix_decode(g, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(plain.view(torch.int16), zero.view(torch.int16))
+
+
+def test_shared_prefix_mismatch_reported():
+    """A row whose visible leading entries are not row 0's is reported."""
+    plan = _plan_with_prefix([40, 40, 40], 2, 8, 2, 64, "bf16", seed=2)
+    plan.block_tables[1, 1] = plan.block_tables[1, 2]  # row 1's second prefix entry differs
+    layer = make_tiny_layer(plan, seed=2)
+    g = GpuStep(plan, layer)
+    _prefix_decode(g, 2)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) & PKV_DEVERR_PREFIX

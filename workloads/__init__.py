@@ -81,17 +81,20 @@ SHAPES = {
     # Llama-3.2-1B batch of 32 prompts
     "smollm2-135m-prompts": Shape("smollm2-135m-prompts", "bf16", 30, 9, 3, 64, 16, 1024, True),
     "llama-3.2-1b-prompts": Shape("llama-3.2-1b-prompts", "bf16", 16, 32, 8, 64, 16, 8192, True),
+    # 64 users behind one long common prompt (1,024 tokens, 64 shared blocks)
+    "llama-3.2-1b-sharedprompt": Shape("llama-3.2-1b-sharedprompt", "bf16", 16, 32, 8, 64, 16,
+                                       4096, True),
 }
 CONFIG_IDS = {"toy": 1, "smollm2-135m": 2, "llama-3.2-1b": 3, "llama-7b": 4, "llama2-70b-mixed": 5,
               "llama2-70b-prefill": 6, "llama2-70b-decode64": 7, "smollm2-135m-prompts": 8,
-              "llama-3.2-1b-prompts": 9}
+              "llama-3.2-1b-prompts": 9, "llama-3.2-1b-sharedprompt": 10}
 
 # Layers materialised (each with its own pool) in one timed step.  The toy
 # step is one layer.  One 70B pool of 65,536 blocks is 4.3 GB, so that step
 # is timed on one layer and per-step token rates are scaled by its 80 layers.
 TIMED_LAYERS = {"toy": 1, "smollm2-135m": 30, "llama-3.2-1b": 16, "llama-7b": 32, "llama2-70b-mixed": 1,
                 "llama2-70b-prefill": 1, "llama2-70b-decode64": 1, "smollm2-135m-prompts": 30,
-                "llama-3.2-1b-prompts": 16}
+                "llama-3.2-1b-prompts": 16, "llama-3.2-1b-sharedprompt": 16}
 
 
 @dataclass
@@ -174,6 +177,12 @@ def draw_plan(name: str, *, num_seqs: int | None = None) -> Plan:
         b = 32 if num_seqs is None else num_seqs
         lens = rng.integers(128, 2049, size=b)
         n_decode = 0
+    elif name == "llama-3.2-1b-sharedprompt":
+        # a 1,024-token common prompt (blocks 1..64) plus each user's own
+        # 16..512 tokens, so every step's token lands in a private block
+        b = 64 if num_seqs is None else num_seqs
+        lens = 1024 + rng.integers(16, 513, size=b)
+        shared = tuple(range(1, 65))
     else:
         raise KeyError(name)
 
