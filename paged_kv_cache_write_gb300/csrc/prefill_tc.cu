@@ -68,6 +68,7 @@ struct TcParams {
   __nv_bfloat16* out;
   int32_t* err;
   int B, n_heads, n_kv, rep, W, num_blocks, max_len, total_q, q_per_tile;
+  int ordered;  // 1: heaviest-first slot order (see the kernel), 0: natural grid
   float scale_log2;
 };
 
@@ -101,18 +102,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int b = blockIdx.z;
-  const int g = blockIdx.y;
+  // Work order.  CTAs are dispatched in blockIdx order (x fastest).  With
+  // a batch of at most blockDim.x sequences (p.ordered), x numbers the
+  // (sequence, KV head, tile pair) triples: sequences by descending work
+  // (visible keys of the chunk, c (2L - c + 1) / 2), each sequence's KV
+  // heads in turn, and within those the pairs from the last (most keys)
+  // down: heavy CTAs start first, the pairs of one (sequence, KV head) run
+  // together and share its history in L2, and no CTA is spent on pairs past
+  // a short chunk.  Otherwise z is the sequence, y the KV head and x the
+  // pair, in the natural order.  The work values are staged in the (still
+  // unused) V stages.
+  __shared__ int order_s, pair_s, head_s;
+  int g = blockIdx.y;
+  int b = blockIdx.z, pair = blockIdx.x;
+  if (p.ordered) {
+    const int t = threadIdx.x;
+    int64_t* work_s = reinterpret_cast<int64_t*>(smem + Layout<HD>::V_OFF);
+    int* seq_s = reinterpret_cast<int*>(work_s + p.B);   // [B] sequence of each rank
+    int* pairs_s = seq_s + p.B;                         // [B] pairs of each rank
+    const int qpp = 2 * p.q_per_tile;                   // queries per pair
+    int64_t wt = 0;
+    int pt = 0;
+    if (t < p.B) {
+      const int64_t cs = __ldg(p.cu_q + t + 1) - __ldg(p.cu_q + t);
+      const int64_t Ls = min(__ldg(p.seq_lens + t), p.max_len);
+      wt = cs * (2 * Ls - cs + 1);
+      pt = cs > 0 ? static_cast<int>((cs + qpp - 1) / qpp) : 0;
+      work_s[t] = wt;
+    }
+    if (t == 0) order_s = -1;
+    __syncthreads();
+    int rank = 0;
+    if (t < p.B) {
+      for (int s = 0; s < p.B; ++s) {
+        const int64_t ws = work_s[s];
+        rank += (ws > wt) || (ws == wt && s < t);
+      }
+      seq_s[rank] = t;
+      pairs_s[rank] = pt;
+    }
+    __syncthreads();
+    if (t < p.B) {  // rank t's first slot: the (head, pair) slots of the heavier ranks
+      int first = 0;
+      for (int r = 0; r < t; ++r) first += pairs_s[r];
+      const int64_t x = blockIdx.x;
+      const int64_t lo = int64_t(first) * p.n_kv, n = int64_t(pairs_s[t]) * p.n_kv;
+      if (x >= lo && x < lo + n) {
+        const int off = static_cast<int>(x - lo);
+        order_s = seq_s[t];
+        head_s = off / pairs_s[t];
+        pair_s = pairs_s[t] - 1 - (off - (off / pairs_s[t]) * pairs_s[t]);  // last pair first
+      }
+      fence_proxy_async_smem();  // before the V stages are filled by TMA
+    }
+    __syncthreads();
+    if (order_s < 0) return;  // slot past the last pair
+    b = order_s;
+    g = head_s;
+    pair = pair_s;
+  }
   const int q0 = __ldg(p.cu_q + b);
   const int c = __ldg(p.cu_q + b + 1) - q0;
-  const int i0 = blockIdx.x * 2 * p.q_per_tile;  // first query of tile A
+  const int i0 = pair * 2 * p.q_per_tile;  // first query of tile A
   if (i0 >= c) return;  // idle CTA: leave before any barrier or TMEM use
   if (q0 < 0 || q0 + c > p.total_q) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.err, PKV_DEVERR_LENGTH);
+    if (threadIdx.x == 0 && i0 == 0 && g == 0) report(p.err, PKV_DEVERR_LENGTH);
     return;
   }
   int L = __ldg(p.seq_lens + b);
-  if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) {
+  if (threadIdx.x == 0 && i0 == 0 && g == 0) {
     if (L < c || L < 0) report(p.err, PKV_DEVERR_LENGTH);
     else if (L > p.max_len)
       report(p.err, L > p.W * kBlk ? PKV_DEVERR_TABLE_WIDTH : PKV_DEVERR_LENGTH);
@@ -486,8 +544,13 @@ cudaError_t run_tc(const AttnArgs& a, cudaStream_t stream) {
   static KernelSetup setup;
   const cudaError_t e = kernel_setup(setup, kern, Lay::REQUEST, kThreads, nullptr);
   if (e != cudaSuccess) return e;
-  const int pairs = (a.max_q_len + 2 * p.q_per_tile - 1) / (2 * p.q_per_tile);
-  dim3 grid(pairs, pool.n_kv, a.num_seqs);
+  const int qpp = 2 * p.q_per_tile;
+  p.ordered = a.num_seqs <= kThreads;
+  // ordered: one slot per (sequence, KV head, pair); the pairs number at
+  // most total_q / qpp + one partial pair per sequence
+  const int64_t n_slots = (int64_t(a.total_q) + qpp - 1) / qpp + a.num_seqs;
+  dim3 grid = p.ordered ? dim3(static_cast<unsigned>(n_slots * pool.n_kv), 1, 1)
+                        : dim3((a.max_q_len + qpp - 1) / qpp, pool.n_kv, a.num_seqs);
   kern<<<grid, kThreads, Lay::REQUEST, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
