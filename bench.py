@@ -379,48 +379,61 @@ def run_gb300(args, rank, world, local):
             pkv.paged_attention_decode(q, k_pool, v_pool, bt_, sl_, sh.scale, max_dec, out=out,
                                        workspace=ws, err=err)
 
-    def step(timed=False, inputs=None):
+    def step_head(inputs=None):
         src_bt, src_sl, src_cu = (bt, seq_lens, cu_new) if inputs is None else inputs[:3]
         if has_pre or not fused:
             pkv.slot_mapping(src_bt, src_sl, src_cu, T, sh.block_size, sh.num_blocks, out=slots,
                              err=err)
-        for li, lay in enumerate(L):
-            q, k, v = (lay["q"], lay["k"], lay["v"]) if inputs is None else inputs[3][li]
-            if not fused:
-                pkv.kv_write(k, v, slots, lay["k_pool"], lay["v_pool"], err=err)
-            elif has_pre:  # the prefill chunks' tokens follow the decode rows' tokens
-                pkv.kv_write(k[nd:], v[nd:], slots[nd:], lay["k_pool"], lay["v_pool"], err=err)
+
+    def layer_decode(li, inputs=None, timed=False):
+        lay = L[li]
+        src_bt, src_sl = (bt, seq_lens) if inputs is None else inputs[:2]
+        q, k, v = (lay["q"], lay["k"], lay["v"]) if inputs is None else inputs[3][li]
+        if not fused:  # the decode rows' tokens come first in the step's token order
+            pkv.kv_write(k[:nd], v[:nd], slots[:nd], lay["k_pool"], lay["v_pool"], err=err)
+        if timed:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        if fused:
+            pkv.paged_attention_decode_append(
+                q[:nd], k[:nd], v[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
+                sh.scale, max_dec, out=dec_out[li], workspace=ws, err=err)
+        else:
+            decode_call(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
+                        dec_out[li])
+        if timed:
+            e1.record(stream)
+            ev_dec.append((e0, e1))
+
+    def layer_prefill(li, inputs=None, timed=False):
+        lay = L[li]
+        src_bt, src_sl = (bt, seq_lens) if inputs is None else inputs[:2]
+        q, k, v = (lay["q"], lay["k"], lay["v"]) if inputs is None else inputs[3][li]
+        pkv.kv_write(k[nd:], v[nd:], slots[nd:], lay["k_pool"], lay["v_pool"], err=err)
+        if timed:
+            e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e2.record(stream)
+        pkv.paged_attention_prefill(q[nd:], cu_q, lay["k_pool"], lay["v_pool"], src_bt[nd:],
+                                    src_sl[nd:], sh.scale, max_q, max_pre, out=pre_out[li],
+                                    err=err)
+        if timed:
+            e3.record(stream)
+            ev_pre.append((e2, e3))
+
+    def step(timed=False, inputs=None):
+        step_head(inputs)
+        for li in range(len(L)):
             if nd:
-                if timed:
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                if fused:
-                    pkv.paged_attention_decode_append(
-                        q[:nd], k[:nd], v[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd],
-                        src_sl[:nd], sh.scale, max_dec, out=dec_out[li], workspace=ws, err=err)
-                else:
-                    decode_call(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
-                                dec_out[li])
-                if timed:
-                    e1.record(stream)
-                    ev_dec.append((e0, e1))
+                layer_decode(li, inputs, timed)
             if has_pre:
-                if timed:
-                    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e2.record(stream)
-                pkv.paged_attention_prefill(q[nd:], cu_q, lay["k_pool"], lay["v_pool"], src_bt[nd:],
-                                            src_sl[nd:], sh.scale, max_q, max_pre, out=pre_out[li],
-                                            err=err)
-                if timed:
-                    e3.record(stream)
-                    ev_pre.append((e2, e3))
+                layer_prefill(li, inputs, timed)
 
     # (prefix runs + their combine) + (plan above 2,048 sequences) + main + merge
     dec_launches = ((2 if nd <= 2048 else 3) + (2 if P else 0)) if nd else 0
     if fused:
         launches_per_step = (1 if has_pre else 0) + n_layers * (dec_launches + (2 if has_pre else 0))
     else:
-        launches_per_step = 1 + n_layers * (1 + dec_launches + (1 if has_pre else 0))
+        launches_per_step = 1 + n_layers * ((1 if nd else 0) + dec_launches + (2 if has_pre else 0))
 
     def decode_all():
         for li, lay in enumerate(L):
@@ -540,17 +553,45 @@ def run_gb300(args, rank, world, local):
         h2d = sum(t.numel() * t.element_size() for t in host_in) + sum(
             t.numel() * t.element_size() for lay in host_layers for t in lay)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
-        dev_outs = dec_out + (pre_out if has_pre else [])
+        h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
         def e2e_step():
+            # Pipelined: the tables go first; one stream then brings in each
+            # layer's decode rows, then its prefill rows, while the compute
+            # stream starts each part as soon as it has landed (decode and
+            # prefill rows are different sequences); a second stream copies
+            # each part's output back as soon as it is computed.
+            main = torch.cuda.current_stream(dev)
             for d, h in zip(dev_in, host_in):
                 d.copy_(h, non_blocking=True)
-            for dl, hl in zip(dev_layers, host_layers):
-                for d, h in zip(dl, hl):
-                    d.copy_(h, non_blocking=True)
-            step(inputs=(dev_in[0], dev_in[1], dev_in[2], dev_layers))
-            for h, d in zip(host_out, dev_outs):
-                h.copy_(d, non_blocking=True)
+            h2d_s.wait_stream(main)  # the previous step is done with the input buffers
+            d2h_s.wait_stream(main)
+            ev_d, ev_p = [], []
+            with torch.cuda.stream(h2d_s):
+                for dl, hl in zip(dev_layers, host_layers):
+                    for part, evs in ((slice(0, nd), ev_d), (slice(nd, None), ev_p)):
+                        for d, h in zip(dl, hl):
+                            d[part].copy_(h[part], non_blocking=True)
+                        e = torch.cuda.Event()
+                        e.record(h2d_s)
+                        evs.append(e)
+            inputs = (dev_in[0], dev_in[1], dev_in[2], dev_layers)
+            step_head(inputs)
+            for li in range(len(L)):
+                for run, outs, evs, off, on in ((layer_decode, dec_out, ev_d, 0, nd > 0),
+                                                (layer_prefill, pre_out, ev_p, len(dec_out),
+                                                 has_pre)):
+                    if not on:
+                        continue
+                    main.wait_event(evs[li])
+                    run(li, inputs)
+                    e = torch.cuda.Event()
+                    e.record(main)
+                    d2h_s.wait_event(e)
+                    with torch.cuda.stream(d2h_s):
+                        host_out[off + li].copy_(outs[li], non_blocking=True)
+            main.wait_stream(h2d_s)
+            main.wait_stream(d2h_s)
 
         for _ in range(3):
             e2e_step()
@@ -566,7 +607,9 @@ def run_gb300(args, rank, world, local):
         torch.cuda.synchronize()
         e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev) / e_steps
         e2e = {"value": world * step_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "copies": "each layer's decode, then prefill, inputs copied in on one stream and "
+                         "outputs copied back on another, overlapping the compute"}
 
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} in the timed region")
