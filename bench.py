@@ -278,6 +278,38 @@ def oracle_sample(plan, layer, n_decode: int, n_prefill_queries: int, offset: in
     return secs, nbytes, len(rows), len(pre)
 
 
+def pages_method_sample(plan, layer, rows, outputs=None):
+    """Time the pages' own method on the CPU for decode rows ``rows``: per
+    sequence, gather its blocks through the table into contiguous K and V,
+    repeat each KV head onto its query heads, and attend with einsum and
+    softmax in fp32 PyTorch ("Build a Mini vLLM" section 3, gather_kv and
+    paged_attention; written fresh here, sharing nothing with the kernels
+    or the oracle).  Returns (seconds, algorithmic bytes); each row's output
+    is appended to ``outputs`` when a list is given."""
+    import torch
+    sh = plan.shape
+    rep = sh.n_heads // sh.n_kv
+    kp = layer["k_pool"].float()
+    vp = layer["v_pool"].float()
+    q = layer["q"].float()
+    row = sh.n_kv * sh.head_dim * sh.itemsize
+    t0 = time.perf_counter()
+    for b in rows:
+        L = int(plan.seq_lens[b])
+        nb = -(-L // sh.block_size)
+        ids = torch.from_numpy(plan.block_tables[b, :nb].astype(np.int64))
+        K = kp.index_select(0, ids).reshape(-1, sh.n_kv, sh.head_dim)[:L]
+        V = vp.index_select(0, ids).reshape(-1, sh.n_kv, sh.head_dim)[:L]
+        K = K.repeat_interleave(rep, dim=1)
+        V = V.repeat_interleave(rep, dim=1)
+        s = torch.einsum("hd,lhd->hl", q[b], K) * sh.scale
+        o = torch.einsum("hl,lhd->hd", torch.softmax(s, dim=-1), V)
+        if outputs is not None:
+            outputs.append(o)
+    secs = time.perf_counter() - t0
+    return secs, sum(int(plan.seq_lens[b]) * row * 2 for b in rows)
+
+
 # --------------------------------------------------------------- arms
 
 
@@ -660,6 +692,18 @@ def run_gb300(args, rank, world, local):
                "sample": f"{passes} passes over layer 0: {nr} decode sequences + {npq} prefill "
                          f"queries in all ({nbytes / 1e6:.0f} MB of KV), float64 numpy oracle, "
                          f"{secs:.1f} s on one core"}
+    pages_cpu = None
+    if not args.no_cpu_baseline and layers_cpu and nd:
+        import torch as _t
+        psecs = pbytes = ppasses = 0
+        while psecs < 5.0 and ppasses < 20:
+            s_, b_ = pages_method_sample(plan, layers_cpu[0], range(nd))
+            psecs, pbytes, ppasses = psecs + s_, pbytes + b_, ppasses + 1
+        pages_cpu = {"value": pbytes / psecs / 1e9, "unit": "GB/s", "cores": _t.get_num_threads(),
+                     "kind": "the pages' method: per-sequence gather + einsum attention, "
+                             "fp32 PyTorch on the CPU",
+                     "sample": f"{ppasses} passes over layer 0's {nd} decode sequences, "
+                               f"{psecs:.1f} s"}
     dec_tok_s = world * nd / (ms_step * 1e-3 * (sh.layers / n_layers)) if nd else None
     n_pre_tok = int(plan.new_lens[nd:].sum())
     pre_tok_s = (world * n_pre_tok / (ms_step * 1e-3 * (sh.layers / n_layers))
@@ -683,7 +727,7 @@ def run_gb300(args, rank, world, local):
         "percent_of_hbm_peak_step": 100.0 * value / world / hbm,
         "prefill_tokens_per_s": pre_tok_s,
         "roofline": dominant, "decode_roofline": roof, "prefill_roofline": pre_roof,
-        "cpu_baseline": cpu, "e2e": e2e,
+        "cpu_baseline": cpu, "cpu_pages_method": pages_cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "bytes_per_step": step_bytes,
