@@ -1462,6 +1462,11 @@ struct DecodeLaunch {
     if (per_sm < 1) per_sm = 1;
     *G = sm_count() * per_sm;
     if (a.max_ctas > 0 && a.max_ctas < *G) *G = a.max_ctas;
+    // no more CTAs than the batch can have units (a small batch would
+    // otherwise leave most ranges empty and its split groups spread thin)
+    const int64_t max_units = int64_t(a.num_seqs) * (a.pool.n_kv / hg) *
+                              ((min(a.max_seq_len, a.max_blocks_per_seq * kBS) + kBS - 1) / kBS);
+    if (max_units < *G) *G = static_cast<int>(std::max<int64_t>(1, max_units));
     return cudaSuccess;
   }
   static cudaError_t run(const AttnArgs& a, int hg, cudaStream_t stream) {
