@@ -382,6 +382,24 @@ pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t num_seqs, i
                                               float scale, int32_t max_ctas, void* out,
                                               int32_t* err_word, void* stream);
 
+/*
+ * pkv_selftest_bounded_wait - check the kernels' failure path on this GPU.
+ *
+ * The pages have no counterpart of this entry point.  Every wait in the
+ * kernels (on an mbarrier phase: a shared-memory stage filled, a stage
+ * released) is bounded; when the bound runs out the kernel ORs
+ * PKV_DEVERR_TIMEOUT into the error word, lets its own copies land and
+ * returns, so the context stays usable.  This launches one thread that
+ * waits, with that same wait, on a phase nothing completes, for at most
+ * `polls` polls (each try_wait may park the thread briefly), then reports
+ * the timeout.  Nothing faults or hangs.
+ *
+ *   polls     >= 1 (else PKV_ERR_RANGE); a few thousand end in well under a
+ *             second
+ *   err_word  device int32, required (PKV_ERR_NULL)
+ */
+pkv_status pkv_selftest_bounded_wait(int32_t polls, int32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

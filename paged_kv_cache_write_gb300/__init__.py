@@ -65,6 +65,8 @@ def _load():
     L.pkv_slot_mapping.argtypes = [_p, _i32, _p, _p, _i32, _i32, _i32, _i32, _p, _p, _p]
     L.pkv_kv_write.restype = _i32
     L.pkv_kv_write.argtypes = [_p, _p, _p, _i32, _p, _p, _desc, _p, _p]
+    L.pkv_selftest_bounded_wait.restype = _i32
+    L.pkv_selftest_bounded_wait.argtypes = [_i32, _p, _p]
     L.pkv_copy_blocks.restype = _i32
     L.pkv_copy_blocks.argtypes = [_p, _p, _desc, _p, _i32, _p, _p]
     L.pkv_kv_gather.restype = _i32
@@ -186,6 +188,13 @@ def kv_write(k, v, slot_mapping, k_pool, v_pool, *, err=None, stream=None):
         _dev(slot_mapping, "slot_mapping", torch.int64), T, _dev(k_pool, "k_pool"),
         _dev(v_pool, "v_pool"), ctypes.byref(desc), _opt(err, "err", torch.int32),
         _stream(stream)))
+
+
+def selftest_bounded_wait(err, polls: int = 4096, *, stream=None):
+    """Run one wait that nothing completes, bounded by ``polls``; the
+    kernel ORs the timeout bit into the device int32 ``err`` and returns."""
+    _check("pkv_selftest_bounded_wait", _load().pkv_selftest_bounded_wait(
+        int(polls), _dev(err, "err", torch.int32), _stream(stream)))
 
 
 def copy_blocks(k_pool, v_pool, block_pairs, *, err=None, stream=None):

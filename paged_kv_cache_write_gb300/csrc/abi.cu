@@ -290,4 +290,11 @@ pkv_status pkv_paged_attention_prefill(const void* q, const int32_t* cu_q_lens, 
   return from_cuda(pkv::launch_prefill(a, as_stream(stream)));
 }
 
+pkv_status pkv_selftest_bounded_wait(int32_t polls, int32_t* err_word, void* stream) {
+  if (polls < 1) return PKV_ERR_RANGE;
+  if (!err_word) return PKV_ERR_NULL;
+  return from_cuda(
+      pkv::launch_bounded_wait_selftest(static_cast<uint32_t>(polls), err_word, as_stream(stream)));
+}
+
 }  // extern "C"

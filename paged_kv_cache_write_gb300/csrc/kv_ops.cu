@@ -197,6 +197,22 @@ cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_ma
   return cudaGetLastError();
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier phase
+// that nothing completes, with the same wait the kernels use but at most
+// `polls` polls, then reports PKV_DEVERR_TIMEOUT and returns.
+__global__ void bounded_wait_selftest_kernel(uint32_t polls, int32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (!mbar_wait(&bar, 0, polls)) report(err, PKV_DEVERR_TIMEOUT);
+}
+
+cudaError_t launch_bounded_wait_selftest(uint32_t polls, int32_t* err, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(polls, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const PoolShape& pool,
                                const int32_t* pairs, int32_t num_pairs, int32_t* err,
                                cudaStream_t stream) {

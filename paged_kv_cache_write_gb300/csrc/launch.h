@@ -24,6 +24,8 @@ cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_ma
                             int32_t num_tokens, void* k_pool, void* v_pool, const PoolShape& pool,
                             int32_t* err, cudaStream_t stream);
 
+cudaError_t launch_bounded_wait_selftest(uint32_t polls, int32_t* err, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const PoolShape& pool,
                                const int32_t* pairs, int32_t num_pairs, int32_t* err,
                                cudaStream_t stream);

@@ -84,6 +84,12 @@ def test_copy_blocks_host_checks(pkv):
     assert lib.pkv_copy_blocks(None, None, by(d), None, 0, None, None) == 0
 
 
+def test_selftest_bounded_wait_host_checks(pkv):
+    lib = pkv.lib
+    assert lib.pkv_selftest_bounded_wait(0, FAKE, None) == 5
+    assert lib.pkv_selftest_bounded_wait(100, None, None) == 1
+
+
 def test_slot_mapping_host_checks(pkv):
     lib = pkv.lib
     assert lib.pkv_slot_mapping(FAKE, 4, FAKE, FAKE, -1, 3, 16, 8, FAKE, None, None) == 2
