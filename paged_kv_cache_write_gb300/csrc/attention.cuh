@@ -1,5 +1,5 @@
-// Paged attention over the block pool: decode (one query per sequence,
-// split over the whole machine and merged by log-sum-exp weights) and
+// Paged attention over the block pool, included by the decode and prefill
+// translation units: decode (one query per sequence, split over the whole machine and merged by log-sum-exp weights) and
 // chunked prefill (a causal query chunk over paged history).
 //
 // What is computed ("Build a Mini vLLM" section 3, paged_attention, and
@@ -35,6 +35,8 @@
 //    results are bit-identical under any placement or sharing of blocks.
 //  * Every mbarrier wait is bounded; a wait that runs out sets
 //    PKV_DEVERR_TIMEOUT, and the producer drains its copies before exit.
+#pragma once
+
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -47,8 +49,7 @@
 #include "launch.h"
 
 namespace pkv {
-
-namespace {
+namespace attn {
 
 constexpr int kBS = 16;          // tokens per block handled by these kernels
 constexpr int kMaxRep = 16;      // query heads per KV head (MMA rows)
@@ -1233,7 +1234,7 @@ __global__ void __launch_bounds__(288) prefill_kernel(PrefillParams p) {
 
 // ------------------------------------------------------------ host side
 
-int sm_count() {
+inline int sm_count() {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0;
@@ -1244,11 +1245,11 @@ int sm_count() {
   return sms;
 }
 
-bool use_mma(const PoolShape& pool) { return pool.dtype == PKV_BF16 && (pool.head_dim == 64 || pool.head_dim == 128); }
+inline bool use_mma(const PoolShape& pool) { return pool.dtype == PKV_BF16 && (pool.head_dim == 64 || pool.head_dim == 128); }
 
 // Heads per CTA for decode: the largest divisor of n_kv, at most 8, whose
 // rows (heads x head_dim elements) fit in 1 KB.
-int decode_group(const PoolShape& pool) {
+inline int decode_group(const PoolShape& pool) {
   const int per_head = pool.head_dim * pool.elem_bytes();
   int best = 1;
   for (int h = 1; h <= 8 && h <= pool.n_kv; ++h)
@@ -1256,7 +1257,7 @@ int decode_group(const PoolShape& pool) {
   return best;
 }
 
-int stages_for(int stage_bytes, int scratch_bytes, int target_bytes) {
+inline int stages_for(int stage_bytes, int scratch_bytes, int target_bytes) {
   int ns = (target_bytes - kBarrierBytes - scratch_bytes) / stage_bytes;
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < 2) ns = 2;
@@ -1391,7 +1392,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
 }
 
 // Shared memory of the merge kernel.
-size_t merge_smem_bytes(int rows, int hd) {
+inline size_t merge_smem_bytes(int rows, int hd) {
   const int P = merge_parts_per_round(rows, hd);
   return size_t(merge_head_bytes(rows, P)) + size_t(P) * rows * hd * 4;
 }
@@ -1401,13 +1402,13 @@ size_t merge_smem_bytes(int rows, int hd) {
 // kMaxPrefixRuns runs and at most 1,024 run-rows per query head (which
 // bounds the partials' workspace), at least one block per run.  *bpc =
 // blocks per run.  One more slot holds the combined partials.
-int max_prefix_runs(int num_seqs, int prefix_blocks) {
+inline int max_prefix_runs(int num_seqs, int prefix_blocks) {
   const int k = 1024 / (num_seqs > 0 ? num_seqs : 1);
   return std::max(1, std::min({kMaxPrefixRuns, prefix_blocks, std::max(1, k)}));
 }
-int prefix_slots(int runs) { return runs > 0 ? runs + 1 : 0; }
+inline int prefix_slots(int runs) { return runs > 0 ? runs + 1 : 0; }
 
-int prefix_runs(int num_seqs, int n_groups, int seqs_per_cta, int prefix_blocks, int* bpc) {
+inline int prefix_runs(int num_seqs, int n_groups, int seqs_per_cta, int prefix_blocks, int* bpc) {
   const int base = n_groups * ((num_seqs + seqs_per_cta - 1) / seqs_per_cta);
   int k = (2 * sm_count() + base - 1) / base;
   k = std::max(1, std::min(k, max_prefix_runs(num_seqs, prefix_blocks)));
@@ -1652,102 +1653,21 @@ cudaError_t by_rep_simt(int rep, const AttnArgs& a, cudaStream_t s, int hg) {
   }
 }
 
-bool simt_head_dim(int hd) { return hd == 16 || hd == 32 || hd == 64 || hd == 128; }
+inline bool simt_head_dim(int hd) { return hd == 16 || hd == 32 || hd == 64 || hd == 128; }
 
-}  // namespace
 
-bool decode_supported(const PoolShape& pool, int32_t n_heads) {
-  if (pool.block_size != kBS || pool.n_kv <= 0 || n_heads % pool.n_kv != 0) return false;
-  if (n_heads / pool.n_kv > kMaxRep) return false;
-  if (pool.dtype == PKV_BF16) return use_mma(pool) || simt_head_dim(pool.head_dim);
-  return pool.dtype == PKV_F32 && simt_head_dim(pool.head_dim);
-}
+// Decode paths compiled in their own translation units so the kernels build
+// in parallel: decode_mma64.cu (tensor cores, bf16 head_dim 64),
+// decode_simt.cu (CUDA cores, fp32 head_dim 64 / 128) and
+// decode_simt_narrow.cu (CUDA cores, head_dim 16 / 32 of either type);
+// decode.cu holds the head_dim-128 tensor-core path and the dispatch.  Each
+// launches, or sizes the workspace of, one decode for its pool type.
+cudaError_t launch_decode_mma64(const AttnArgs& a, int hg, cudaStream_t s);
+size_t exact_workspace_mma64(const AttnArgs& a, int hg);
+cudaError_t launch_decode_simt_wide(const AttnArgs& a, int hg, cudaStream_t s);
+size_t exact_workspace_simt_wide(const AttnArgs& a, int hg);
+cudaError_t launch_decode_simt_narrow(const AttnArgs& a, int hg, cudaStream_t s);
+size_t exact_workspace_simt_narrow(const AttnArgs& a, int hg);
 
-bool prefill_supported(const PoolShape& pool, int32_t n_heads) { return decode_supported(pool, n_heads); }
-
-int32_t decode_default_partition(int32_t, int32_t, int32_t, int32_t) { return 0; }
-
-// Upper bound of the decode workspace over every grid this device can run.
-size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim, int32_t, int32_t,
-                              int32_t shared_prefix_blocks) {
-  // rows per head group <= n_heads; at most 16 resident CTAs per SM
-  return DecodeWs(num_seqs, size_t(sm_count()) * 16, size_t(n_heads), head_dim,
-                  shared_prefix_blocks > 0
-                      ? prefix_slots(max_prefix_runs(num_seqs, shared_prefix_blocks)) * n_heads
-                      : 0)
-      .total;
-}
-
-cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s) {
-  const PoolShape& pool = a.pool;
-  const int rep = a.n_heads / pool.n_kv;
-  const int hg = decode_group(pool);
-  if (use_mma(pool)) {
-    if (pool.head_dim == 64) return DecodeLaunch<__nv_bfloat16, 64, 16, true>::run(a, hg, s);
-    return DecodeLaunch<__nv_bfloat16, 128, 16, true>::run(a, hg, s);
-  }
-  if (pool.dtype == PKV_F32) {
-    switch (pool.head_dim) {
-      case 16: return by_rep_simt<DecodeLaunch, float, 16>(rep, a, s, hg);
-      case 32: return by_rep_simt<DecodeLaunch, float, 32>(rep, a, s, hg);
-      case 64: return by_rep_simt<DecodeLaunch, float, 64>(rep, a, s, hg);
-      default: return by_rep_simt<DecodeLaunch, float, 128>(rep, a, s, hg);
-    }
-  }
-  switch (pool.head_dim) {
-    case 16: return by_rep_simt<DecodeLaunch, __nv_bfloat16, 16>(rep, a, s, hg);
-    default: return by_rep_simt<DecodeLaunch, __nv_bfloat16, 32>(rep, a, s, hg);
-  }
-}
-
-size_t decode_workspace_bytes_exact(const AttnArgs& a) {
-  const PoolShape& pool = a.pool;
-  const int rep = a.n_heads / pool.n_kv;
-  const int hg = decode_group(pool);
-  if (use_mma(pool)) {
-    if (pool.head_dim == 64) return decode_exact_workspace<__nv_bfloat16, 64, 16, true>(a, hg);
-    return decode_exact_workspace<__nv_bfloat16, 128, 16, true>(a, hg);
-  }
-  const bool small = rep <= 4;
-  if (pool.dtype == PKV_F32) {
-    switch (pool.head_dim) {
-      case 16: return small ? decode_exact_workspace<float, 16, 4, false>(a, hg)
-                            : decode_exact_workspace<float, 16, 16, false>(a, hg);
-      case 32: return small ? decode_exact_workspace<float, 32, 4, false>(a, hg)
-                            : decode_exact_workspace<float, 32, 16, false>(a, hg);
-      case 64: return small ? decode_exact_workspace<float, 64, 4, false>(a, hg)
-                            : decode_exact_workspace<float, 64, 16, false>(a, hg);
-      default: return small ? decode_exact_workspace<float, 128, 4, false>(a, hg)
-                            : decode_exact_workspace<float, 128, 16, false>(a, hg);
-    }
-  }
-  if (pool.head_dim == 16)
-    return small ? decode_exact_workspace<__nv_bfloat16, 16, 4, false>(a, hg)
-                 : decode_exact_workspace<__nv_bfloat16, 16, 16, false>(a, hg);
-  return small ? decode_exact_workspace<__nv_bfloat16, 32, 4, false>(a, hg)
-               : decode_exact_workspace<__nv_bfloat16, 32, 16, false>(a, hg);
-}
-
-cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t s) {
-  const PoolShape& pool = a.pool;
-  const int rep = a.n_heads / pool.n_kv;
-  if (prefill_tc_supported(pool, a.n_heads)) return launch_prefill_tc(a, s);
-  if (use_mma(pool)) {
-    if (pool.head_dim == 64) return PrefillLaunch<__nv_bfloat16, 64, 16, true>::run(a, s);
-    return PrefillLaunch<__nv_bfloat16, 128, 16, true>::run(a, s);
-  }
-  if (pool.dtype == PKV_F32) {
-    switch (pool.head_dim) {
-      case 16: return by_rep_simt<PrefillLaunch, float, 16>(rep, a, s, 0);
-      case 32: return by_rep_simt<PrefillLaunch, float, 32>(rep, a, s, 0);
-      case 64: return by_rep_simt<PrefillLaunch, float, 64>(rep, a, s, 0);
-      default: return by_rep_simt<PrefillLaunch, float, 128>(rep, a, s, 0);
-    }
-  }
-  switch (pool.head_dim) {
-    case 16: return by_rep_simt<PrefillLaunch, __nv_bfloat16, 16>(rep, a, s, 0);
-    default: return by_rep_simt<PrefillLaunch, __nv_bfloat16, 32>(rep, a, s, 0);
-  }
-}
-
+}  // namespace attn
 }  // namespace pkv
