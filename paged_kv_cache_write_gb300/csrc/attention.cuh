@@ -47,6 +47,8 @@
 #include "device.cuh"
 #include "host_cache.h"
 #include "launch.h"
+#include "tcgen05.cuh"
+#include "tma_host.h"
 
 namespace pkv {
 namespace attn {
@@ -127,17 +129,47 @@ struct MmaRows {
   __device__ __forceinline__ void block(const uint8_t* k_tile, const uint8_t* v_tile, int stride,
                                         int j0, float scale_log2) {
     const int lane = threadIdx.x & 31;
-    const int c = lane & 3;
     const int mi = lane >> 3, ri = lane & 7;
+    const uint8_t* kaddr = k_tile + ((mi >> 1) * 8 + ri) * stride + (mi & 1) * 16;
+    const uint8_t* vaddr = v_tile + ((mi & 1) * 8 + ri) * stride + (mi >> 1) * 16;
+    block_from([&](int kk) { return kaddr + kk * 32; }, [&](int dp) { return vaddr + dp * 32; },
+               j0, scale_log2);
+  }
+
+  // One 16-token block from TMA tiles in the 128-byte-swizzled layout: rows
+  // of 64 head dims (128 bytes), row (h * HD/64 + d / 64) * 16 + t holding
+  // token t, dims [d, d + 64) of the group's head h; within a row the
+  // 16-byte piece c sits at position c ^ (row % 8).  `head` is this warp's
+  // head within the group.
+  __device__ __forceinline__ void block_sw(const uint8_t* k_tile, const uint8_t* v_tile, int head,
+                                           int j0, float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int hrow = head * (HD / 64) * kBS;
+    const uint8_t* kaddr = k_tile + (hrow + (mi >> 1) * 8 + ri) * 128;
+    const uint8_t* vaddr = v_tile + (hrow + (mi & 1) * 8 + ri) * 128;
+    const int kx = (mi & 1) ^ ri, vx = (mi >> 1) ^ ri;
+    block_from([&](int kk) { return kaddr + (kk >> 2) * (kBS * 128) + ((((kk & 3) * 2) ^ kx) << 4); },
+               [&](int dp) { return vaddr + (dp >> 2) * (kBS * 128) + ((((dp & 3) * 2) ^ vx) << 4); },
+               j0, scale_log2);
+  }
+
+  // kaddr(kk): this lane's ldmatrix row address for the K matrices of dims
+  // [16 kk, 16 kk + 16) (lane / 8 = matrix: tokens 0-7 | 8-15 x dims lo |
+  // hi); vaddr(dp): the same for V, matrices tokens 0-7 | 8-15 (fast) x
+  // dims lo | hi.
+  template <typename KAddr, typename VAddr>
+  __device__ __forceinline__ void block_from(KAddr kaddr, VAddr vaddr, int j0, float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int c = lane & 3;
     float s[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
     // S = Q K^T: the four 8x8 matrices are (tokens 0-7 | 8-15) x (dims lo | hi).
-    const uint8_t* kaddr = k_tile + ((mi >> 1) * 8 + ri) * stride + (mi & 1) * 16;
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
       uint32_t kb[4];
-      ldsm_x4(kb, kaddr + kk * 32);
+      ldsm_x4(kb, kaddr(kk));
       mma_bf16_16816(s[0], qa[kk], kb[0], kb[1]);
       mma_bf16_16816(s[1], qa[kk], kb[2], kb[3]);
     }
@@ -186,11 +218,10 @@ struct MmaRows {
       o[i][3] *= alpha[1];
     }
     // O += P V: matrices (tokens 0-7 | 8-15) x (dims lo | hi), transposed.
-    const uint8_t* vaddr = v_tile + ((mi & 1) * 8 + ri) * stride + (mi >> 1) * 16;
 #pragma unroll
     for (int dp = 0; dp < HD / 16; ++dp) {
       uint32_t vb[4];
-      ldsm_x4_trans(vb, vaddr + dp * 32);
+      ldsm_x4_trans(vb, vaddr(dp));
       mma_bf16_16816(o[2 * dp], pa, vb[0], vb[1]);
       mma_bf16_16816(o[2 * dp + 1], pa, vb[2], vb[3]);
     }
@@ -431,6 +462,24 @@ __device__ __forceinline__ Ring make_ring(uint8_t* smem, int nstages, int row_by
   return r;
 }
 
+// Ring of TMA tiles: per stage a K tile and a V tile of tile_bytes each,
+// starting on 1024-byte boundaries (the period of the 128-byte swizzle).
+// Needs 1024 bytes of slack after the barriers.
+__device__ __forceinline__ Ring make_tile_ring(uint8_t* smem, int nstages, int tile_bytes) {
+  Ring r;
+  r.full = reinterpret_cast<uint64_t*>(smem);
+  r.empty = r.full + kMaxStages;
+  r.abort_flag = reinterpret_cast<volatile int*>(r.empty + kMaxStages);
+  uint8_t* base = smem + kBarrierBytes;
+  r.stages = base + ((1024u - (smem_addr(base) & 1023u)) & 1023u);
+  r.nstages = nstages;
+  r.row_bytes = 0;
+  r.row_stride = 0;
+  r.tile_bytes = tile_bytes;
+  r.stage_bytes = 2 * tile_bytes;
+  return r;
+}
+
 __device__ __forceinline__ void ring_init(const Ring& r, int consumer_warps) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < r.nstages; ++i) {
@@ -478,6 +527,76 @@ __device__ __forceinline__ bool ring_fill(const Ring& r, uint32_t it, const uint
     bulk_copy_g2s(dst, src, static_cast<uint32_t>(r.row_bytes), r.full + st);
   }
   return true;
+}
+
+// Producer side of a tile ring, one lane: wait for stage `it` to be free,
+// then load the K and V boxes at pool slot `slot` (a block's first token),
+// heads [head0, head0 + group) into it.  A slot past the pool's end reads
+// zeros.  Returns false if the wait timed out.
+__device__ __forceinline__ bool tile_fill(const Ring& r, uint32_t it, const CUtensorMap* tm_k,
+                                          const CUtensorMap* tm_v, int slot, int head0,
+                                          int32_t* err) {
+  const int st = static_cast<int>(it % r.nstages);
+  const uint32_t use = it / r.nstages;
+  if (use > 0 && !mbar_wait(r.empty + st, (use - 1) & 1)) {
+    report(err, PKV_DEVERR_TIMEOUT);
+    return false;
+  }
+  mbar_arrive_expect_tx(r.full + st, static_cast<uint32_t>(r.stage_bytes));
+  tc::tma_load_4d(r.k_tile(st), tm_k, 0, slot, 0, head0, r.full + st);
+  tc::tma_load_4d(r.v_tile(st), tm_v, 0, slot, 0, head0, r.full + st);
+  return true;
+}
+
+// This lane's HD / 16 bytes of the bf16 rows k_new[row_elem ..] and
+// v_new[row_elem ..] (HD elements each).
+template <int HD>
+__device__ __forceinline__ void new_row_piece(const uint8_t* k_new, const uint8_t* v_new,
+                                              int64_t row_elem, uint32_t (&kn)[2],
+                                              uint32_t (&vn)[2]) {
+  const int lane = threadIdx.x & 31;
+  const int64_t off = row_elem * 2 + lane * (HD / 16);
+  if constexpr (HD / 16 == 8) {
+    const uint2 k = __ldg(reinterpret_cast<const uint2*>(k_new + off));
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(v_new + off));
+    kn[0] = k.x, kn[1] = k.y, vn[0] = v.x, vn[1] = v.y;
+  } else {
+    static_assert(HD / 16 == 4, "tile path: head_dim 64 or 128");
+    kn[0] = __ldg(reinterpret_cast<const uint32_t*>(k_new + off));
+    vn[0] = __ldg(reinterpret_cast<const uint32_t*>(v_new + off));
+  }
+}
+
+// One warp, in its head `head` of a K / V tile pair (layout of
+// MmaRows::block_sw) holding a sequence's last block with `valid` tokens:
+// zero the V rows [valid, 16) and, if `fresh`, store the new token's row
+// (row valid - 1) from this lane's pieces.
+template <int HD>
+__device__ __forceinline__ void tile_fix(uint8_t* kt, uint8_t* vt, int head, int valid, bool fresh,
+                                         const uint32_t (&kn)[2], const uint32_t (&vn)[2]) {
+  constexpr int NH = HD / 64;
+  const int lane = threadIdx.x & 31;
+  const int hrow = head * NH * kBS;
+  const int nz = kBS - valid;
+  for (int i = lane; i < NH * nz * 8; i += 32) {
+    const int half = i / (nz * 8), rem = i - half * nz * 8;
+    *reinterpret_cast<uint4*>(vt + (hrow + half * kBS + valid + (rem >> 3)) * 128 + (rem & 7) * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (fresh) {
+    const int t = valid - 1;
+    const int o = lane * (HD / 16);  // byte of the row
+    const int half = o >> 7, ob = o & 127;
+    const int off = (hrow + half * kBS + t) * 128 + (((ob >> 4) ^ (t & 7)) << 4) + (ob & 15);
+    if constexpr (HD / 16 == 8) {
+      *reinterpret_cast<uint2*>(kt + off) = make_uint2(kn[0], kn[1]);
+      *reinterpret_cast<uint2*>(vt + off) = make_uint2(vn[0], vn[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(kt + off) = kn[0];
+      *reinterpret_cast<uint32_t*>(vt + off) = vn[0];
+    }
+  }
+  __syncwarp();
 }
 
 // Producer after an abort: wait (bounded) for every stage it may still
@@ -774,13 +893,18 @@ constexpr int decode_max_threads() {
   return ((1024 / (HD * int(sizeof(T))) < 8 ? 1024 / (HD * int(sizeof(T))) : 8) + 1) * 32;
 }
 
+// The decode body; tm_k / tm_v are the pools' tile maps (tensor-core path)
+// or null (CUDA-core path).
 template <typename T, int HD, int MAXR, bool MMA>
-__global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(DecodeParams p) {
+__device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                            const DecodeParams& p) {
   extern __shared__ __align__(128) uint8_t smem[];
   using Rows = typename RowsOf<T, HD, MAXR, MMA>::type;
   const int consumers = p.hg_size;
   const int row_bytes = p.hg_size * HD * p.elem_bytes;
-  Ring ring = make_ring(smem, p.nstages, row_bytes);
+  // tensor-core path: whole-block TMA tiles; CUDA-core path: a copy per row
+  Ring ring = MMA ? make_tile_ring(smem, p.nstages, kBS * row_bytes)
+                  : make_ring(smem, p.nstages, row_bytes);
   ring_init(ring, consumers);
   pdl_wait();  // inputs written by the preceding kernel (the plan, when there is one)
   pdl_launch_dependents();  // the merge kernel may be scheduled (it waits for this grid)
@@ -864,15 +988,27 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
                              __ldg(p.seq_lens + cur.b) == cur.L;  // not a clamped bad length
           const int new_row = fresh ? cur.L - 1 - j * kBS : -1;
           const int64_t new_off = int64_t(cur.b) * p.n_kv * HD * p.elem_bytes + head_off;
-          if (!ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err,
-                         new_row, p.k_new + new_off, p.v_new + new_off)) {
+          bool filled;
+          if constexpr (MMA) {
+            // one lane loads the block's K and V boxes (a bad id reads the
+            // zeros past the pool's end); the consumers put the new row in
+            filled = lane == 0 ? tile_fill(ring, it, tm_k, tm_v,
+                                           valid > 0 ? blk * kBS : p.num_blocks * kBS,
+                                           cur.grp * p.hg_size, p.err)
+                               : true;
+            filled = __shfl_sync(0xffffffffu, filled, 0);
+          } else {
+            filled = ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err,
+                               new_row, p.k_new + new_off, p.v_new + new_off);
+          }
+          if (!filled) {
             *ring.abort_flag = 1;
             ok = false;
             break;
           }
           ++it;
           if (fresh) {
-            const int nvec = ring.row_bytes / 16;  // 16-byte pieces of this group's row
+            const int nvec = row_bytes / 16;  // 16-byte pieces of this group's row
             const int64_t dst = off + int64_t(new_row) * token_pitch;
             for (int i = lane; i < 2 * nvec; i += 32) {
               const bool is_v = i >= nvec;
@@ -924,6 +1060,18 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
         rows.seed([&](int r) -> const float* { return r < p.rep ? p.pre_o + (prow + r) * HD : nullptr; },
                   [&](int r) -> const float* { return p.pre_ml + (prow + r) * 2; });
       }
+      // tile path, append: this lane's piece of the new token's K / V row
+      // for this warp's head (the pool's copy is written by the producer)
+      const bool has_last = cur.j + n == cur.nblk;
+      bool fresh = false;
+      uint32_t kn[2] = {0u, 0u}, vn[2] = {0u, 0u};
+      if constexpr (MMA) {
+        if (has_last && p.k_new != nullptr && __ldg(p.seq_lens + b) == cur.L) {
+          const int blk = __ldg(p.bt + int64_t(b) * p.W + p.prefix_blocks + cur.nblk - 1);
+          fresh = blk >= 0 && blk < p.num_blocks;
+          if (fresh) new_row_piece<HD>(p.k_new, p.v_new, (int64_t(b) * p.n_kv + kv_head) * HD, kn, vn);
+        }
+      }
       for (int k = 0; k < n; ++k) {
         if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
           *ring.abort_flag = 1;
@@ -931,9 +1079,22 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
           break;
         }
         const int st = static_cast<int>(it % ring.nstages);
-        const int hoff = warp * HD * p.elem_bytes;
-        rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride,
-                   (p.prefix_blocks + cur.j + k) * kBS, p.scale_log2);
+        const int j0 = (p.prefix_blocks + cur.j + k) * kBS;
+        if constexpr (MMA) {
+          uint8_t* kt = ring.k_tile(st);
+          uint8_t* vt = ring.v_tile(st);
+          // the sequence's last block: rows past its end hold whatever the
+          // pool slots hold, so zero them in V (K's are masked), and put in
+          // the new token's row
+          const bool fix = has_last && k == n - 1 && (cur.L - j0 < kBS || fresh);
+          if (fix) tile_fix<HD>(kt, vt, warp, cur.L - j0, fresh, kn, vn);
+          rows.block_sw(kt, vt, warp, j0, p.scale_log2);
+          if (fix) fence_proxy_async_smem();  // before the stage's next TMA writes
+        } else {
+          const int hoff = warp * HD * p.elem_bytes;
+          rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride, j0,
+                     p.scale_log2);
+        }
         ring_release(ring, it);
         ++it;
       }
@@ -955,6 +1116,22 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_kernel(Dec
       cur.advance(p, n);
     }
   }
+}
+
+// Tensor-core path (bf16, head_dim 64 / 128): whole blocks as TMA tiles.
+// The head_dim-64 kernel gets up to 112 registers (two 288-thread CTAs per
+// SM), enough to keep it free of spills.
+template <typename T, int HD>
+__global__ void __launch_bounds__(decode_max_threads<T, HD>()) __maxnreg__(HD == 64 ? 112 : 224)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  DecodeParams p) {
+  decode_body<T, HD, 16, true>(&tm_k, &tm_v, p);
+}
+
+// CUDA-core path: a bulk copy per token row into a padded ring.
+template <typename T, int HD, int MAXR>
+__global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_rows_kernel(DecodeParams p) {
+  decode_body<T, HD, MAXR, false>(nullptr, nullptr, p);
 }
 
 // Shared-prefix attention: the first prefix_blocks table entries are the
@@ -1445,19 +1622,33 @@ struct DecodeLaunch {
   static size_t scratch_bytes(int warps) {
     return MMA ? 0 : size_t(warps) * RowsOf<T, HD, MAXR, MMA>::kScratch * sizeof(float);
   }
-  static size_t smem_bytes(int hg, int elem_bytes, int* nstages) {
+  // Bytes of one ring stage: padded rows (CUDA-core path, and the shared
+  // prefix kernel, which shares the launch shape) or TMA tiles.
+  static int stage_bytes(int hg, int elem_bytes, bool tiles) {
     const int row_bytes = hg * HD * elem_bytes;
-    const int stage_bytes = 2 * kBS * (row_bytes + 16);
+    return tiles ? 2 * kBS * row_bytes : 2 * kBS * (row_bytes + 16);
+  }
+  static size_t smem_bytes(int hg, int elem_bytes, int* nstages) {
+    const int padded = stage_bytes(hg, elem_bytes, false);
     const size_t scratch = scratch_bytes(hg);
-    *nstages = stages_for(stage_bytes, static_cast<int>(scratch), 110 * 1024);
-    return kBarrierBytes + size_t(*nstages) * stage_bytes + scratch;
+    *nstages = stages_for(padded, static_cast<int>(scratch), 110 * 1024);
+    size_t bytes = kBarrierBytes + size_t(*nstages) * padded + scratch;
+    if (MMA)  // tile ring: 1024 bytes of alignment slack after the barriers
+      bytes = std::max(bytes, kBarrierBytes + 1024 + size_t(*nstages) * stage_bytes(hg, elem_bytes, true));
+    return bytes;
+  }
+  static auto main_kernel() {
+    if constexpr (MMA)
+      return decode_kernel<T, HD>;
+    else
+      return decode_rows_kernel<T, HD, MAXR>;
   }
   // Persistent grid: every SM filled with as many CTAs as fit, capped by max_ctas.
   static cudaError_t grid(const AttnArgs& a, int hg, int* G, size_t* smem, int* nstages) {
     *smem = smem_bytes(hg, a.pool.elem_bytes(), nstages);
     static KernelSetup setup;
     int per_sm = 0;
-    const cudaError_t e = kernel_setup(setup, decode_kernel<T, HD, MAXR, MMA>,
+    const cudaError_t e = kernel_setup(setup, main_kernel(),
                                        static_cast<int>(*smem), (hg + 1) * 32, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
@@ -1519,6 +1710,19 @@ struct DecodeLaunch {
     p.ws_o = reinterpret_cast<float*>(ws + L.o);
     p.pre_o = reinterpret_cast<float*>(ws + L.pre_o);
     p.pre_ml = reinterpret_cast<float*>(ws + L.pre_ml);
+    // tensor-core path: the pools as 4-D tensors (64 dims, slot, 64-dim half,
+    // KV head) read in boxes of one block's 16 slots x the group's heads
+    CUtensorMap tm_k{}, tm_v{};
+    if constexpr (MMA) {
+      const uint64_t slots = uint64_t(pool.num_blocks) * kBS;
+      if (slots >= (uint64_t(1) << 31)) return cudaErrorInvalidValue;  // 32-bit box coordinates
+      const uint64_t dims[4] = {64, slots, HD / 64, uint64_t(pool.n_kv)};
+      const uint64_t strides[3] = {uint64_t(pool.n_kv) * HD * 2, 128, uint64_t(HD) * 2};
+      const uint32_t box[4] = {64, kBS, HD / 64, static_cast<uint32_t>(hg)};
+      if (!encode_bf16_sw128(&tm_k, a.k_pool, 4, dims, strides, box) ||
+          !encode_bf16_sw128(&tm_v, a.v_pool, 4, dims, strides, box))
+        return cudaErrorInvalidValue;
+    }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1547,7 +1751,7 @@ struct DecodeLaunch {
       if (e != cudaSuccess) return e;
     }
     // small batches: every CTA scans the lengths in its ring stages
-    const size_t ring_bytes = smem - kBarrierBytes - scratch_bytes(hg);
+    const size_t ring_bytes = size_t(p.nstages) * stage_bytes(hg, p.elem_bytes, MMA);
     p.plan_in_kernel =
         a.num_seqs <= kKernelPlanSeqs && size_t(a.num_seqs + 1 + 32) * 4 <= ring_bytes;
     if (!p.plan_in_kernel) {
@@ -1563,7 +1767,10 @@ struct DecodeLaunch {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_kernel<T, HD, MAXR, MMA>, p);
+    if constexpr (MMA)
+      e = cudaLaunchKernelEx(&cfg, decode_kernel<T, HD>, tm_k, tm_v, p);
+    else
+      e = cudaLaunchKernelEx(&cfg, decode_rows_kernel<T, HD, MAXR>, p);
     if (e != cudaSuccess) return e;
     // split groups: one small CTA per main-kernel boundary, most exit at once
     const size_t msmem = merge_smem_bytes(hg * p.rep, HD);
