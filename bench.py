@@ -83,6 +83,9 @@ def parse_args(argv=None):
     ap.add_argument("--shared-prefix", action="store_true",
                     help="decode with the shared-prefix entry point (the workload's common "
                          "prompt blocks read once per step); the K/V write is then separate")
+    ap.add_argument("--no-plan", action="store_true",
+                    help="let every decode call split its work itself instead of planning the "
+                         "split once per step for all layers")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers materialised per step (0 = the workload's own count)")
     return ap.parse_args(argv)
@@ -402,11 +405,26 @@ def run_gb300(args, rank, world, local):
     ev_dec, ev_pre = [], []
 
     fused = not args.separate_write and P == 0
+    # the decode rows' work split, planned once per step for all its layers
+    # (a one-layer step plans inside its call: a separate plan would not be
+    # shared by anything)
+    planned = P == 0 and not args.no_plan and len(L) > 1
 
-    def decode_call(q, k_pool, v_pool, bt_, sl_, out):
+    def decode_plan(sl_):
+        pkv.decode_plan(L[0]["k_pool"], sl_[:nd], sh.n_heads, bt.shape[1], max_dec, workspace=ws,
+                        err=err)
+
+    def decode_call(q, k_pool, v_pool, bt_, sl_, out, k_new=None, v_new=None):
         if P:
             pkv.paged_attention_decode_shared_prefix(q, k_pool, v_pool, bt_, sl_, sh.scale, P,
                                                      max_dec, out=out, workspace=ws, err=err)
+        elif planned:
+            pkv.paged_attention_decode_planned(q, k_pool, v_pool, bt_, sl_, sh.scale, max_dec,
+                                               workspace=ws, k_new=k_new, v_new=v_new, out=out,
+                                               err=err)
+        elif k_new is not None:
+            pkv.paged_attention_decode_append(q, k_new, v_new, k_pool, v_pool, bt_, sl_, sh.scale,
+                                              max_dec, out=out, workspace=ws, err=err)
         else:
             pkv.paged_attention_decode(q, k_pool, v_pool, bt_, sl_, sh.scale, max_dec, out=out,
                                        workspace=ws, err=err)
@@ -416,6 +434,8 @@ def run_gb300(args, rank, world, local):
         if has_pre or not fused:
             pkv.slot_mapping(src_bt, src_sl, src_cu, T, sh.block_size, sh.num_blocks, out=slots,
                              err=err)
+        if planned and nd:
+            decode_plan(src_sl)
 
     def layer_decode(li, inputs=None, timed=False):
         lay = L[li]
@@ -427,9 +447,8 @@ def run_gb300(args, rank, world, local):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
         if fused:
-            pkv.paged_attention_decode_append(
-                q[:nd], k[:nd], v[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
-                sh.scale, max_dec, out=dec_out[li], workspace=ws, err=err)
+            decode_call(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
+                        dec_out[li], k_new=k[:nd], v_new=v[:nd])
         else:
             decode_call(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
                         dec_out[li])
@@ -460,14 +479,20 @@ def run_gb300(args, rank, world, local):
             if has_pre:
                 layer_prefill(li, inputs, timed)
 
-    # (prefix runs + their combine) + (plan above 2,048 sequences) + main + merge
-    dec_launches = ((2 if nd <= 2048 else 3) + (2 if P else 0)) if nd else 0
+    # (prefix runs + their combine) + (plan above 2,048 sequences) + main + merge;
+    # planned: one plan kernel per step, then main + merge per layer
+    dec_launches = (2 if planned else (2 if nd <= 2048 else 3) + (2 if P else 0)) if nd else 0
+    plan_launches = 1 if planned and nd else 0
     if fused:
-        launches_per_step = (1 if has_pre else 0) + n_layers * (dec_launches + (2 if has_pre else 0))
+        launches_per_step = (plan_launches + (1 if has_pre else 0) +
+                             n_layers * (dec_launches + (2 if has_pre else 0)))
     else:
-        launches_per_step = 1 + n_layers * ((1 if nd else 0) + dec_launches + (2 if has_pre else 0))
+        launches_per_step = plan_launches + 1 + n_layers * ((1 if nd else 0) + dec_launches +
+                                                            (2 if has_pre else 0))
 
     def decode_all():
+        if planned:
+            decode_plan(seq_lens)
         for li, lay in enumerate(L):
             decode_call(lay["q"][:nd], lay["k_pool"], lay["v_pool"], bt[:nd], seq_lens[:nd],
                         dec_out[li])
@@ -721,6 +746,8 @@ def run_gb300(args, rank, world, local):
         "decode_write": ("fused into the decode launch (decode_append)" if fused
                          else "separate kv_write launch"),
         "decode_shared_prefix_blocks": P,
+        "decode_plan": ("once per step for all timed layers (decode_plan + decode_planned)"
+                        if planned else "inside each decode call"),
         "decode_tokens_per_s": dec_tok_s,
         "decode_tokens_per_s_note": f"{nd} decode tokens per step of {sh.layers} layers, "
                                     f"{n_layers} timed layer(s) scaled by {sh.layers / n_layers:g}",

@@ -318,6 +318,51 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
                                              int32_t* err_word, void* stream);
 
 /*
+ * pkv_decode_plan / pkv_paged_attention_decode_planned - the work split of
+ * a decode step computed once and reused by every layer.
+ *
+ * "Day 16: the paged KV cache", design call 1: one block table serves every
+ * layer and grows once per step, so the lengths and tables a decode step
+ * reads are the same for all layers.  pkv_decode_plan turns seq_lens into
+ * the split of the step's blocks over the decode grid (which CTA walks
+ * which blocks) and leaves it in `workspace`; each layer's
+ * pkv_paged_attention_decode_planned then reads that plan instead of
+ * computing it, and reads its plan and first table entries before waiting
+ * for the kernel launched just before it (programmatic dependent launch),
+ * so that work overlaps the previous kernel's end.  The outputs are those
+ * of pkv_paged_attention_decode (k_new and v_new both NULL) or
+ * pkv_paged_attention_decode_append (both given), bit for bit.
+ *
+ * Contract: the planned calls pass the same num_seqs, n_heads, pool shape,
+ * max_blocks_per_seq, seq_lens (pointer and contents), max_seq_len and
+ * max_ctas as the plan call, and block_tables, seq_lens and the plan part
+ * of the workspace stay unchanged from the plan call to the last planned
+ * call (the decode writes only the partial-result part of the workspace,
+ * so one workspace serves a whole step's layers in stream order).  The
+ * plan reports bad lengths (PKV_DEVERR_LENGTH / _TABLE_WIDTH) once.
+ * Shared prefixes are not planned this way.
+ *
+ *   workspace  at least pkv_decode_workspace_bytes(...) bytes, 16-byte
+ *              aligned (the same workspace for the plan and its calls)
+ *   everything else as for pkv_paged_attention_decode(_append)
+ */
+pkv_status pkv_decode_plan(int32_t num_seqs, int32_t n_heads, const pkv_pool_desc* pool,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t max_ctas, void* workspace,
+                           size_t workspace_bytes, int32_t* err_word, void* stream);
+
+pkv_status pkv_paged_attention_decode_planned(const void* q, const void* k_new,
+                                              const void* v_new, int32_t num_seqs,
+                                              int32_t n_heads, void* k_pool, void* v_pool,
+                                              const pkv_pool_desc* pool,
+                                              const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq,
+                                              const int32_t* seq_lens, int32_t max_seq_len,
+                                              float scale, int32_t max_ctas, void* out,
+                                              void* workspace, size_t workspace_bytes,
+                                              int32_t* err_word, void* stream);
+
+/*
  * pkv_paged_attention_prefill - causal attention of a query chunk over the
  * sequence's paged history (chunked prefill).
  *

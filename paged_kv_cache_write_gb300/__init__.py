@@ -20,9 +20,12 @@ import torch
 
 __all__ = [
     "lib", "library_path", "PoolDesc", "PKV_F32", "PKV_BF16", "DEVERR",
-    "slot_mapping", "kv_write", "kv_gather", "decode_workspace_bytes",
-    "paged_attention_decode", "prefill_workspace_bytes", "paged_attention_prefill",
-    "status_string", "abi_version", "paged_attention_decode_noalloc",
+    "slot_mapping", "kv_write", "kv_gather", "copy_blocks", "decode_workspace_bytes",
+    "paged_attention_decode", "paged_attention_decode_append",
+    "decode_shared_prefix_workspace_bytes", "paged_attention_decode_shared_prefix",
+    "decode_plan", "paged_attention_decode_planned", "prefill_workspace_bytes",
+    "paged_attention_prefill", "status_string", "abi_version", "paged_attention_decode_noalloc",
+    "selftest_bounded_wait",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +33,7 @@ library_path = os.path.join(HERE, "libpkv.so")
 
 PKV_F32 = 0
 PKV_BF16 = 1
-DEVERR = {"block_id": 1, "slot": 2, "table_width": 4, "length": 8, "timeout": 16}
+DEVERR = {"block_id": 1, "slot": 2, "table_width": 4, "length": 8, "timeout": 16, "prefix": 32}
 
 
 class PoolDesc(ctypes.Structure):
@@ -85,6 +88,12 @@ def _load():
     L.pkv_paged_attention_decode_append.restype = _i32
     L.pkv_paged_attention_decode_append.argtypes = [_p, _p, _p, _i32, _i32, _p, _p, _desc, _p,
                                                     _i32, _p, _i32, _f, _i32, _p, _p, _sz, _p, _p]
+    L.pkv_decode_plan.restype = _i32
+    L.pkv_decode_plan.argtypes = [_i32, _i32, _desc, _i32, _p, _i32, _i32, _p, _sz, _p, _p]
+    L.pkv_paged_attention_decode_planned.restype = _i32
+    L.pkv_paged_attention_decode_planned.argtypes = [_p, _p, _p, _i32, _i32, _p, _p, _desc, _p,
+                                                     _i32, _p, _i32, _f, _i32, _p, _p, _sz, _p,
+                                                     _p]
     L.pkv_prefill_workspace_bytes.restype = _sz
     L.pkv_prefill_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
     L.pkv_paged_attention_prefill.restype = _i32
@@ -324,6 +333,49 @@ def paged_attention_decode_append(q, k_new, v_new, k_pool, v_pool, block_tables,
         _dev(q, "q", k_pool.dtype), _dev(k_new, "k_new", k_pool.dtype),
         _dev(v_new, "v_new", k_pool.dtype), B, H, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
         ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32), W,
+        _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), float(scale), int(max_ctas),
+        _dev(out, "out", k_pool.dtype), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _opt(err, "err", torch.int32),
+        _stream(stream)))
+    return out
+
+
+def decode_plan(k_pool, seq_lens, n_heads: int, max_blocks_per_seq: int, max_seq_len: int, *,
+                workspace, max_ctas: int = 0, err=None, stream=None):
+    """Split a decode step's blocks over the decode grid once, into
+    ``workspace``, for every layer's ``paged_attention_decode_planned``
+    (same lengths, tables, shapes and ``max_ctas`` until the step ends)."""
+    desc = pool_desc(k_pool)
+    B = seq_lens.shape[0]
+    _check("pkv_decode_plan", _load().pkv_decode_plan(
+        B, int(n_heads), ctypes.byref(desc), int(max_blocks_per_seq),
+        _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), int(max_ctas),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _opt(err, "err", torch.int32), _stream(stream)))
+    return workspace
+
+
+def paged_attention_decode_planned(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
+                                   max_seq_len: int, *, workspace, k_new=None, v_new=None,
+                                   out=None, max_ctas: int = 0, err=None, stream=None):
+    """``paged_attention_decode`` (or, with ``k_new``/``v_new``,
+    ``paged_attention_decode_append``) using the plan ``decode_plan`` left
+    in ``workspace``."""
+    desc = pool_desc(k_pool)
+    B, H, hd = q.shape
+    W = block_tables.shape[1]
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None and (k_new.shape != (B, desc.n_kv, hd) or v_new.shape != k_new.shape):
+        raise ValueError(f"k_new/v_new must be {(B, desc.n_kv, hd)}")
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pkv_paged_attention_decode_planned", _load().pkv_paged_attention_decode_planned(
+        _dev(q, "q", k_pool.dtype),
+        None if k_new is None else _dev(k_new, "k_new", k_pool.dtype),
+        None if v_new is None else _dev(v_new, "v_new", k_pool.dtype), B, H,
+        _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), ctypes.byref(desc),
+        _dev(block_tables, "block_tables", torch.int32), W,
         _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), float(scale), int(max_ctas),
         _dev(out, "out", k_pool.dtype), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _opt(err, "err", torch.int32),

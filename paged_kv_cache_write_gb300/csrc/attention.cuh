@@ -652,6 +652,12 @@ struct DecodeParams {
   float* pre_o;   // [chunks][B][n_heads][HD] normalised prefix outputs
   float* pre_ml;  // [chunks][B][n_heads][2] prefix max (log2 units) and exp-sum
   int plan_in_kernel;  // 1: each CTA scans the lengths itself (no plan kernel)
+  // 1 (plan kernel): compute the plan only, for later calls: write cu_units,
+  // zero no output, let no dependent start before it has finished
+  int plan_only;
+  // 1 (main kernel): the plan is in the workspace from a finished plan-only
+  // launch, so it and the tables are read before the dependency wait
+  int planned;
   float scale_log2;
 };
 
@@ -790,7 +796,7 @@ __device__ __forceinline__ void zero_empty(const DecodeParams& p, int first, int
 
 template <typename T, int HD>
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
-  pdl_launch_dependents();
+  if (!p.plan_only) pdl_launch_dependents();
   __shared__ int warp_tot[32];
   __shared__ int cu_s[kPlanSmemSeqs + 1];
   const bool in_smem = p.B <= kPlanSmemSeqs;
@@ -826,8 +832,12 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     }
     p.starts[c] = st;
   }
-  if (p.prefix_blocks == 0)  // with a prefix, the prefix kernel writes them
+  if (p.plan_only) {  // kept for the calls that use the plan (empty sequences)
+    if (in_smem)
+      for (int b = tid; b <= p.B; b += blockDim.x) p.cu_units[b] = cu[b];
+  } else if (p.prefix_blocks == 0) {  // with a prefix, the prefix kernel writes them
     zero_empty<T, HD>(p, 0, 1, [&](int b) { return used_len(p, b) == 0; });
+  }
 }
 
 // Walks this CTA's contiguous range of units segment by segment: a segment
@@ -906,7 +916,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
   Ring ring = MMA ? make_tile_ring(smem, p.nstages, kBS * row_bytes)
                   : make_ring(smem, p.nstages, row_bytes);
   ring_init(ring, consumers);
-  pdl_wait();  // inputs written by the preceding kernel (the plan, when there is one)
+  // inputs written by the preceding kernel (the plan, when there is one);
+  // a planned call waits after reading its plan and first table entries
+  if (!p.planned) pdl_wait();
   pdl_launch_dependents();  // the merge kernel may be scheduled (it waits for this grid)
 
   const int warp = threadIdx.x >> 5;
@@ -960,6 +972,21 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
   const int rows_per_group = p.hg_size * p.rep;
   Cursor cur;
   if (r0 < r1) cur.load(p, st);
+  // planned call: the producer's first table entries are loaded before the
+  // wait (the plan's contract: lengths and tables unchanged since the plan)
+  int pre_id = 0;
+  bool pre = false;
+  if (p.planned) {
+    if (warp == consumers && r0 < r1) {
+      const int n0 = min(r1 - r0, cur.nblk - cur.j);
+      pre_id = lane < n0 ? __ldg(p.bt + int64_t(cur.b) * p.W + p.prefix_blocks + cur.j + lane) : 0;
+      pre = true;
+    }
+    pdl_wait();
+    if (p.prefix_blocks == 0)
+      zero_empty<T, HD>(p, blockIdx.x, G,
+                        [&](int b) { return __ldcg(p.cu_units + b + 1) == __ldcg(p.cu_units + b); });
+  }
 
   if (warp == consumers) {
     // ------------------------------------------------------ producer
@@ -970,7 +997,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
       const int32_t* row = p.bt + int64_t(cur.b) * p.W;
       const int64_t head_off = int64_t(cur.grp) * p.hg_size * HD * p.elem_bytes;
       for (int jj = 0; jj < n && ok; jj += 32) {
-        int id = (jj + lane < n) ? __ldg(row + p.prefix_blocks + cur.j + jj + lane) : 0;
+        int id = pre ? pre_id : (jj + lane < n) ? __ldg(row + p.prefix_blocks + cur.j + jj + lane) : 0;
+        pre = false;
         const int n_here = min(32, n - jj);
         for (int k = 0; k < n_here; ++k) {
           if (*ring.abort_flag) { ok = false; break; }
@@ -1463,6 +1491,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     mbar_init(bar, 1);
     fence_barrier_init();
   }
+  pdl_launch_dependents();  // the next kernel's prologue may overlap this merge
   pdl_wait();  // the main kernel's partials and split entries
   const int4 sp = __ldcg(p.splits + blockIdx.x);
   if (sp.x < 0) return;
@@ -1710,6 +1739,13 @@ struct DecodeLaunch {
     p.ws_o = reinterpret_cast<float*>(ws + L.o);
     p.pre_o = reinterpret_cast<float*>(ws + L.pre_o);
     p.pre_ml = reinterpret_cast<float*>(ws + L.pre_ml);
+    if (a.decode_plan != kPlanInCall && p.prefix_blocks > 0) return cudaErrorInvalidValue;
+    if (a.decode_plan == kPlanOnly) {  // the plan alone, kept in the workspace
+      p.plan_only = 1;
+      p.out = nullptr;
+      decode_plan_kernel<T, HD><<<1, 1024, 0, stream>>>(p);
+      return cudaGetLastError();
+    }
     // tensor-core path: the pools as 4-D tensors (64 dims, slot, 64-dim half,
     // KV head) read in boxes of one block's 16 slots x the group's heads
     CUtensorMap tm_k{}, tm_v{};
@@ -1750,11 +1786,13 @@ struct DecodeLaunch {
       e = cudaLaunchKernelEx(&pcfg, decode_prefix_combine_kernel<T, HD>, p);
       if (e != cudaSuccess) return e;
     }
-    // small batches: every CTA scans the lengths in its ring stages
+    // small batches: every CTA scans the lengths in its ring stages (unless
+    // the plan is already in the workspace)
     const size_t ring_bytes = size_t(p.nstages) * stage_bytes(hg, p.elem_bytes, MMA);
-    p.plan_in_kernel =
-        a.num_seqs <= kKernelPlanSeqs && size_t(a.num_seqs + 1 + 32) * 4 <= ring_bytes;
-    if (!p.plan_in_kernel) {
+    p.planned = a.decode_plan == kPlanned;
+    p.plan_in_kernel = !p.planned && a.num_seqs <= kKernelPlanSeqs &&
+                       size_t(a.num_seqs + 1 + 32) * 4 <= ring_bytes;
+    if (!p.plan_in_kernel && !p.planned) {
       decode_plan_kernel<T, HD><<<1, 1024, 0, stream>>>(p);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

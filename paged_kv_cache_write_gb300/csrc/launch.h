@@ -56,10 +56,16 @@ struct AttnArgs {
   const void* v_new;
   // decode: leading table entries shared by every sequence (0: none)
   int32_t prefix_blocks;
+  // decode: kPlanInCall (plan inside the call), kPlanOnly (compute the
+  // plan into the workspace, nothing else) or kPlanned (use the plan a
+  // kPlanOnly call with the same arguments left in the workspace)
+  int32_t decode_plan;
   void* workspace;
   size_t workspace_bytes;
   int32_t* err;
 };
+
+enum : int32_t { kPlanInCall = 0, kPlanOnly = 1, kPlanned = 2 };
 
 // Decode support / sizing.
 bool decode_supported(const PoolShape& pool, int32_t n_heads);

@@ -188,3 +188,49 @@ def test_prefill_host_checks(pkv):
 def test_workspace_bytes_positive(pkv):
     assert pkv.decode_workspace_bytes(4, 8, 16, 100) > 0
     assert pkv.decode_workspace_bytes(0, 8, 16, 0) > 0
+
+
+def _plan(pkv, **over):
+    a = dict(B=2, H=8, desc=_desc(pkv), W=4, sl=FAKE, maxlen=64, max_ctas=0, ws=FAKE,
+             wsb=1 << 40, err=None)
+    a.update(over)
+    return pkv.lib.pkv_decode_plan(a["B"], a["H"], ctypes.byref(a["desc"]), a["W"], a["sl"],
+                                   a["maxlen"], a["max_ctas"], a["ws"], a["wsb"], a["err"], None)
+
+
+def test_decode_plan_host_checks(pkv):
+    assert _plan(pkv, sl=None) == 1
+    assert _plan(pkv, H=7) == 2                        # n_heads % n_kv
+    assert _plan(pkv, maxlen=65) == 2                  # > W * block_size
+    assert _plan(pkv, B=-1) == 2
+    assert _plan(pkv, max_ctas=-1) == 5
+    assert _plan(pkv, ws=None) == 6
+    assert _plan(pkv, wsb=16) == 6
+    assert _plan(pkv, ws=FAKE + 8) == 4
+    assert _plan(pkv, desc=_desc(pkv, head_dim=48)) == 7
+    assert _plan(pkv, desc=_desc(pkv, dtype=9)) == 3
+    assert _plan(pkv, B=0, sl=None) == 0
+
+
+def _planned(pkv, **over):
+    a = dict(q=FAKE, kn=None, vn=None, B=2, H=8, k=FAKE, v=FAKE, desc=_desc(pkv), bt=FAKE, W=4,
+             sl=FAKE, maxlen=64, scale=0.125, max_ctas=0, out=FAKE, ws=FAKE, wsb=1 << 40, err=None)
+    a.update(over)
+    return pkv.lib.pkv_paged_attention_decode_planned(
+        a["q"], a["kn"], a["vn"], a["B"], a["H"], a["k"], a["v"], ctypes.byref(a["desc"]), a["bt"],
+        a["W"], a["sl"], a["maxlen"], a["scale"], a["max_ctas"], a["out"], a["ws"], a["wsb"],
+        a["err"], None)
+
+
+def test_decode_planned_host_checks(pkv):
+    assert _planned(pkv, kn=FAKE) == 1                 # k_new without v_new
+    assert _planned(pkv, vn=FAKE) == 1
+    assert _planned(pkv, kn=FAKE, vn=FAKE + 4) == 4
+    assert _planned(pkv, q=None) == 1
+    assert _planned(pkv, bt=None) == 1
+    assert _planned(pkv, H=7) == 2
+    assert _planned(pkv, scale=0.0) == 5
+    assert _planned(pkv, ws=None) == 6
+    assert _planned(pkv, wsb=16) == 6
+    assert _planned(pkv, desc=_desc(pkv, head_dim=48)) == 7
+    assert _planned(pkv, B=0) == 0

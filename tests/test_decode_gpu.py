@@ -179,3 +179,34 @@ def test_decode_reports_bad_lengths_and_ids():
     torch.cuda.synchronize()
     assert g.err.item() & (pkv.DEVERR["length"] | pkv.DEVERR["table_width"])
     assert torch.isfinite(out.float()).all()
+
+
+REUSE = [("llama2-70b-decode64", "bf16"), ("llama-3.2-1b", "bf16"), ("smollm2-135m", "bf16"),
+         ("toy", "f32")]
+
+
+@pytest.mark.parametrize("name,dt", REUSE, ids=[r[0] for r in REUSE])
+def test_workspace_reused_across_calls_and_grids(name, dt):
+    """One workspace serves many calls of different grid sizes without
+    clearing: every output row is written each call (outputs start as
+    NaN) and each call matches the oracle."""
+    plan = draw_plan(name)
+    layer = make_layer(plan, 0)
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.run_write()
+    g.write(g.slots())
+    rows = _sample_rows(plan)
+    ref = o.decode(rows=rows)
+    sh, nd, t = plan.shape, plan.n_decode, g.t
+    ws = torch.full((g.pkv.decode_workspace_bytes(nd, sh.n_heads, sh.head_dim, g.max_dec),),
+                    255, dtype=torch.uint8, device="cuda")  # garbage before the first call
+    for max_ctas in (0, 3, 16, 0, 7):
+        for _ in range(2):
+            out = torch.full_like(t["q"][:nd], float("nan"))
+            g.pkv.paged_attention_decode(t["q"][:nd], t["k_pool"], t["v_pool"], g.bt[:nd],
+                                         g.seq_lens[:nd], sh.scale, g.max_dec, out=out,
+                                         workspace=ws, max_ctas=max_ctas, err=g.err)
+            torch.cuda.synchronize()
+            assert int(g.err.item()) == 0
+            assert_close(f64(out)[rows], ref[rows], dt, f"{name} max_ctas={max_ctas}")
+            assert not torch.isnan(out.float()).any()
