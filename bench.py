@@ -437,7 +437,7 @@ def run_gb300(args, rank, world, local):
         if planned and nd:
             decode_plan(src_sl)
 
-    def layer_decode(li, inputs=None, timed=False):
+    def layer_decode(li, inputs=None, timed=False, outs=None):
         lay = L[li]
         src_bt, src_sl = (bt, seq_lens) if inputs is None else inputs[:2]
         q, k, v = (lay["q"], lay["k"], lay["v"]) if inputs is None else inputs[3][li]
@@ -448,15 +448,15 @@ def run_gb300(args, rank, world, local):
             e0.record(stream)
         if fused:
             decode_call(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
-                        dec_out[li], k_new=k[:nd], v_new=v[:nd])
+                        (outs or dec_out)[li], k_new=k[:nd], v_new=v[:nd])
         else:
             decode_call(q[:nd], lay["k_pool"], lay["v_pool"], src_bt[:nd], src_sl[:nd],
-                        dec_out[li])
+                        (outs or dec_out)[li])
         if timed:
             e1.record(stream)
             ev_dec.append((e0, e1))
 
-    def layer_prefill(li, inputs=None, timed=False):
+    def layer_prefill(li, inputs=None, timed=False, outs=None):
         lay = L[li]
         src_bt, src_sl = (bt, seq_lens) if inputs is None else inputs[:2]
         q, k, v = (lay["q"], lay["k"], lay["v"]) if inputs is None else inputs[3][li]
@@ -465,7 +465,7 @@ def run_gb300(args, rank, world, local):
             e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e2.record(stream)
         pkv.paged_attention_prefill(q[nd:], cu_q, lay["k_pool"], lay["v_pool"], src_bt[nd:],
-                                    src_sl[nd:], sh.scale, max_q, max_pre, out=pre_out[li],
+                                    src_sl[nd:], sh.scale, max_q, max_pre, out=(outs or pre_out)[li],
                                     err=err)
         if timed:
             e3.record(stream)
@@ -603,70 +603,93 @@ def run_gb300(args, rank, world, local):
     if not args.no_e2e:
         host_in = [t.cpu().pin_memory() for t in (bt, seq_lens, cu_new)]
         host_layers = [[lay[n].cpu().pin_memory() for n in ("q", "k", "v")] for lay in L]
-        dev_in = [torch.empty_like(t) for t in (bt, seq_lens, cu_new)]
-        dev_layers = [[torch.empty_like(lay[n]) for n in ("q", "k", "v")] for lay in L]
         host_out = [o.cpu().pin_memory() for o in dec_out] + ([o.cpu().pin_memory() for o in pre_out]
                                                               if has_pre else [])
+        # two sets of device inputs and outputs, alternating between steps, so
+        # a step's copies overlap its neighbours' compute
+        dev_in = [[torch.empty_like(t) for t in (bt, seq_lens, cu_new)] for _ in range(2)]
+        dev_layers = [[[torch.empty_like(lay[n]) for n in ("q", "k", "v")] for lay in L]
+                      for _ in range(2)]
+        dev_dec = [dec_out, [torch.empty_like(o) for o in dec_out]]
+        dev_pre = [pre_out, [torch.empty_like(o) for o in pre_out] if has_pre else None]
         h2d = sum(t.numel() * t.element_size() for t in host_in) + sum(
             t.numel() * t.element_size() for lay in host_layers for t in lay)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
         h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        steps_per_graph = 4
 
-        def e2e_step():
-            # Pipelined: the tables go first; one stream then brings in each
-            # layer's decode rows, then its prefill rows, while the compute
-            # stream starts each part as soon as it has landed (decode and
-            # prefill rows are different sequences); a second stream copies
-            # each part's output back as soon as it is computed.
+        def e2e_steps():
+            # Step i uses buffer set i % 2.  Its copies in start once step i-2
+            # has finished computing from that set; its compute starts each
+            # layer's decode rows, then prefill rows, as soon as they have
+            # landed; each part's output goes back on a second stream once it
+            # is computed, and step i+2 overwrites those outputs only after
+            # that copy.  Every step copies all its inputs in and all its
+            # outputs out.
             main = torch.cuda.current_stream(dev)
-            for d, h in zip(dev_in, host_in):
-                d.copy_(h, non_blocking=True)
-            h2d_s.wait_stream(main)  # the previous step is done with the input buffers
+            h2d_s.wait_stream(main)
             d2h_s.wait_stream(main)
-            ev_d, ev_p = [], []
-            with torch.cuda.stream(h2d_s):
-                for dl, hl in zip(dev_layers, host_layers):
-                    for part, evs in ((slice(0, nd), ev_d), (slice(nd, None), ev_p)):
-                        for d, h in zip(dl, hl):
-                            d[part].copy_(h[part], non_blocking=True)
+            computed = [None] * steps_per_graph
+            copied_out = [None] * steps_per_graph
+            for i in range(steps_per_graph):
+                b = i % 2
+                if i >= 2:
+                    h2d_s.wait_event(computed[i - 2])
+                ev_d, ev_p = [], []
+                with torch.cuda.stream(h2d_s):
+                    for d, h in zip(dev_in[b], host_in):
+                        d.copy_(h, non_blocking=True)
+                    for dl, hl in zip(dev_layers[b], host_layers):
+                        for part, evs in ((slice(0, nd), ev_d), (slice(nd, None), ev_p)):
+                            for d, h in zip(dl, hl):
+                                d[part].copy_(h[part], non_blocking=True)
+                            e = torch.cuda.Event()
+                            e.record(h2d_s)
+                            evs.append(e)
+                if i >= 2:
+                    main.wait_event(copied_out[i - 2])
+                inputs = (dev_in[b][0], dev_in[b][1], dev_in[b][2], dev_layers[b])
+                main.wait_event(ev_d[0])  # the tables came first
+                step_head(inputs)
+                for li in range(len(L)):
+                    for run, outs, evs, off, on in ((layer_decode, dev_dec[b], ev_d, 0, nd > 0),
+                                                    (layer_prefill, dev_pre[b], ev_p, len(dec_out),
+                                                     has_pre)):
+                        if not on:
+                            continue
+                        main.wait_event(evs[li])
+                        run(li, inputs, outs=outs)
                         e = torch.cuda.Event()
-                        e.record(h2d_s)
-                        evs.append(e)
-            inputs = (dev_in[0], dev_in[1], dev_in[2], dev_layers)
-            step_head(inputs)
-            for li in range(len(L)):
-                for run, outs, evs, off, on in ((layer_decode, dec_out, ev_d, 0, nd > 0),
-                                                (layer_prefill, pre_out, ev_p, len(dec_out),
-                                                 has_pre)):
-                    if not on:
-                        continue
-                    main.wait_event(evs[li])
-                    run(li, inputs)
-                    e = torch.cuda.Event()
-                    e.record(main)
-                    d2h_s.wait_event(e)
-                    with torch.cuda.stream(d2h_s):
-                        host_out[off + li].copy_(outs[li], non_blocking=True)
+                        e.record(main)
+                        d2h_s.wait_event(e)
+                        with torch.cuda.stream(d2h_s):
+                            host_out[off + li].copy_(outs[li], non_blocking=True)
+                computed[i] = torch.cuda.Event()
+                computed[i].record(main)
+                copied_out[i] = torch.cuda.Event()
+                copied_out[i].record(d2h_s)
             main.wait_stream(h2d_s)
             main.wait_stream(d2h_s)
 
-        for _ in range(3):
-            e2e_step()
+        for _ in range(2):
+            e2e_steps()
         torch.cuda.synchronize()
-        run_e2e = capture(e2e_step).replay if use_graph else e2e_step
+        run_e2e = capture(e2e_steps).replay if use_graph else e2e_steps
         barrier(world)
-        e_steps = max(3, args.steps // 3)
+        e_reps = max(1, args.steps // (3 * steps_per_graph))
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
-        for _ in range(e_steps):
+        for _ in range(e_reps):
             run_e2e()
         s1.record(stream)
         torch.cuda.synchronize()
-        e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev) / e_steps
+        e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev) / (e_reps * steps_per_graph)
         e2e = {"value": world * step_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "copies": "each layer's decode, then prefill, inputs copied in on one stream and "
-                         "outputs copied back on another, overlapping the compute"}
+               "copies": f"every step copies all its inputs in and all its outputs out; inputs "
+                         f"and outputs double-buffered so a step's copies (one stream in, one "
+                         f"out, per layer and part as soon as possible) overlap its neighbours' "
+                         f"compute; timed over {e_reps} x {steps_per_graph} steps"}
 
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} in the timed region")
