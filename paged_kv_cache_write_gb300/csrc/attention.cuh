@@ -1280,30 +1280,29 @@ __global__ void __launch_bounds__(256) decode_prefix_combine_kernel(DecodeParams
   const int64_t row = i / V;
   const int e = static_cast<int>(i - row * V) * 4;
   const int K = p.prefix_chunks;
-  float mk[kMaxPrefixRuns], lk[kMaxPrefixRuns];
-  float M = -INFINITY;
+  // every run's max / sum and partial output are loaded before any is used,
+  // so the loads are all in flight at once
+  float2 ml[kMaxPrefixRuns];
+  float4 o[kMaxPrefixRuns];
 #pragma unroll
   for (int k = 0; k < kMaxPrefixRuns; ++k) {
-    mk[k] = -INFINITY;
-    lk[k] = 0.f;
-    if (k < K) {
-      const float2 x = *reinterpret_cast<const float2*>(p.pre_ml + (k * rows + row) * 2);
-      mk[k] = x.x;
-      lk[k] = x.y;
-    }
-    if (lk[k] > 0.f) M = fmaxf(M, mk[k]);  // a run that saw no key has no weight
+    ml[k] = k < K ? __ldcg(reinterpret_cast<const float2*>(p.pre_ml + (k * rows + row) * 2))
+                  : make_float2(-INFINITY, 0.f);
+    o[k] = k < K ? __ldcg(reinterpret_cast<const float4*>(p.pre_o + (k * rows + row) * HD + e))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kMaxPrefixRuns; ++k)
+    if (ml[k].y > 0.f) M = fmaxf(M, ml[k].x);  // a run that saw no key has no weight
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
 #pragma unroll
   for (int k = 0; k < kMaxPrefixRuns; ++k) {
-    if (k < K) {
-      const float w = lk[k] > 0.f ? fast_exp2(mk[k] - M) * lk[k] : 0.f;
-      den += w;
-      const float4 o = *reinterpret_cast<const float4*>(p.pre_o + (k * rows + row) * HD + e);
-      acc = make_float4(fmaf(w, o.x, acc.x), fmaf(w, o.y, acc.y), fmaf(w, o.z, acc.z),
-                        fmaf(w, o.w, acc.w));
-    }
+    const float w = ml[k].y > 0.f ? fast_exp2(ml[k].x - M) * ml[k].y : 0.f;
+    den += w;
+    acc = make_float4(fmaf(w, o[k].x, acc.x), fmaf(w, o[k].y, acc.y), fmaf(w, o[k].z, acc.z),
+                      fmaf(w, o[k].w, acc.w));
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   const int b = static_cast<int>(row / p.n_heads);
