@@ -408,20 +408,20 @@ def run_gb300(args, rank, world, local):
     # the decode rows' work split, planned once per step for all its layers
     # (a one-layer step plans inside its call: a separate plan would not be
     # shared by anything)
-    planned = P == 0 and not args.no_plan and len(L) > 1
+    planned = not args.no_plan and len(L) > 1
 
     def decode_plan(sl_):
         pkv.decode_plan(L[0]["k_pool"], sl_[:nd], sh.n_heads, bt.shape[1], max_dec, workspace=ws,
-                        err=err)
+                        shared_prefix_blocks=P, err=err)
 
     def decode_call(q, k_pool, v_pool, bt_, sl_, out, k_new=None, v_new=None):
-        if P:
+        if planned:
+            pkv.paged_attention_decode_planned(q, k_pool, v_pool, bt_, sl_, sh.scale, max_dec,
+                                               workspace=ws, k_new=k_new, v_new=v_new,
+                                               shared_prefix_blocks=P, out=out, err=err)
+        elif P:
             pkv.paged_attention_decode_shared_prefix(q, k_pool, v_pool, bt_, sl_, sh.scale, P,
                                                      max_dec, out=out, workspace=ws, err=err)
-        elif planned:
-            pkv.paged_attention_decode_planned(q, k_pool, v_pool, bt_, sl_, sh.scale, max_dec,
-                                               workspace=ws, k_new=k_new, v_new=v_new, out=out,
-                                               err=err)
         elif k_new is not None:
             pkv.paged_attention_decode_append(q, k_new, v_new, k_pool, v_pool, bt_, sl_, sh.scale,
                                               max_dec, out=out, workspace=ws, err=err)
@@ -480,8 +480,8 @@ def run_gb300(args, rank, world, local):
                 layer_prefill(li, inputs, timed)
 
     # (prefix runs + their combine) + (plan above 2,048 sequences) + main + merge;
-    # planned: one plan kernel per step, then main + merge per layer
-    dec_launches = (2 if planned else (2 if nd <= 2048 else 3) + (2 if P else 0)) if nd else 0
+    # planned: one plan kernel per step, then (prefix runs + combine +) main + merge per layer
+    dec_launches = (((2 if planned or nd <= 2048 else 3) + (2 if P else 0)) if nd else 0)
     plan_launches = 1 if planned and nd else 0
     if fused:
         launches_per_step = (plan_launches + (1 if has_pre else 0) +

@@ -321,9 +321,9 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * pkv_decode_plan / pkv_paged_attention_decode_planned - the work split of
  * a decode step computed once and reused by every layer.
  *
- * "Day 16: the paged KV cache", design call 1: one block table serves every
- * layer and grows once per step, so the lengths and tables a decode step
- * reads are the same for all layers.  pkv_decode_plan turns seq_lens into
+ * "Day 16: the paged KV cache", What I learned 1-2: one block table serves
+ * every layer and grows once per step, at layer 0, so the lengths and
+ * tables a decode step reads are the same for all layers.  pkv_decode_plan turns seq_lens into
  * the split of the step's blocks over the decode grid (which CTA walks
  * which blocks) and leaves it in `workspace`; each layer's
  * pkv_paged_attention_decode_planned then reads that plan instead of
@@ -331,7 +331,11 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * for the kernel launched just before it (programmatic dependent launch),
  * so that work overlaps the previous kernel's end.  The outputs are those
  * of pkv_paged_attention_decode (k_new and v_new both NULL) or
- * pkv_paged_attention_decode_append (both given), bit for bit.
+ * pkv_paged_attention_decode_append (both given), bit for bit; with
+ * shared_prefix_blocks > 0 they are those of
+ * pkv_paged_attention_decode_shared_prefix (the prefix runs and their
+ * combine are launched by each planned call; the plan covers the blocks
+ * after the prefix), bit for bit.
  *
  * Contract: the planned calls pass the same num_seqs, n_heads, pool shape,
  * max_blocks_per_seq, seq_lens (pointer and contents), max_seq_len and
@@ -340,16 +344,22 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * call (the decode writes only the partial-result part of the workspace,
  * so one workspace serves a whole step's layers in stream order).  The
  * plan reports bad lengths (PKV_DEVERR_LENGTH / _TABLE_WIDTH) once.
- * Shared prefixes are not planned this way.
  *
- *   workspace  at least pkv_decode_workspace_bytes(...) bytes, 16-byte
- *              aligned (the same workspace for the plan and its calls)
+ *   shared_prefix_blocks  as for pkv_paged_attention_decode_shared_prefix
+ *              (0 = none; the same value for the plan and its calls); with
+ *              a shared prefix k_new and v_new must be NULL (else
+ *              PKV_ERR_RANGE)
+ *   workspace  at least pkv_decode_workspace_bytes(...) bytes (with a
+ *              shared prefix, pkv_decode_shared_prefix_workspace_bytes),
+ *              16-byte aligned (the same workspace for the plan and its
+ *              calls)
  *   everything else as for pkv_paged_attention_decode(_append)
  */
 pkv_status pkv_decode_plan(int32_t num_seqs, int32_t n_heads, const pkv_pool_desc* pool,
                            int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                           int32_t max_seq_len, int32_t max_ctas, void* workspace,
-                           size_t workspace_bytes, int32_t* err_word, void* stream);
+                           int32_t max_seq_len, int32_t shared_prefix_blocks, int32_t max_ctas,
+                           void* workspace, size_t workspace_bytes, int32_t* err_word,
+                           void* stream);
 
 pkv_status pkv_paged_attention_decode_planned(const void* q, const void* k_new,
                                               const void* v_new, int32_t num_seqs,
@@ -358,9 +368,10 @@ pkv_status pkv_paged_attention_decode_planned(const void* q, const void* k_new,
                                               const int32_t* block_tables,
                                               int32_t max_blocks_per_seq,
                                               const int32_t* seq_lens, int32_t max_seq_len,
-                                              float scale, int32_t max_ctas, void* out,
-                                              void* workspace, size_t workspace_bytes,
-                                              int32_t* err_word, void* stream);
+                                              int32_t shared_prefix_blocks, float scale,
+                                              int32_t max_ctas, void* out, void* workspace,
+                                              size_t workspace_bytes, int32_t* err_word,
+                                              void* stream);
 
 /*
  * pkv_paged_attention_prefill - causal attention of a query chunk over the

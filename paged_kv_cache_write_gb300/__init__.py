@@ -89,11 +89,11 @@ def _load():
     L.pkv_paged_attention_decode_append.argtypes = [_p, _p, _p, _i32, _i32, _p, _p, _desc, _p,
                                                     _i32, _p, _i32, _f, _i32, _p, _p, _sz, _p, _p]
     L.pkv_decode_plan.restype = _i32
-    L.pkv_decode_plan.argtypes = [_i32, _i32, _desc, _i32, _p, _i32, _i32, _p, _sz, _p, _p]
+    L.pkv_decode_plan.argtypes = [_i32, _i32, _desc, _i32, _p, _i32, _i32, _i32, _p, _sz, _p, _p]
     L.pkv_paged_attention_decode_planned.restype = _i32
     L.pkv_paged_attention_decode_planned.argtypes = [_p, _p, _p, _i32, _i32, _p, _p, _desc, _p,
-                                                     _i32, _p, _i32, _f, _i32, _p, _p, _sz, _p,
-                                                     _p]
+                                                     _i32, _p, _i32, _i32, _f, _i32, _p, _p, _sz,
+                                                     _p, _p]
     L.pkv_prefill_workspace_bytes.restype = _sz
     L.pkv_prefill_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
     L.pkv_paged_attention_prefill.restype = _i32
@@ -341,15 +341,18 @@ def paged_attention_decode_append(q, k_new, v_new, k_pool, v_pool, block_tables,
 
 
 def decode_plan(k_pool, seq_lens, n_heads: int, max_blocks_per_seq: int, max_seq_len: int, *,
-                workspace, max_ctas: int = 0, err=None, stream=None):
+                workspace, shared_prefix_blocks: int = 0, max_ctas: int = 0, err=None,
+                stream=None):
     """Split a decode step's blocks over the decode grid once, into
     ``workspace``, for every layer's ``paged_attention_decode_planned``
-    (same lengths, tables, shapes and ``max_ctas`` until the step ends)."""
+    (same lengths, tables, shapes, shared prefix and ``max_ctas`` until the
+    step ends)."""
     desc = pool_desc(k_pool)
     B = seq_lens.shape[0]
     _check("pkv_decode_plan", _load().pkv_decode_plan(
         B, int(n_heads), ctypes.byref(desc), int(max_blocks_per_seq),
-        _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), int(max_ctas),
+        _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), int(shared_prefix_blocks),
+        int(max_ctas),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _opt(err, "err", torch.int32), _stream(stream)))
     return workspace
@@ -357,10 +360,12 @@ def decode_plan(k_pool, seq_lens, n_heads: int, max_blocks_per_seq: int, max_seq
 
 def paged_attention_decode_planned(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
                                    max_seq_len: int, *, workspace, k_new=None, v_new=None,
-                                   out=None, max_ctas: int = 0, err=None, stream=None):
-    """``paged_attention_decode`` (or, with ``k_new``/``v_new``,
-    ``paged_attention_decode_append``) using the plan ``decode_plan`` left
-    in ``workspace``."""
+                                   shared_prefix_blocks: int = 0, out=None, max_ctas: int = 0,
+                                   err=None, stream=None):
+    """``paged_attention_decode`` (with ``k_new``/``v_new``,
+    ``paged_attention_decode_append``; with ``shared_prefix_blocks``,
+    ``paged_attention_decode_shared_prefix``) using the plan
+    ``decode_plan`` left in ``workspace``."""
     desc = pool_desc(k_pool)
     B, H, hd = q.shape
     W = block_tables.shape[1]
@@ -376,8 +381,8 @@ def paged_attention_decode_planned(q, k_pool, v_pool, block_tables, seq_lens, sc
         None if v_new is None else _dev(v_new, "v_new", k_pool.dtype), B, H,
         _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), ctypes.byref(desc),
         _dev(block_tables, "block_tables", torch.int32), W,
-        _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), float(scale), int(max_ctas),
-        _dev(out, "out", k_pool.dtype), _dev(workspace, "workspace"),
+        _dev(seq_lens, "seq_lens", torch.int32), int(max_seq_len), int(shared_prefix_blocks),
+        float(scale), int(max_ctas), _dev(out, "out", k_pool.dtype), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _opt(err, "err", torch.int32),
         _stream(stream)))
     return out

@@ -252,8 +252,9 @@ pkv_status pkv_paged_attention_decode_append(
 
 pkv_status pkv_decode_plan(int32_t num_seqs, int32_t n_heads, const pkv_pool_desc* pool,
                            int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                           int32_t max_seq_len, int32_t max_ctas, void* workspace,
-                           size_t workspace_bytes, int32_t* err_word, void* stream) {
+                           int32_t max_seq_len, int32_t shared_prefix_blocks, int32_t max_ctas,
+                           void* workspace, size_t workspace_bytes, int32_t* err_word,
+                           void* stream) {
   PoolShape shape;
   pkv_status st = check_pool(pool, &shape);
   if (st != PKV_OK) return st;
@@ -261,14 +262,15 @@ pkv_status pkv_decode_plan(int32_t num_seqs, int32_t n_heads, const pkv_pool_des
     return PKV_ERR_SHAPE;
   if (n_heads % shape.n_kv != 0) return PKV_ERR_SHAPE;
   if (max_ctas < 0) return PKV_ERR_RANGE;
+  if (shared_prefix_blocks < 0 || shared_prefix_blocks > max_blocks_per_seq) return PKV_ERR_RANGE;
   if (!pkv::decode_supported(shape, n_heads)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
   if (!seq_lens) return PKV_ERR_NULL;
   if (max_blocks_per_seq == 0 && max_seq_len > 0) return PKV_ERR_SHAPE;
   if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * shape.block_size) return PKV_ERR_SHAPE;
   if (!workspace) return PKV_ERR_WORKSPACE;
-  if (workspace_bytes <
-      pkv::decode_workspace_bytes(num_seqs, n_heads, shape.head_dim, max_seq_len, max_ctas, 0))
+  if (workspace_bytes < pkv::decode_workspace_bytes(num_seqs, n_heads, shape.head_dim,
+                                                    max_seq_len, max_ctas, shared_prefix_blocks))
     return PKV_ERR_WORKSPACE;
   if (!aligned16(workspace)) return PKV_ERR_ALIGN;
   pkv::AttnArgs a{};
@@ -284,6 +286,7 @@ pkv_status pkv_decode_plan(int32_t num_seqs, int32_t n_heads, const pkv_pool_des
   a.max_ctas = max_ctas;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
+  a.prefix_blocks = shared_prefix_blocks;
   a.decode_plan = pkv::kPlanOnly;
   a.err = err_word;
   return from_cuda(pkv::launch_decode(a, as_stream(stream)));
@@ -292,12 +295,15 @@ pkv_status pkv_decode_plan(int32_t num_seqs, int32_t n_heads, const pkv_pool_des
 pkv_status pkv_paged_attention_decode_planned(
     const void* q, const void* k_new, const void* v_new, int32_t num_seqs, int32_t n_heads,
     void* k_pool, void* v_pool, const pkv_pool_desc* pool, const int32_t* block_tables,
-    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len, float scale,
-    int32_t max_ctas, void* out, void* workspace, size_t workspace_bytes, int32_t* err_word,
-    void* stream) {
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+    int32_t shared_prefix_blocks, float scale, int32_t max_ctas, void* out, void* workspace,
+    size_t workspace_bytes, int32_t* err_word, void* stream) {
+  // the new token may not be written into a block other sequences share
+  if (shared_prefix_blocks > 0 && (k_new != nullptr || v_new != nullptr)) return PKV_ERR_RANGE;
   return decode_entry(q, k_new, v_new, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
-                      max_blocks_per_seq, seq_lens, max_seq_len, 0, scale, max_ctas, out,
-                      workspace, workspace_bytes, err_word, stream, pkv::kPlanned);
+                      max_blocks_per_seq, seq_lens, max_seq_len, shared_prefix_blocks, scale,
+                      max_ctas, out, workspace, workspace_bytes, err_word, stream,
+                      pkv::kPlanned);
 }
 
 size_t pkv_prefill_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }

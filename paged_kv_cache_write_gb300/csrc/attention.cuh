@@ -1177,13 +1177,18 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_rows_kerne
 // end.  Consumer warp 0 also checks that each sequence's table starts with
 // row 0's blocks in this run.
 template <typename T, int HD, int MAXR, bool MMA>
-__global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_prefix_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(decode_max_threads<T, HD>())
+    decode_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   using Rows = typename RowsOf<T, HD, MAXR, MMA>::type;
   constexpr int R = MMA ? 16 : MAXR;  // rows one warp carries
   const int consumers = p.hg_size;
   const int row_bytes = p.hg_size * HD * p.elem_bytes;
-  Ring ring = make_ring(smem, p.nstages, row_bytes);
+  // tensor-core path: whole-block TMA tiles (as the main kernel); the maps
+  // are unused on the CUDA-core path
+  Ring ring = MMA ? make_tile_ring(smem, p.nstages, kBS * row_bytes)
+                  : make_ring(smem, p.nstages, row_bytes);
   ring_init(ring, consumers);
   pdl_wait();  // inputs written by the preceding kernel
   pdl_launch_dependents();
@@ -1212,7 +1217,17 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_prefix_ker
           valid = 0;
         }
         const int64_t off = int64_t(valid > 0 ? blk : 0) * kBS * token_pitch + head_off;
-        if (!ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err)) {
+        bool filled;
+        if constexpr (MMA) {  // a bad id reads the zeros past the pool's end
+          filled = lane == 0 ? tile_fill(ring, it, &tm_k, &tm_v,
+                                         valid > 0 ? blk * kBS : p.num_blocks * kBS,
+                                         g * p.hg_size, p.err)
+                             : true;
+          filled = __shfl_sync(0xffffffffu, filled, 0);
+        } else {
+          filled = ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err);
+        }
+        if (!filled) {
           *ring.abort_flag = 1;
           ok = false;
           break;
@@ -1252,8 +1267,12 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_prefix_ker
       return;
     }
     const int st = static_cast<int>(it % ring.nstages);
-    rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride,
-               (j0 + static_cast<int>(it)) * kBS, p.scale_log2);
+    if constexpr (MMA)
+      rows.block_sw(ring.k_tile(st), ring.v_tile(st), warp, (j0 + static_cast<int>(it)) * kBS,
+                    p.scale_log2);
+    else
+      rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride,
+                 (j0 + static_cast<int>(it)) * kBS, p.scale_log2);
     ring_release(ring, it);
   }
   const int64_t part = int64_t(kc) * p.B * p.n_heads;  // run kc's rows
@@ -1738,7 +1757,6 @@ struct DecodeLaunch {
     p.ws_o = reinterpret_cast<float*>(ws + L.o);
     p.pre_o = reinterpret_cast<float*>(ws + L.pre_o);
     p.pre_ml = reinterpret_cast<float*>(ws + L.pre_ml);
-    if (a.decode_plan != kPlanInCall && p.prefix_blocks > 0) return cudaErrorInvalidValue;
     if (a.decode_plan == kPlanOnly) {  // the plan alone, kept in the workspace
       p.plan_only = 1;
       p.out = nullptr;
@@ -1776,7 +1794,7 @@ struct DecodeLaunch {
       pcfg.stream = stream;
       pcfg.attrs = attr;
       pcfg.numAttrs = 1;
-      e = cudaLaunchKernelEx(&pcfg, decode_prefix_kernel<T, HD, MAXR, MMA>, p);
+      e = cudaLaunchKernelEx(&pcfg, decode_prefix_kernel<T, HD, MAXR, MMA>, tm_k, tm_v, p);
       if (e != cudaSuccess) return e;
       const int64_t threads = int64_t(p.B) * p.n_heads * (HD / 4);
       pcfg.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));

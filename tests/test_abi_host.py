@@ -191,11 +191,12 @@ def test_workspace_bytes_positive(pkv):
 
 
 def _plan(pkv, **over):
-    a = dict(B=2, H=8, desc=_desc(pkv), W=4, sl=FAKE, maxlen=64, max_ctas=0, ws=FAKE,
+    a = dict(B=2, H=8, desc=_desc(pkv), W=4, sl=FAKE, maxlen=64, P=0, max_ctas=0, ws=FAKE,
              wsb=1 << 40, err=None)
     a.update(over)
     return pkv.lib.pkv_decode_plan(a["B"], a["H"], ctypes.byref(a["desc"]), a["W"], a["sl"],
-                                   a["maxlen"], a["max_ctas"], a["ws"], a["wsb"], a["err"], None)
+                                   a["maxlen"], a["P"], a["max_ctas"], a["ws"], a["wsb"],
+                                   a["err"], None)
 
 
 def test_decode_plan_host_checks(pkv):
@@ -209,17 +210,20 @@ def test_decode_plan_host_checks(pkv):
     assert _plan(pkv, ws=FAKE + 8) == 4
     assert _plan(pkv, desc=_desc(pkv, head_dim=48)) == 7
     assert _plan(pkv, desc=_desc(pkv, dtype=9)) == 3
+    assert _plan(pkv, P=-1) == 5
+    assert _plan(pkv, P=5) == 5                        # more shared blocks than a table row has
     assert _plan(pkv, B=0, sl=None) == 0
 
 
 def _planned(pkv, **over):
     a = dict(q=FAKE, kn=None, vn=None, B=2, H=8, k=FAKE, v=FAKE, desc=_desc(pkv), bt=FAKE, W=4,
-             sl=FAKE, maxlen=64, scale=0.125, max_ctas=0, out=FAKE, ws=FAKE, wsb=1 << 40, err=None)
+             sl=FAKE, maxlen=64, P=0, scale=0.125, max_ctas=0, out=FAKE, ws=FAKE, wsb=1 << 40,
+             err=None)
     a.update(over)
     return pkv.lib.pkv_paged_attention_decode_planned(
         a["q"], a["kn"], a["vn"], a["B"], a["H"], a["k"], a["v"], ctypes.byref(a["desc"]), a["bt"],
-        a["W"], a["sl"], a["maxlen"], a["scale"], a["max_ctas"], a["out"], a["ws"], a["wsb"],
-        a["err"], None)
+        a["W"], a["sl"], a["maxlen"], a["P"], a["scale"], a["max_ctas"], a["out"], a["ws"],
+        a["wsb"], a["err"], None)
 
 
 def test_decode_planned_host_checks(pkv):
@@ -233,4 +237,6 @@ def test_decode_planned_host_checks(pkv):
     assert _planned(pkv, ws=None) == 6
     assert _planned(pkv, wsb=16) == 6
     assert _planned(pkv, desc=_desc(pkv, head_dim=48)) == 7
+    assert _planned(pkv, P=5) == 5
+    assert _planned(pkv, P=2, kn=FAKE, vn=FAKE) == 5   # no append into shared blocks
     assert _planned(pkv, B=0) == 0

@@ -123,3 +123,40 @@ def test_planned_empty_sequences_and_bad_length(shape):
     torch.cuda.synchronize()
     assert int(err.item()) & PKV_DEVERR_LENGTH
     assert not torch.isnan(out[:3].float()).any()  # rows before the bad one are untouched by it
+
+
+@pytest.mark.parametrize("name", ["smollm2-135m", "llama-3.2-1b-sharedprompt"])
+def test_planned_shared_prefix_bit_identical(name):
+    """With a shared prefix the planned call equals
+    pkv_paged_attention_decode_shared_prefix bit for bit, over two layers
+    sharing one plan, and matches the oracle."""
+    plan = draw_plan(name)
+    P = len(plan.shared_prefix_blocks)
+    assert P > 0
+    ws = None
+    for layer_id in range(2):
+        layer = make_layer(plan, layer_id)
+        g = GpuStep(plan, layer)
+        g.write(g.slots())
+        nd, t, sh = g.nd, g.t, g.sh
+        if ws is None:
+            ws = torch.zeros(pkv.decode_shared_prefix_workspace_bytes(nd, sh.n_heads, sh.head_dim,
+                                                                      g.max_dec, P),
+                             dtype=torch.uint8, device="cuda")
+            pkv.decode_plan(t["k_pool"], g.seq_lens[:nd], sh.n_heads, g.bt.shape[1], g.max_dec,
+                            workspace=ws, shared_prefix_blocks=P, err=g.err)
+        out = torch.full_like(t["q"][:nd], float("nan"))
+        pkv.paged_attention_decode_planned(t["q"][:nd], t["k_pool"], t["v_pool"], g.bt[:nd],
+                                           g.seq_lens[:nd], sh.scale, g.max_dec, workspace=ws,
+                                           shared_prefix_blocks=P, out=out, err=g.err)
+        ref = pkv.paged_attention_decode_shared_prefix(t["q"][:nd], t["k_pool"], t["v_pool"],
+                                                       g.bt[:nd], g.seq_lens[:nd], sh.scale, P,
+                                                       g.max_dec, err=g.err)
+        torch.cuda.synchronize()
+        assert int(g.err.item()) == 0
+        assert torch.equal(_bits(out), _bits(ref)), f"{name} layer {layer_id}"
+        if layer_id == 0:
+            o = OracleStep(plan, layer)
+            o.run_write()
+            rows = list(range(min(nd, 24)))
+            assert_close(f64(out)[rows], o.decode(rows=rows)[rows], plan.shape.dtype, name)
