@@ -7,9 +7,10 @@
 // its KV head, read in place through the block table.
 //
 // One CTA (one per SM) owns two 128-row tiles, A and B, of one (sequence,
-// KV head): each row is one (query, query head) pair, 128 / rep queries x
-// the rep query heads that share the KV head, so one K/V tile feeds every
-// head of the GQA group and both tiles.  Keys go in tiles of 128 (eight
+// KV head): each row is one (query, query head) pair, floor(128 / rep)
+// queries x the rep query heads that share the KV head (the last 128 mod
+// rep rows idle), so one K/V tile feeds every head of the GQA group and
+// both tiles.  Keys go in tiles of 128 (eight
 // 16-token blocks).
 //
 //  warp 8    TMA producer for Q_A and Q_B (once; 64-column halves, 128-byte
@@ -236,7 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty = is_k ? k_empty : v_empty;
     const CUtensorMap* map = is_k ? &tk : &tv;
     if (is_k && lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * Lay::Q_TILE);
+      // each Q tile holds q_per_tile queries x rep heads (all 128 rows when
+      // rep divides 128)
+      mbar_arrive_expect_tx(q_full, 2 * Lay::NH * (p.q_per_tile * p.rep) * 128);
       for (int x = 0; x < 2; ++x)
         for (int h = 0; h < Lay::NH; ++h)
           tc::tma_load_3d(q_tile(x) + h * Lay::Q_HALF, &tq, h * 64, g * p.rep,
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x - x * kRows;     // TMEM lane = row of the tile
     const int qi = i0 + x * p.q_per_tile + r / p.rep;
     const int hh = r - (r / p.rep) * p.rep;
-    const bool active = qi < c;
+    const bool active = r < p.q_per_tile * p.rep && qi < c;  // rows past the last full query are idle
     const int last = active ? L - c + qi : -1;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float m_used = -INFINITY, l_sum = 0.f;
@@ -545,7 +548,7 @@ bool prefill_tc_supported(const PoolShape& pool, int32_t n_heads) {
   if (pool.head_dim != 64 && pool.head_dim != 128) return false;
   if (pool.n_kv <= 0 || n_heads % pool.n_kv != 0) return false;
   const int rep = n_heads / pool.n_kv;
-  return rep == 1 || rep == 2 || rep == 4 || rep == 8 || rep == 16;
+  return rep >= 1 && rep <= 16;  // a tile holds 128 / rep queries of all rep heads
 }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {

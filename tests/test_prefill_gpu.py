@@ -53,7 +53,8 @@ def test_batched_full_prompt_prefill_sampled(name):
 
 
 SMALL = [(8, 4, 16, "f32"), (16, 2, 64, "f32"), (9, 3, 64, "bf16"), (32, 8, 64, "bf16"),
-         (64, 8, 128, "bf16"), (8, 8, 128, "bf16"), (16, 1, 64, "bf16"), (4, 2, 32, "bf16")]
+         (64, 8, 128, "bf16"), (8, 8, 128, "bf16"), (16, 1, 64, "bf16"), (4, 2, 32, "bf16"),
+         (15, 3, 128, "bf16"), (14, 2, 64, "bf16"), (12, 1, 128, "bf16")]
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=[f"{h}x{k}x{d}-{t}" for h, k, d, t in SMALL])
@@ -74,6 +75,34 @@ def test_prefill_small_ragged(shape):
         ref = np.stack([o.prefill_row(b, i) for i in range(chunk[b])])
         lo = int(plan.cu_new_lens[b])
         assert_close(got[lo:lo + chunk[b]], ref, dt, f"seq {b}")
+    assert int(g.err.item()) == 0
+
+
+GROUPS = [(9, 3, 64), (15, 3, 128), (12, 2, 64), (21, 3, 128), (13, 1, 64)]
+
+
+@pytest.mark.parametrize("shape", GROUPS, ids=[f"{h}x{k}x{d}" for h, k, d in GROUPS])
+def test_prefill_groups_not_dividing_the_tile(shape):
+    """Query heads per KV head that do not divide the 128-row tile (3, 5,
+    6, 7, 13): each tile holds floor(128 / rep) queries; chunks spanning
+    several tile pairs, with ragged ends, against the oracle on every
+    query."""
+    H, K, D = shape
+    hist = [0, 50, 300]
+    chunk = [200, 131, 90]
+    lens = [h + c for h, c in zip(hist, chunk)]
+    plan = tiny_plan(lens, chunk, n_heads=H, n_kv=K, head_dim=D, block_size=16, num_blocks=96,
+                     dtype="bf16", seed=H + D)
+    plan.n_decode = 0
+    layer = make_tiny_layer(plan, seed=H, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.run_write()
+    _, _, pre = g.run()
+    got = f64(pre)
+    for b in range(len(lens)):
+        ref = np.stack([o.prefill_row(b, i) for i in range(chunk[b])])
+        lo = int(plan.cu_new_lens[b])
+        assert_close(got[lo:lo + chunk[b]], ref, "bf16", f"seq {b}")
     assert int(g.err.item()) == 0
 
 
