@@ -727,7 +727,8 @@ def run_gb300(args, rank, world, local):
         pre_roof = {"bound": "tensor", "kernel": "paged_attention_prefill", "achieved": tf,
                     "peak": tc, "unit": "TFLOP/s", "frac": tf / tc,
                     "peak_source": f"bf16_tflops of {src}", "flops_per_launch": acc["prefill_flops"],
-                    "ms_per_launch": pre_ms}
+                    "ms_per_launch": pre_ms,
+                    "traffic": None, "traffic_note": "tensor-bound: DRAM bytes are not its limit"}
     cpu = None
     if not args.no_cpu_baseline and layers_cpu:
         # passes over layer 0 (every decode sequence, 64 prefill queries
