@@ -824,13 +824,18 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   for (int c = tid; c < p.grid; c += blockDim.x) {
     const int r0 = range_begin(c, U, p.grid);
     int4 st = make_int4(0, 0, 0, 0);
+    int4 sp = make_int4(-1, 0, 0, 0);
     if (r0 < range_begin(c + 1, U, p.grid)) {
       const int b = seq_of_unit(cu, p.B, r0);
       const int nblk = walked_blocks(p, used_len(p, b));
       const int grp = (r0 - cu[b]) / nblk;
       st = make_int4(b, grp, (r0 - cu[b]) - grp * nblk, 0);
+      sp = split_entry(c, p.grid, U, b, grp, st.z, nblk);
     }
     p.starts[c] = st;
+    // a plan kept for later calls also fixes which split group each merge
+    // CTA merges, so those calls' merge CTAs can read it before they wait
+    if (p.plan_only) p.splits[c] = sp;
   }
   if (p.plan_only) {  // kept for the calls that use the plan (empty sequences)
     if (in_smem)
@@ -1053,8 +1058,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
       cur.advance(p, n);
     }
     if (!ok) ring_drain(ring, it);
-    // the split group this CTA merges (read by the merge kernel)
-    if (lane == 0) {
+    // the split group this CTA merges (read by the merge kernel; a planned
+    // call's plan already holds it)
+    if (lane == 0 && !p.planned) {
       p.splits[blockIdx.x] = r0 < r1 ? split_entry(blockIdx.x, G, U, st.x, st.y, st.z,
                                                    walked_blocks(p, used_len(p, st.x)))
                                      : make_int4(-1, 0, 0, 0);
@@ -1510,8 +1516,16 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     fence_barrier_init();
   }
   pdl_launch_dependents();  // the next kernel's prologue may overlap this merge
-  pdl_wait();  // the main kernel's partials and split entries
-  const int4 sp = __ldcg(p.splits + blockIdx.x);
+  // the split group to merge: from the plan of a planned call (written by a
+  // finished plan launch, so read before the wait: a CTA with nothing to
+  // merge leaves at once), else written by the main kernel
+  int4 sp = make_int4(-1, 0, 0, 0);
+  if (p.planned) {
+    sp = __ldcg(p.splits + blockIdx.x);
+    if (sp.x < 0) return;
+  }
+  pdl_wait();  // the main kernel's partials (and split entries)
+  if (!p.planned) sp = __ldcg(p.splits + blockIdx.x);
   if (sp.x < 0) return;
   const int grp = sp.y & 0xffff;
   const bool c0_tail = (sp.y & kSplitC0Tail) != 0;
