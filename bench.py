@@ -620,12 +620,14 @@ def run_gb300(args, rank, world, local):
 
         def e2e_steps():
             # Step i uses buffer set i % 2.  Its copies in start once step i-2
-            # has finished computing from that set; its compute starts each
-            # layer's decode rows, then prefill rows, as soon as they have
-            # landed; each part's output goes back on a second stream once it
-            # is computed, and step i+2 overwrites those outputs only after
-            # that copy.  Every step copies all its inputs in and all its
-            # outputs out.
+            # has finished computing from that set, so they land while step
+            # i-1 computes and its compute waits for them once (one wait per
+            # step keeps the kernels of a step chained back to back); the
+            # first step of the graph instead starts each layer's decode rows,
+            # then prefill rows, as soon as they have landed.  Each part's
+            # output goes back on a second stream once it is computed, and
+            # step i+2 overwrites those outputs only after that copy.  Every
+            # step copies all its inputs in and all its outputs out.
             main = torch.cuda.current_stream(dev)
             h2d_s.wait_stream(main)
             d2h_s.wait_stream(main)
@@ -649,7 +651,7 @@ def run_gb300(args, rank, world, local):
                 if i >= 2:
                     main.wait_event(copied_out[i - 2])
                 inputs = (dev_in[b][0], dev_in[b][1], dev_in[b][2], dev_layers[b])
-                main.wait_event(ev_d[0])  # the tables came first
+                main.wait_event(ev_d[0] if i == 0 else ev_p[-1])  # tables first / everything
                 step_head(inputs)
                 for li in range(len(L)):
                     for run, outs, evs, off, on in ((layer_decode, dev_dec[b], ev_d, 0, nd > 0),
@@ -657,7 +659,8 @@ def run_gb300(args, rank, world, local):
                                                      has_pre)):
                         if not on:
                             continue
-                        main.wait_event(evs[li])
+                        if i == 0:
+                            main.wait_event(evs[li])
                         run(li, inputs, outs=outs)
                         e = torch.cuda.Event()
                         e.record(main)
@@ -688,8 +691,8 @@ def run_gb300(args, rank, world, local):
                "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "copies": f"every step copies all its inputs in and all its outputs out; inputs "
                          f"and outputs double-buffered so a step's copies (one stream in, one "
-                         f"out, per layer and part as soon as possible) overlap its neighbours' "
-                         f"compute; timed over {e_reps} x {steps_per_graph} steps"}
+                         f"out, each layer's outputs as soon as computed) overlap its "
+                         f"neighbours' compute; timed over {e_reps} x {steps_per_graph} steps"}
 
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} in the timed region")
