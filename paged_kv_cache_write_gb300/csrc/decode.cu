@@ -13,8 +13,6 @@ bool decode_supported(const PoolShape& pool, int32_t n_heads) {
   return pool.dtype == PKV_F32 && simt_head_dim(pool.head_dim);
 }
 
-int32_t decode_default_partition(int32_t, int32_t, int32_t, int32_t) { return 0; }
-
 // Upper bound of the decode workspace over every grid this device can run.
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim, int32_t, int32_t,
                               int32_t shared_prefix_blocks) {

@@ -69,10 +69,8 @@ enum : int32_t { kPlanInCall = 0, kPlanOnly = 1, kPlanned = 2 };
 
 // Decode support / sizing.
 bool decode_supported(const PoolShape& pool, int32_t n_heads);
-int32_t decode_default_partition(int32_t num_seqs, int32_t n_kv, int32_t max_seq_len,
-                                 int32_t block_size);
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim,
-                              int32_t max_seq_len, int32_t partition_tokens,
+                              int32_t max_seq_len, int32_t max_ctas,
                               int32_t shared_prefix_blocks);
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream);
 // Workspace the decode launch for `a` needs on the current device (0 on error).
