@@ -11,9 +11,9 @@ from workloads import draw_plan, make_layer, tiny_plan, make_tiny_layer
 
 pytestmark = pytest.mark.gpu
 
-# (shape, layers checked).  All layers of the toy and SmolLM2 steps; three
-# layers of Llama-3.2-1B; first and last layer of LLaMA-7B; the one 70B layer.
-CASES = [("toy", [0]), ("smollm2-135m", list(range(30))), ("llama-3.2-1b", [0, 7, 15]),
+# (shape, layers checked).  All layers of the toy, SmolLM2 and Llama-3.2-1B
+# steps; first and last layer of LLaMA-7B; the one 70B layer.
+CASES = [("toy", [0]), ("smollm2-135m", list(range(30))), ("llama-3.2-1b", list(range(16))),
          ("llama-7b", [0, 31]), ("llama2-70b-mixed", [0]), ("llama2-70b-decode64", [0])]
 
 
