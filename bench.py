@@ -81,8 +81,9 @@ def parse_args(argv=None):
                     help="write every new token with kv_write, then run plain decode "
                          "(instead of the fused decode-with-append launch)")
     ap.add_argument("--shared-prefix", action="store_true",
-                    help="decode with the shared-prefix entry point (the workload's common "
-                         "prompt blocks read once per step); the K/V write is then separate")
+                    help="decode with the shared-prefix path (the workload's common prompt "
+                         "blocks read once per step); the K/V write is fused only when the "
+                         "step's work split is planned once (several layers, no --no-plan)")
     ap.add_argument("--no-plan", action="store_true",
                     help="let every decode call split its work itself instead of planning the "
                          "split once per step for all layers")
@@ -404,7 +405,9 @@ def run_gb300(args, rank, world, local):
 
     ev_dec, ev_pre = [], []
 
-    fused = not args.separate_write and P == 0
+    # the step's decode K/V write rides in the decode launch (with a shared
+    # prefix, only in the once-per-step planned call)
+    fused = not args.separate_write and (P == 0 or (not args.no_plan and len(L) > 1))
     # the decode rows' work split, planned once per step for all its layers
     # (a one-layer step plans inside its call: a separate plan would not be
     # shared by anything)
@@ -770,7 +773,7 @@ def run_gb300(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if sh.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; workloads/)",
         "config": workload_config(plan, n_layers, "cuda_graph" if use_graph else "eager"),
-        "decode_write": ("fused into the decode launch (decode_append)" if fused
+        "decode_write": ("fused into the decode launch" if fused
                          else "separate kv_write launch"),
         "decode_shared_prefix_blocks": P,
         "decode_plan": ("once per step for all timed layers (decode_plan + decode_planned)"

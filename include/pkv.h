@@ -333,9 +333,10 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * of pkv_paged_attention_decode (k_new and v_new both NULL) or
  * pkv_paged_attention_decode_append (both given), bit for bit; with
  * shared_prefix_blocks > 0 they are those of
- * pkv_paged_attention_decode_shared_prefix (the prefix runs and their
- * combine are launched by each planned call; the plan covers the blocks
- * after the prefix), bit for bit.
+ * pkv_paged_attention_decode_shared_prefix (preceded, when k_new and v_new
+ * are given, by pkv_kv_write of each sequence's new token at its last
+ * slot; the prefix runs and their combine are launched by each planned
+ * call; the plan covers the blocks after the prefix), bit for bit.
  *
  * Contract: the planned calls pass the same num_seqs, n_heads, pool shape,
  * max_blocks_per_seq, seq_lens (pointer and contents), max_seq_len and
@@ -346,9 +347,11 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * plan reports bad lengths (PKV_DEVERR_LENGTH / _TABLE_WIDTH) once.
  *
  *   shared_prefix_blocks  as for pkv_paged_attention_decode_shared_prefix
- *              (0 = none; the same value for the plan and its calls); with
- *              a shared prefix k_new and v_new must be NULL (else
- *              PKV_ERR_RANGE)
+ *              (0 = none; the same value for the plan and its calls).  With
+ *              a shared prefix and k_new / v_new, every sequence's new
+ *              token must fall after the prefix (a private block); a
+ *              sequence wholly inside the prefix gets no write and is
+ *              reported as PKV_DEVERR_PREFIX
  *   workspace  at least pkv_decode_workspace_bytes(...) bytes (with a
  *              shared prefix, pkv_decode_shared_prefix_workspace_bytes),
  *              16-byte aligned (the same workspace for the plan and its

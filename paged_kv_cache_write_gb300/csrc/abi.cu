@@ -298,8 +298,6 @@ pkv_status pkv_paged_attention_decode_planned(
     int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
     int32_t shared_prefix_blocks, float scale, int32_t max_ctas, void* out, void* workspace,
     size_t workspace_bytes, int32_t* err_word, void* stream) {
-  // the new token may not be written into a block other sequences share
-  if (shared_prefix_blocks > 0 && (k_new != nullptr || v_new != nullptr)) return PKV_ERR_RANGE;
   return decode_entry(q, k_new, v_new, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
                       max_blocks_per_seq, seq_lens, max_seq_len, shared_prefix_blocks, scale,
                       max_ctas, out, workspace, workspace_bytes, err_word, stream,

@@ -1332,6 +1332,10 @@ __global__ void __launch_bounds__(256) decode_prefix_combine_kernel(DecodeParams
   const float inv = den > 0.f ? 1.f / den : 0.f;
   const int b = static_cast<int>(row / p.n_heads);
   if (used_len(p, b) <= p.prefix_blocks * kBS) {
+    // with append, this sequence's new token would belong in a shared block
+    // (other sequences read it): not written, reported
+    if (p.k_new != nullptr && used_len(p, b) > 0 && i % (int64_t(p.n_heads) * V) == 0)
+      report(p.err, PKV_DEVERR_PREFIX);
     T* out = static_cast<T*>(p.out) + row * HD + e;
     out[0] = Elem<T>::from_f(acc.x * inv);
     out[1] = Elem<T>::from_f(acc.y * inv);

@@ -238,5 +238,4 @@ def test_decode_planned_host_checks(pkv):
     assert _planned(pkv, wsb=16) == 6
     assert _planned(pkv, desc=_desc(pkv, head_dim=48)) == 7
     assert _planned(pkv, P=5) == 5
-    assert _planned(pkv, P=2, kn=FAKE, vn=FAKE) == 5   # no append into shared blocks
     assert _planned(pkv, B=0) == 0

@@ -160,3 +160,33 @@ def test_planned_shared_prefix_bit_identical(name):
             o.run_write()
             rows = list(range(min(nd, 24)))
             assert_close(f64(out)[rows], o.decode(rows=rows)[rows], plan.shape.dtype, name)
+
+
+def test_planned_shared_prefix_append_bit_identical():
+    """Shared prefix with the step's K/V write fused (each new token lands
+    after the prefix): outputs and pools bit-identical to pkv_kv_write at
+    the new slots followed by the planned shared-prefix call."""
+    plan = draw_plan("llama-3.2-1b-sharedprompt")
+    P = len(plan.shared_prefix_blocks)
+    layer = make_layer(plan, 0)
+    g = GpuStep(plan, layer)
+    nd, t, sh = g.nd, g.t, g.sh
+    k_new, v_new = t["k"][:nd].contiguous(), t["v"][:nd].contiguous()
+    kp1, vp1 = t["k_pool"].clone(), t["v_pool"].clone()
+    kp2, vp2 = t["k_pool"].clone(), t["v_pool"].clone()
+    ws = torch.zeros(pkv.decode_shared_prefix_workspace_bytes(nd, sh.n_heads, sh.head_dim,
+                                                              g.max_dec, P),
+                     dtype=torch.uint8, device="cuda")
+    pkv.decode_plan(t["k_pool"], g.seq_lens[:nd], sh.n_heads, g.bt.shape[1], g.max_dec,
+                    workspace=ws, shared_prefix_blocks=P, err=g.err)
+    pkv.kv_write(k_new, v_new, g.slots()[:nd], kp1, vp1, err=g.err)
+    ref = pkv.paged_attention_decode_planned(t["q"][:nd], kp1, vp1, g.bt[:nd], g.seq_lens[:nd],
+                                             sh.scale, g.max_dec, workspace=ws,
+                                             shared_prefix_blocks=P, err=g.err)
+    out = pkv.paged_attention_decode_planned(t["q"][:nd], kp2, vp2, g.bt[:nd], g.seq_lens[:nd],
+                                             sh.scale, g.max_dec, workspace=ws, k_new=k_new,
+                                             v_new=v_new, shared_prefix_blocks=P, err=g.err)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert torch.equal(_bits(out), _bits(ref))
+    assert torch.equal(_bits(kp2), _bits(kp1)) and torch.equal(_bits(vp2), _bits(vp1))
