@@ -210,3 +210,53 @@ def test_workspace_reused_across_calls_and_grids(name, dt):
             assert int(g.err.item()) == 0
             assert_close(f64(out)[rows], ref[rows], dt, f"{name} max_ctas={max_ctas}")
             assert not torch.isnan(out.float()).any()
+
+
+@pytest.mark.parametrize("B", [3000, 9000])
+@pytest.mark.parametrize("shape", [(8, 2, 64, "bf16"), (8, 2, 16, "f32")], ids=["bf16", "f32"])
+def test_decode_large_batches(B, shape):
+    """Batches past the kernel's own plan (2,048 sequences: a plan launch
+    splits the work) and past the plan's shared-memory prefix (8,191: the
+    prefix lives in the workspace), with empty and one-token sequences:
+    plain, planned and append calls agree with the oracle on sampled rows."""
+    H, K, D, dt = shape
+    rng = np.random.default_rng(B)
+    lens = rng.integers(0, 60, size=B)
+    lens[::97] = 0
+    lens[1::89] = 1
+    plan = tiny_plan(lens.tolist(), [1] * B, n_heads=H, n_kv=K, head_dim=D, block_size=16,
+                     num_blocks=int(sum((l + 15) // 16 for l in lens)) + 8, dtype=dt, seed=B)
+    layer = make_tiny_layer(plan, seed=B, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.kp, o.vp = o.raw["k_pool"], o.raw["v_pool"]
+    rows = sorted(set(rng.choice(B, 40, replace=False).tolist()) | {0, 1, B - 1})
+    ref = o.decode(rows=rows)
+    t, sh, nd = g.t, g.sh, g.nd
+    plain = g.decode()
+    ws = torch.zeros(g.pkv.decode_workspace_bytes(nd, H, D, g.max_dec), dtype=torch.uint8,
+                     device="cuda")
+    g.pkv.decode_plan(t["k_pool"], g.seq_lens, H, g.bt.shape[1], g.max_dec, workspace=ws,
+                      err=g.err)
+    planned = g.pkv.paged_attention_decode_planned(t["q"], t["k_pool"], t["v_pool"], g.bt,
+                                                   g.seq_lens, sh.scale, g.max_dec, workspace=ws,
+                                                   err=g.err)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert_close(f64(plain)[rows], ref[rows], dt, f"B={B} plain")
+    assert torch.equal(plain.view(torch.int16 if dt == "bf16" else torch.int32),
+                       planned.view(torch.int16 if dt == "bf16" else torch.int32))
+    for b in np.nonzero(lens == 0)[0][:5]:
+        assert torch.count_nonzero(plain[int(b)].float()) == 0
+    # append: the step's K/V fused in (sequences of length 0 write nothing),
+    # against the oracle after the same write
+    sel = [b for b in range(B) if lens[b] > 0]
+    slots = np.array([oracle.slot_of(plan.block_tables[b], int(lens[b]) - 1, 16) for b in sel])
+    o.kp, o.vp = oracle.kv_write(o.raw["k"][sel], o.raw["v"][sel], slots, o.raw["k_pool"],
+                                 o.raw["v_pool"])
+    ref_a = o.decode(rows=rows)
+    kp, vp = t["k_pool"].clone(), t["v_pool"].clone()
+    app = g.pkv.paged_attention_decode_append(t["q"], t["k"], t["v"], kp, vp, g.bt, g.seq_lens,
+                                              sh.scale, g.max_dec, err=g.err)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert_close(f64(app)[rows], ref_a[rows], dt, f"B={B} append")
