@@ -120,3 +120,33 @@ def test_prefill_chunk_of_one_equals_decode():
                                             g.seq_lens, plan.shape.scale, 1, max(lens))
         torch.cuda.synchronize()
         assert_close(f64(pre), f64(dec), dt, "prefill(c=1) vs decode")
+
+
+@pytest.mark.parametrize("shape", [(32, 8, 64), (9, 3, 128)], ids=["32x8x64", "9x3x128"])
+def test_prefill_many_sequences_natural_grid(shape):
+    """More sequences than the tcgen05 kernel ranks by work (352): the grid
+    falls back to (pair, KV head, sequence) order.  400 chunks of 1..70
+    queries over 0..150 tokens of history; sampled queries of every chunk
+    against the oracle."""
+    H, K, D = shape
+    rng = np.random.default_rng(H + D)
+    B = 400
+    chunk = rng.integers(1, 71, size=B)
+    hist = rng.integers(0, 151, size=B)
+    lens = (hist + chunk).tolist()
+    plan = tiny_plan(lens, chunk.tolist(), n_heads=H, n_kv=K, head_dim=D, block_size=16,
+                     num_blocks=int(sum((l + 15) // 16 for l in lens)) + 8, dtype="bf16",
+                     seed=H + D)
+    plan.n_decode = 0
+    layer = make_tiny_layer(plan, seed=D, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.run_write()
+    _, _, pre = g.run()
+    got = f64(pre)
+    for b in range(0, B, 7):
+        c = int(chunk[b])
+        lo = int(plan.cu_new_lens[b])
+        qs = sorted({0, c - 1, c // 2})
+        ref = np.stack([o.prefill_row(b, i) for i in qs])
+        assert_close(got[[lo + i for i in qs]], ref, "bf16", f"seq {b}")
+    assert int(g.err.item()) == 0
