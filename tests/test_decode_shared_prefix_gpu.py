@@ -47,10 +47,10 @@ def test_shared_prefix_workloads(name, layer_id):
     assert_close(f64(shared), f64(plain), "bf16", "vs plain decode")
 
 
-def _plan_with_prefix(lens, P, H, K, D, dt, seed):
+def _plan_with_prefix(lens, P, H, K, D, dt, seed, num_blocks=160):
     shared = tuple(range(1, 1 + P))
     plan = tiny_plan(lens, [1] * len(lens), n_heads=H, n_kv=K, head_dim=D, block_size=16,
-                     num_blocks=160, dtype=dt, seed=seed, shared=shared)
+                     num_blocks=num_blocks, dtype=dt, seed=seed, shared=shared)
     bt = plan.block_tables.copy()
     if bt.shape[1] < P:
         bt = np.concatenate([bt, np.zeros((bt.shape[0], P - bt.shape[1]), bt.dtype)], axis=1)
@@ -105,3 +105,23 @@ def test_shared_prefix_mismatch_reported():
     _prefix_decode(g, 2)
     torch.cuda.synchronize()
     assert int(g.err.item()) & PKV_DEVERR_PREFIX
+
+
+def test_shared_prefix_large_batch():
+    """3,000 sequences behind a 3-block prompt (the main kernel's work split
+    then comes from a plan launch), lengths inside, at and past the prefix:
+    sampled rows against the oracle."""
+    rng = np.random.default_rng(3)
+    B, P = 3000, 3
+    lens = rng.integers(0, 100, size=B).tolist()
+    plan = _plan_with_prefix(lens, P, 32, 8, 64, "bf16", seed=4,
+                             num_blocks=sum((l + 15) // 16 for l in lens) + 8)
+    layer = make_tiny_layer(plan, seed=4)
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.kp, o.vp = o.raw["k_pool"], o.raw["v_pool"]
+    rows = sorted(set(rng.choice(B, 40, replace=False).tolist()) | {0, B - 1})
+    ref = o.decode(rows=rows)
+    out = _prefix_decode(g, P)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert_close(f64(out)[rows], ref[rows], "bf16", "B=3000")
