@@ -92,6 +92,7 @@ typedef enum pkv_dtype {
 #define PKV_DEVERR_LENGTH      8  /* a length < 0, > max_seq_len, or < its chunk      */
 #define PKV_DEVERR_TIMEOUT    16  /* a pipeline wait gave up (kernel returned early) */
 #define PKV_DEVERR_PREFIX     32  /* a table does not start with the declared shared prefix */
+#define PKV_DEVERR_PLAN       64  /* a planned call whose plan was made for other sizes     */
 
 /* Shape of one layer's K pool (the V pool has the same shape). */
 typedef struct pkv_pool_desc {
@@ -344,7 +345,11 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * of the workspace stay unchanged from the plan call to the last planned
  * call (the decode writes only the partial-result part of the workspace,
  * so one workspace serves a whole step's layers in stream order).  The
- * plan reports bad lengths (PKV_DEVERR_LENGTH / _TABLE_WIDTH) once.
+ * plan reports bad lengths (PKV_DEVERR_LENGTH / _TABLE_WIDTH) once.  A
+ * planned call whose batch, shared prefix or grid (max_ctas, device)
+ * differs from its plan's computes nothing and reports PKV_DEVERR_PLAN;
+ * so does one whose workspace was never planned or was last used by a call
+ * that plans for itself (pkv_paged_attention_decode and the like).
  *
  *   shared_prefix_blocks  as for pkv_paged_attention_decode_shared_prefix
  *              (0 = none; the same value for the plan and its calls).  With

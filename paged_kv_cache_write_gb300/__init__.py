@@ -33,7 +33,8 @@ library_path = os.path.join(HERE, "libpkv.so")
 
 PKV_F32 = 0
 PKV_BF16 = 1
-DEVERR = {"block_id": 1, "slot": 2, "table_width": 4, "length": 8, "timeout": 16, "prefix": 32}
+DEVERR = {"block_id": 1, "slot": 2, "table_width": 4, "length": 8, "timeout": 16, "prefix": 32,
+          "plan": 64}
 
 
 class PoolDesc(ctypes.Structure):

@@ -719,6 +719,13 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // Wait until the preceding kernel has finished and its writes are visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// A plan kept in the workspace (by a plan-only launch) was made for this
+// grid, batch and shared prefix.
+__device__ __forceinline__ bool plan_matches(const DecodeParams& p, int G) {
+  return __ldcg(p.total_units + 1) == G && __ldcg(p.total_units + 2) == p.B &&
+         __ldcg(p.total_units + 3) == p.prefix_blocks;
+}
+
 // Plan for batches too large for the main kernel's own scan: one CTA
 // computes the exclusive scan of units per sequence, each CTA's first
 // segment and the batch total, zeroes outputs of empty sequences and
@@ -818,6 +825,13 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   if (tid == blockDim.x - 1) {
     cu[p.B] = run;
     *p.total_units = run;
+    if (p.plan_only) {  // what the plan was made for, checked by the calls using it
+      p.total_units[1] = p.grid;
+      p.total_units[2] = p.B;
+      p.total_units[3] = p.prefix_blocks;
+    } else {
+      p.total_units[1] = -1;  // a call planning for itself replaces any kept plan
+    }
   }
   __syncthreads();  // the prefix is complete (same CTA: visible after the barrier)
   const int U = cu[p.B];
@@ -964,11 +978,18 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
     }
     if (p.prefix_blocks == 0)  // with a prefix, the prefix kernel writes them
       zero_empty<T, HD>(p, blockIdx.x, G, [&](int b) { return cu_s[b + 1] == cu_s[b]; });
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.total_units = U;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      p.total_units[0] = U;
+      p.total_units[1] = -1;  // a call planning for itself replaces any kept plan
+    }
     fence_proxy_async_smem();  // the scan's stores come before the ring's copies
     __syncthreads();
   } else {
     U = __ldcg(p.total_units);
+    if (p.planned && !plan_matches(p, G)) {  // nothing of the stale plan is used
+      if (blockIdx.x == 0 && threadIdx.x == 0) report(p.err, PKV_DEVERR_PLAN);
+      return;
+    }
     st = __ldcg(p.starts + blockIdx.x);
   }
   const int r0 = range_begin(blockIdx.x, U, G);
@@ -1525,6 +1546,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   // merge leaves at once), else written by the main kernel
   int4 sp = make_int4(-1, 0, 0, 0);
   if (p.planned) {
+    if (!plan_matches(p, p.grid)) return;  // reported by the main kernel
     sp = __ldcg(p.splits + blockIdx.x);
     if (sp.x < 0) return;
   }

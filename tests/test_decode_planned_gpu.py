@@ -190,3 +190,47 @@ def test_planned_shared_prefix_append_bit_identical():
     assert int(g.err.item()) == 0
     assert torch.equal(_bits(out), _bits(ref))
     assert torch.equal(_bits(kp2), _bits(kp1)) and torch.equal(_bits(vp2), _bits(vp1))
+
+
+PKV_DEVERR_PLAN = 64
+
+
+@pytest.mark.parametrize("case", ["grid", "batch", "unplanned", "replaced"])
+def test_planned_call_rejects_a_plan_for_other_sizes(case):
+    """A planned call whose plan was made for another grid or batch, or
+    whose workspace was never planned or was last used by a call planning
+    for itself, computes nothing and reports the plan error; the same
+    workspace planned again then gives the right result."""
+    plan = draw_plan("smollm2-135m")
+    layer = make_layer(plan, 0)
+    g = GpuStep(plan, layer)
+    g.write(g.slots())
+    nd, t = g.nd, g.t
+    ws = _workspace(g, 0)  # large enough for either grid
+    if case == "grid":
+        _plan(g, ws, max_ctas=7)
+    elif case == "batch":
+        pkv.decode_plan(t["k_pool"], g.seq_lens[:nd - 1], g.sh.n_heads, g.bt.shape[1], g.max_dec,
+                        workspace=ws, err=g.err)
+    elif case == "replaced":
+        _plan(g, ws)
+        pkv.paged_attention_decode(t["q"][:nd], t["k_pool"], t["v_pool"], g.bt[:nd], g.seq_lens[:nd],
+                                   g.sh.scale, g.max_dec, workspace=ws, err=g.err)
+    out = torch.full_like(t["q"][:nd], float("nan"))
+
+    def call():
+        pkv.paged_attention_decode_planned(t["q"][:nd], t["k_pool"], t["v_pool"], g.bt[:nd],
+                                           g.seq_lens[:nd], g.sh.scale, g.max_dec, workspace=ws,
+                                           out=out, err=g.err)
+
+    call()
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == PKV_DEVERR_PLAN
+    assert torch.isnan(out).all()
+    g.err.zero_()
+    _plan(g, ws)
+    call()
+    ref = g.decode()
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert torch.equal(_bits(out), _bits(ref))
