@@ -1488,17 +1488,6 @@ __global__ void __launch_bounds__(288) prefill_kernel(PrefillParams p) {
 
 // ------------------------------------------------------------ host side
 
-inline int sm_count() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-  }
-  return sms;
-}
-
 inline bool use_mma(const PoolShape& pool) { return pool.dtype == PKV_BF16 && (pool.head_dim == 64 || pool.head_dim == 128); }
 
 // Heads per CTA for decode: the largest divisor of n_kv, at most 8, whose

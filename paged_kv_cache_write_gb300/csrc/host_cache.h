@@ -48,4 +48,16 @@ cudaError_t kernel_setup(KernelSetup& ks, Kern kern, int smem, int threads, int*
   return cudaSuccess;
 }
 
+// SMs of the current device (looked up once per process).
+inline int sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  return sms;
+}
+
 }  // namespace pkv
