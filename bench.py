@@ -56,7 +56,7 @@ WORKLOAD_LABEL = "llama2-70b-gqa8-mixed-decode256-prefill4x512"
 # llama-3.2-1b workload; keyed by (dtype, n_heads, n_kv, head_dim).  Valid
 # only for the decode kernel as it was captured: drop the entries when the
 # kernel changes and capture again.
-DECODE_DRAM_PER_KV_BYTE = {("bf16", 64, 8, 128): 1.01778, ("bf16", 32, 8, 64): 1.02860}
+DECODE_DRAM_PER_KV_BYTE = {("bf16", 64, 8, 128): 1.01791, ("bf16", 32, 8, 64): 1.02860}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit -> name
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
