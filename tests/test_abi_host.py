@@ -38,6 +38,17 @@ def test_library_exports_every_declared_symbol(pkv):
     assert not missing, missing
 
 
+def test_device_error_bits_match_the_header(pkv):
+    """The binding's names for the device error bits are the header's
+    PKV_DEVERR_* values, one bit each."""
+    text = open(HEADER).read()
+    bits = {m.group(1).lower(): int(m.group(2))
+            for m in re.finditer(r"#define PKV_DEVERR_([A-Z_]+)\s+(\d+)", text)}
+    assert bits == pkv.DEVERR
+    assert all(v & (v - 1) == 0 for v in bits.values())
+    assert len(set(bits.values())) == len(bits)
+
+
 def test_status_strings(pkv):
     assert pkv.status_string(0) == "ok"
     for s in range(1, 9):
