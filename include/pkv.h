@@ -347,9 +347,12 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * so one workspace serves a whole step's layers in stream order).  The
  * plan reports bad lengths (PKV_DEVERR_LENGTH / _TABLE_WIDTH) once.  A
  * planned call whose batch, shared prefix or grid (max_ctas, device)
- * differs from its plan's computes nothing and reports PKV_DEVERR_PLAN;
- * so does one whose workspace was never planned or was last used by a call
- * that plans for itself (pkv_paged_attention_decode and the like).
+ * differs from its plan's reports PKV_DEVERR_PLAN, stores no k_new / v_new
+ * row and writes no output that depends on the plan (with a shared prefix,
+ * the rows of sequences that end inside the prefix, which the plan does
+ * not cover, are still written); so does one whose workspace was never
+ * planned or was last used by a call that plans for itself
+ * (pkv_paged_attention_decode and the like).
  *
  *   shared_prefix_blocks  as for pkv_paged_attention_decode_shared_prefix
  *              (0 = none; the same value for the plan and its calls).  With
