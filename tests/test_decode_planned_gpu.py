@@ -234,3 +234,38 @@ def test_planned_call_rejects_a_plan_for_other_sizes(case):
     torch.cuda.synchronize()
     assert int(g.err.item()) == 0
     assert torch.equal(_bits(out), _bits(ref))
+
+
+def test_stale_plan_stores_nothing():
+    """With k_new / v_new and a plan made for another grid, or with a
+    shared prefix the plan was not made for, the planned call reports the
+    plan error, leaves both pools untouched and writes no output row (every
+    sequence here runs past the 1,024-token prefix)."""
+    plan = draw_plan("llama-3.2-1b-sharedprompt")
+    P = len(plan.shared_prefix_blocks)
+    layer = make_layer(plan, 0)
+    g = GpuStep(plan, layer)
+    nd, t, sh = g.nd, g.t, g.sh
+    assert int(plan.seq_lens[:nd].min()) > P * sh.block_size
+    k_new, v_new = t["k"][:nd].contiguous(), t["v"][:nd].contiguous()
+    kp0, vp0 = t["k_pool"].clone(), t["v_pool"].clone()
+    ws = torch.zeros(pkv.decode_shared_prefix_workspace_bytes(nd, sh.n_heads, sh.head_dim,
+                                                              g.max_dec, P),
+                     dtype=torch.uint8, device="cuda")
+    for plan_ctas, plan_prefix in ((7, P), (0, 0)):
+        pkv.decode_plan(t["k_pool"], g.seq_lens[:nd], sh.n_heads, g.bt.shape[1], g.max_dec,
+                        workspace=ws, shared_prefix_blocks=plan_prefix, max_ctas=plan_ctas,
+                        err=g.err)
+        torch.cuda.synchronize()
+        assert int(g.err.item()) == 0
+        out = torch.full_like(t["q"][:nd], float("nan"))
+        pkv.paged_attention_decode_planned(t["q"][:nd], t["k_pool"], t["v_pool"], g.bt[:nd],
+                                           g.seq_lens[:nd], sh.scale, g.max_dec, workspace=ws,
+                                           k_new=k_new, v_new=v_new, shared_prefix_blocks=P,
+                                           out=out, err=g.err)
+        torch.cuda.synchronize()
+        assert int(g.err.item()) == PKV_DEVERR_PLAN, (plan_ctas, plan_prefix)
+        assert torch.isnan(out).all()
+        assert torch.equal(_bits(t["k_pool"]), _bits(kp0))
+        assert torch.equal(_bits(t["v_pool"]), _bits(vp0))
+        g.err.zero_()
