@@ -10,6 +10,15 @@
  *   pkv_paged_attention_prefill   a causal query chunk over paged history
  *   pkv_kv_gather                 block table -> contiguous K/V (test/debug)
  *
+ * and, around those: pkv_paged_attention_decode_append (the step's K/V
+ * stored and attended in one launch), pkv_paged_attention_decode_shared_prefix
+ * (a common prompt prefix read once per step), pkv_decode_plan +
+ * pkv_paged_attention_decode_planned (the decode work split made once per
+ * step for every layer), pkv_copy_blocks (copy-on-write),
+ * pkv_paged_attention_decode_noalloc (decode without a caller workspace),
+ * the workspace size queries, pkv_status_string, pkv_abi_version and
+ * pkv_selftest_bounded_wait (the kernels' bounded-wait failure path).
+ *
  * Sources of the operations (page title, section):
  *   - "Build a Mini vLLM: Paged KV Cache and Continuous Batching From
  *     Scratch", section 2 (KVPool, BlockManager.append_slot), section 3
