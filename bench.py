@@ -332,8 +332,8 @@ def run_reference(args, rank, world):
         total_s += s
         total_b += b
     gbs = total_b / total_s / 1e9
-    sample = (f"per step: {n_dec} decode sequences (rotating) and {n_pre} prefill queries of one "
-              f"layer of the {WORKLOAD_LABEL} step, float64 numpy oracle")
+    sample = (f"per step: {nr} decode sequences (rotating) and {npq} prefill queries of one "
+              f"layer of the {workload_config(plan)['workload']} step, float64 numpy oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,

@@ -21,3 +21,30 @@ def test_pages_method_matches_oracle(name):
                                         plan.seq_lens[:nd], plan.shape.scale, plan.shape.dtype)
     got = np.stack([o.double().numpy() for o in outs])
     assert np.max(np.abs(got - ref)) < 1e-5
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the float64 oracle on the host cores)
+    prints one JSON line with the contract's keys, its own e2e with no
+    copies, and a cpu_baseline describing the sample it timed."""
+    import json
+    import subprocess
+    import sys
+    root = __import__("os").path.dirname(__import__("os").path.dirname(__file__))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                        "smollm2-135m", "--steps", "2", "--warmup", "1"], cwd=root,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 2
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert "smollm2-135m" in cb["sample"] and "0 prefill queries" in cb["sample"]
+    assert d["config"]["workload"] == "smollm2-135m"
