@@ -95,9 +95,14 @@ def main(argv=None):
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true", help="print registers / spills per kernel")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="push an NVTX range in every entry point (for profiler timelines)")
     a = ap.parse_args(argv)
     extra = ["-Xptxas", "-v"] if a.ptxas_info else []
-    path = build(force=a.force or a.ptxas_info, verbose=a.verbose or a.ptxas_info, extra_flags=extra)
+    if a.nvtx:
+        extra.append("-DPKV_NVTX")
+    path = build(force=a.force or a.ptxas_info or a.nvtx, verbose=a.verbose or a.ptxas_info,
+                 extra_flags=extra)
     print(path)
 
 

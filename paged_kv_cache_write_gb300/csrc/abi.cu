@@ -4,53 +4,19 @@
 #include <stdint.h>
 
 #include "../../include/pkv.h"
+#include "checks.h"
 #include "launch.h"
+#include "nvtx.h"
 
 namespace {
 
 using pkv::PoolShape;
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-pkv_status check_pool(const pkv_pool_desc* pool, PoolShape* out) {
-  if (pool == nullptr) return PKV_ERR_NULL;
-  if (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16) return PKV_ERR_DTYPE;
-  if (pool->num_blocks <= 0 || pool->block_size <= 0 || pool->n_kv <= 0 || pool->head_dim <= 0)
-    return PKV_ERR_SHAPE;
-  *out = PoolShape{pool->num_blocks, pool->block_size, pool->n_kv, pool->head_dim, pool->dtype};
-  if (out->row_bytes() % 16 != 0) return PKV_ERR_ALIGN;
-  if ((int64_t)pool->num_blocks * pool->block_size > INT32_MAX) return PKV_ERR_RANGE;
-  return PKV_OK;
-}
-
-pkv_status from_cuda(cudaError_t e) {
-  if (e == cudaSuccess) return PKV_OK;
-  cudaGetLastError();  // clear a sticky launch-configuration error
-  return PKV_ERR_CUDA;
-}
+using pkv::aligned16;
+using pkv::check_attention;
+using pkv::check_pool;
+using pkv::from_cuda;
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
-
-pkv_status check_attention(const void* q, int32_t num_seqs, int32_t n_heads, const void* k_pool,
-                           const void* v_pool, const pkv_pool_desc* pool,
-                           const int32_t* block_tables, int32_t max_blocks_per_seq,
-                           const int32_t* seq_lens, int32_t max_seq_len, float scale,
-                           const void* out, PoolShape* shape) {
-  pkv_status st = check_pool(pool, shape);
-  if (st != PKV_OK) return st;
-  if (num_seqs < 0 || n_heads <= 0 || max_blocks_per_seq < 0 || max_seq_len < 0)
-    return PKV_ERR_SHAPE;
-  if (n_heads % shape->n_kv != 0) return PKV_ERR_SHAPE;
-  if (!(scale > 0.f) || scale == __builtin_inff())
-    return PKV_ERR_RANGE;
-  if (num_seqs == 0) return PKV_OK;
-  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PKV_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
-    return PKV_ERR_ALIGN;
-  if (max_blocks_per_seq == 0 && max_seq_len > 0) return PKV_ERR_SHAPE;
-  if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * shape->block_size) return PKV_ERR_SHAPE;
-  return PKV_OK;
-}
 
 }  // namespace
 
@@ -77,6 +43,7 @@ pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_
                             const int32_t* seq_lens, const int32_t* cu_new_lens, int32_t num_seqs,
                             int32_t num_tokens, int32_t block_size, int32_t num_blocks,
                             int64_t* slot_mapping, int32_t* err_word, void* stream) {
+  PKV_NVTX_RANGE("pkv_slot_mapping");
   if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0) return PKV_ERR_SHAPE;
   if (block_size <= 0 || num_blocks <= 0) return PKV_ERR_SHAPE;
   if (num_tokens == 0) return PKV_OK;
@@ -91,6 +58,7 @@ pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_
 pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
                         int32_t num_tokens, void* k_pool, void* v_pool, const pkv_pool_desc* pool,
                         int32_t* err_word, void* stream) {
+  PKV_NVTX_RANGE("pkv_kv_write");
   PoolShape shape;
   pkv_status st = check_pool(pool, &shape);
   if (st != PKV_OK) return st;
@@ -106,6 +74,7 @@ pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mappin
 pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const pkv_pool_desc* pool,
                           const int32_t* block_pairs, int32_t num_pairs, int32_t* err_word,
                           void* stream) {
+  PKV_NVTX_RANGE("pkv_copy_blocks");
   PoolShape shape;
   pkv_status st = check_pool(pool, &shape);
   if (st != PKV_OK) return st;
@@ -122,6 +91,7 @@ pkv_status pkv_kv_gather(const void* k_pool, const void* v_pool, const pkv_pool_
                          const int32_t* seq_lens, const int32_t* cu_seq_lens, int32_t num_seqs,
                          int32_t total_tokens, void* k_out, void* v_out, int32_t* err_word,
                          void* stream) {
+  PKV_NVTX_RANGE("pkv_kv_gather");
   PoolShape shape;
   pkv_status st = check_pool(pool, &shape);
   if (st != PKV_OK) return st;
@@ -172,11 +142,10 @@ pkv_status decode_entry(const void* q, const void* k_new, const void* v_new, int
                         void* workspace, size_t workspace_bytes, int32_t* err_word,
                         void* stream, int32_t plan_mode = pkv::kPlanInCall) {
   PoolShape shape;
-  pkv_status st = check_attention(q, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
-                                  max_blocks_per_seq, seq_lens, max_seq_len, scale, out, &shape);
+  pkv_status st = pkv::check_decode(q, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
+                                    max_blocks_per_seq, seq_lens, max_seq_len, scale, max_ctas,
+                                    out, &shape);
   if (st != PKV_OK) return st;
-  if (max_ctas < 0) return PKV_ERR_RANGE;
-  if (!pkv::decode_supported(shape, n_heads)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
   if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_NULL;
   if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_ALIGN;
@@ -222,6 +191,7 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n
                                       int32_t max_seq_len, float scale, int32_t max_ctas,
                                       void* out, void* workspace, size_t workspace_bytes,
                                       int32_t* err_word, void* stream) {
+  PKV_NVTX_RANGE("pkv_paged_attention_decode");
   return decode_entry(q, nullptr, nullptr, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
                       max_blocks_per_seq, seq_lens, max_seq_len, 0, scale, max_ctas, out,
                       workspace, workspace_bytes, err_word, stream);
@@ -233,6 +203,7 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
     const int32_t* seq_lens, int32_t max_seq_len, int32_t shared_prefix_blocks, float scale,
     int32_t max_ctas, void* out, void* workspace, size_t workspace_bytes, int32_t* err_word,
     void* stream) {
+  PKV_NVTX_RANGE("pkv_paged_attention_decode_shared_prefix");
   return decode_entry(q, nullptr, nullptr, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
                       max_blocks_per_seq, seq_lens, max_seq_len, shared_prefix_blocks, scale,
                       max_ctas, out, workspace, workspace_bytes, err_word, stream);
@@ -244,6 +215,7 @@ pkv_status pkv_paged_attention_decode_append(
     int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len, float scale,
     int32_t max_ctas, void* out, void* workspace, size_t workspace_bytes, int32_t* err_word,
     void* stream) {
+  PKV_NVTX_RANGE("pkv_paged_attention_decode_append");
   if (num_seqs > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_NULL;
   return decode_entry(q, k_new, v_new, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
                       max_blocks_per_seq, seq_lens, max_seq_len, 0, scale, max_ctas, out,
@@ -255,6 +227,7 @@ pkv_status pkv_decode_plan(int32_t num_seqs, int32_t n_heads, const pkv_pool_des
                            int32_t max_seq_len, int32_t shared_prefix_blocks, int32_t max_ctas,
                            void* workspace, size_t workspace_bytes, int32_t* err_word,
                            void* stream) {
+  PKV_NVTX_RANGE("pkv_decode_plan");
   PoolShape shape;
   pkv_status st = check_pool(pool, &shape);
   if (st != PKV_OK) return st;
@@ -298,6 +271,7 @@ pkv_status pkv_paged_attention_decode_planned(
     int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
     int32_t shared_prefix_blocks, float scale, int32_t max_ctas, void* out, void* workspace,
     size_t workspace_bytes, int32_t* err_word, void* stream) {
+  PKV_NVTX_RANGE("pkv_paged_attention_decode_planned");
   return decode_entry(q, k_new, v_new, num_seqs, n_heads, k_pool, v_pool, pool, block_tables,
                       max_blocks_per_seq, seq_lens, max_seq_len, shared_prefix_blocks, scale,
                       max_ctas, out, workspace, workspace_bytes, err_word, stream,
@@ -314,6 +288,7 @@ pkv_status pkv_paged_attention_prefill(const void* q, const int32_t* cu_q_lens, 
                                        int32_t max_seq_len, float scale, void* out,
                                        void* workspace, size_t workspace_bytes,
                                        int32_t* err_word, void* stream) {
+  PKV_NVTX_RANGE("pkv_paged_attention_prefill");
   (void)workspace;
   (void)workspace_bytes;
   PoolShape shape;
@@ -346,6 +321,7 @@ pkv_status pkv_paged_attention_prefill(const void* q, const int32_t* cu_q_lens, 
 }
 
 pkv_status pkv_selftest_bounded_wait(int32_t polls, int32_t* err_word, void* stream) {
+  PKV_NVTX_RANGE("pkv_selftest_bounded_wait");
   if (polls < 1) return PKV_ERR_RANGE;
   if (!err_word) return PKV_ERR_NULL;
   return from_cuda(

@@ -20,7 +20,10 @@
 // where the GPU can reach host memory).  The device address is looked up
 // with cudaGetSymbolAddress, once per device, with that device current,
 // during the first call on that device; make that first call before any
-// stream capture.
+// stream capture.  The cached address is kept for the life of the process:
+// cudaDeviceReset destroys the context that holds the array and a later
+// context may load it at another address, so a device that was reset must
+// not be given to this entry point again.
 //
 // All calls share the one array.  Nothing in it needs to start at zero:
 // each call writes the work prefix and every partial slot before reading
@@ -33,7 +36,9 @@
 #include <mutex>
 
 #include "../../include/pkv.h"
+#include "checks.h"
 #include "launch.h"
+#include "nvtx.h"
 
 namespace {
 
@@ -66,8 +71,6 @@ pkv_status scratch_on_current_device(void** addr) {
   return PKV_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" pkv_status pkv_paged_attention_decode_noalloc(
@@ -75,27 +78,15 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
     const pkv_pool_desc* pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
     const int32_t* seq_lens, int32_t max_seq_len, float scale, int32_t max_ctas, void* out,
     int32_t* err_word, void* stream) {
-  // Same argument checks as pkv_paged_attention_decode.
-  if (pool == nullptr) return PKV_ERR_NULL;
-  if (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16) return PKV_ERR_DTYPE;
-  if (pool->num_blocks <= 0 || pool->block_size <= 0 || pool->n_kv <= 0 || pool->head_dim <= 0)
-    return PKV_ERR_SHAPE;
-  const pkv::PoolShape shape{pool->num_blocks, pool->block_size, pool->n_kv, pool->head_dim,
-                             pool->dtype};
-  if (shape.row_bytes() % 16 != 0) return PKV_ERR_ALIGN;
-  if (num_seqs < 0 || n_heads <= 0 || max_blocks_per_seq < 0 || max_seq_len < 0)
-    return PKV_ERR_SHAPE;
-  if (n_heads % shape.n_kv != 0) return PKV_ERR_SHAPE;
-  if (!(scale > 0.f) || scale == __builtin_inff())
-    return PKV_ERR_RANGE;
-  if (max_ctas < 0) return PKV_ERR_RANGE;
-  if (!pkv::decode_supported(shape, n_heads)) return PKV_ERR_UNSUPPORTED;
+  PKV_NVTX_RANGE("pkv_paged_attention_decode_noalloc");
+  // The argument checks of pkv_paged_attention_decode (one shared function,
+  // so the two entry points refuse the same arguments with the same status).
+  pkv::PoolShape shape;
+  const pkv_status chk = pkv::check_decode(q, num_seqs, n_heads, k_pool, v_pool, pool,
+                                           block_tables, max_blocks_per_seq, seq_lens,
+                                           max_seq_len, scale, max_ctas, out, &shape);
+  if (chk != PKV_OK) return chk;
   if (num_seqs == 0) return PKV_OK;
-  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PKV_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
-    return PKV_ERR_ALIGN;
-  if (max_blocks_per_seq == 0 && max_seq_len > 0) return PKV_ERR_SHAPE;
-  if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * shape.block_size) return PKV_ERR_SHAPE;
 
   void* scratch = nullptr;
   const pkv_status st = scratch_on_current_device(&scratch);

@@ -48,15 +48,28 @@ cudaError_t kernel_setup(KernelSetup& ks, Kern kern, int smem, int threads, int*
   return cudaSuccess;
 }
 
-// SMs of the current device (looked up once per process).
+// SMs of the current device, looked up once per device (devices past
+// kMaxCachedDevices are asked every time).  Entries are atomics, so threads
+// calling on different devices neither race nor see each other's count.
 inline int sm_count() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
+  static std::atomic<int> cached[kMaxCachedDevices];  // static storage: starts at 0
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
   }
+  const bool keep = dev >= 0 && dev < kMaxCachedDevices;
+  if (keep) {
+    const int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 0;
+  }
+  if (sms <= 0) sms = 1;
+  if (keep) cached[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
 

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "device.cuh"
+#include "host_cache.h"
 #include "launch.h"
 
 namespace pkv {
@@ -156,16 +157,11 @@ __global__ void kv_gather_kernel(const uint4* __restrict__ k_pool, const uint4* 
   }
 }
 
+// Grid-stride grid for `work` 16-byte words: at most 8 CTAs per SM of the
+// current device.
 int grid_for(int64_t work) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-  }
   int64_t blocks = (work + kThreads - 1) / kThreads;
-  const int64_t cap = int64_t(sms) * 8;
+  const int64_t cap = int64_t(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return static_cast<int>(blocks);

@@ -28,3 +28,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _guard_bands(request, monkeypatch):
+    """GPU tests: every output and workspace the binding allocates, and the
+    device tensors of tests/gpu_step.py's GpuStep, carry canary bands that
+    are checked after every call (the stand-in for an out-of-bounds checker)."""
+    if "gpu" not in request.keywords or not _gpu_available():
+        yield
+        return
+    import gpu_step
+    import paged_kv_cache_write_gb300 as pkv
+    gpu_step.start_guarding(monkeypatch, pkv)
+    yield
+    gpu_step.stop_guarding()

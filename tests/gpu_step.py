@@ -3,12 +3,126 @@ through the C ABI (via the ctypes binding) and the same step through the
 CPU oracle, on the same seeded inputs."""
 from __future__ import annotations
 
+import functools
+import inspect
+import math
+
 import numpy as np
 import torch
 
 import oracle
 
 TOL = {"f32": dict(max_abs=1e-5, mean_abs=1e-5), "bf16": dict(max_abs=2e-2, mean_abs=2e-3)}
+
+# ---------------------------------------------------------------- canaries
+# Guard bands stand in for a memory checker's out-of-bounds detection:
+# device tensors the tests hand to the kernels (inputs, pools, outputs,
+# workspaces) sit inside larger buffers with CANARY bytes of a fixed random
+# pattern on each side, and every call through the binding is followed by
+# a check that no pattern byte changed.
+
+CANARY = 4096  # bytes on each side (keeps the tensor 16- and 256-byte aligned)
+_LIVE = []     # (buffer, payload bytes) of the running test
+_PATTERNS = {}
+
+
+def _pattern(device):
+    key = str(device)
+    if key not in _PATTERNS:
+        g = torch.Generator(device="cpu").manual_seed(0xC0FFEE)
+        _PATTERNS[key] = torch.randint(0, 256, (CANARY,), dtype=torch.uint8,
+                                       generator=g).to(device)
+    return _PATTERNS[key]
+
+
+def guarded_empty(shape, dtype, device="cuda"):
+    """Uninitialised device tensor with canary bands on both sides."""
+    shape = tuple(int(x) for x in shape)
+    n = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+    buf = torch.empty(n + 2 * CANARY, dtype=torch.uint8, device=device)
+    pat = _pattern(buf.device)
+    buf[:CANARY] = pat
+    buf[CANARY + n:] = pat
+    _LIVE.append((buf, n))
+    return buf[CANARY:CANARY + n].view(dtype).view(shape)
+
+
+def guarded_copy(t, device="cuda"):
+    """Device copy of ``t`` with canary bands on both sides."""
+    out = guarded_empty(t.shape, t.dtype, device)
+    out.copy_(t)
+    return out
+
+
+def check_canaries():
+    """Raise if any guard band of the running test changed."""
+    if not _LIVE:
+        return
+    torch.cuda.synchronize()
+    for buf, n in _LIVE:
+        pat = _pattern(buf.device)
+        if not (torch.equal(buf[:CANARY], pat) and torch.equal(buf[CANARY + n:], pat)):
+            raise AssertionError(f"a kernel wrote outside a {n}-byte tensor (canary changed)")
+
+
+def _ws_bytes(pkv, name, a):
+    """Workspace the binding would allocate for call `name` (bound args a)."""
+    q = a["q"]
+    B, H, hd = q.shape
+    msl = a.get("max_seq_len")
+    if msl is None:
+        msl = int(a["seq_lens"].max().item()) if B else 0
+    if name == "paged_attention_decode_shared_prefix":
+        return pkv.decode_shared_prefix_workspace_bytes(B, H, hd, msl, a["shared_prefix_blocks"],
+                                                        a.get("max_ctas", 0))
+    return pkv.decode_workspace_bytes(B, H, hd, msl, a.get("max_ctas", 0))
+
+
+_OUT_LIKE_Q = ("paged_attention_decode", "paged_attention_decode_append",
+               "paged_attention_decode_shared_prefix", "paged_attention_decode_planned",
+               "paged_attention_prefill", "paged_attention_decode_noalloc")
+_WS = ("paged_attention_decode", "paged_attention_decode_append",
+       "paged_attention_decode_shared_prefix")
+_WRAPPED = _OUT_LIKE_Q + ("slot_mapping", "kv_write", "kv_gather", "copy_blocks", "decode_plan")
+
+
+def start_guarding(monkeypatch, pkv):
+    """Wrap the binding's entry points for one test: outputs and workspaces
+    the binding would allocate come from guarded buffers, and the canaries
+    of every guarded tensor are checked after each call."""
+    _LIVE.clear()
+    for name in _WRAPPED:
+        fn = getattr(pkv, name)
+        sig = inspect.signature(fn)
+
+        @functools.wraps(fn)
+        def wrapper(*args, __fn=fn, __sig=sig, __name=name, **kwargs):
+            bound = __sig.bind(*args, **kwargs)
+            bound.apply_defaults()
+            a = bound.arguments
+            if __name in _OUT_LIKE_Q and a.get("out") is None:
+                a["out"] = guarded_empty(a["q"].shape, a["q"].dtype, a["q"].device)
+            if __name in _WS and a.get("workspace") is None:
+                a["workspace"] = guarded_empty((_ws_bytes(pkv, __name, a),), torch.uint8,
+                                               a["q"].device)
+            if __name == "slot_mapping" and a.get("out") is None:
+                a["out"] = guarded_empty((a["num_tokens"],), torch.int64,
+                                         a["block_tables"].device)
+            if __name == "kv_gather":
+                shape = (int(a["total_tokens"]), a["k_pool"].shape[2], a["k_pool"].shape[3])
+                for k in ("k_out", "v_out"):
+                    if a.get(k) is None:
+                        a[k] = guarded_empty(shape, a["k_pool"].dtype, a["k_pool"].device)
+            result = __fn(*bound.args, **bound.kwargs)
+            check_canaries()
+            return result
+
+        monkeypatch.setattr(pkv, name, wrapper)
+
+
+def stop_guarding():
+    check_canaries()
+    _LIVE.clear()
 
 
 def raw(t: torch.Tensor) -> np.ndarray:
@@ -44,19 +158,20 @@ class GpuStep:
         self.plan = plan
         sh = plan.shape
         self.sh = sh
-        self.bt = torch.from_numpy(plan.block_tables).to(device)
-        self.seq_lens = torch.from_numpy(plan.seq_lens).to(device)
-        self.cu_new = torch.from_numpy(plan.cu_new_lens).to(device)
-        self.t = {n: v.to(device) for n, v in layer.items()}
+        self.bt = guarded_copy(torch.from_numpy(plan.block_tables), device)
+        self.seq_lens = guarded_copy(torch.from_numpy(plan.seq_lens), device)
+        self.cu_new = guarded_copy(torch.from_numpy(plan.cu_new_lens), device)
+        self.t = {n: guarded_copy(v, device) for n, v in layer.items()}
         nd = plan.n_decode
         self.nd = nd
         self.max_dec = int(plan.seq_lens[:nd].max()) if nd else 0
         if plan.num_seqs > nd:
             cu = plan.cu_new_lens[nd:] - plan.cu_new_lens[nd]
-            self.cu_q = torch.from_numpy(cu.astype(np.int32)).to(device)
+            self.cu_q = guarded_copy(torch.from_numpy(cu.astype(np.int32)), device)
             self.max_q = int(plan.new_lens[nd:].max())
             self.max_pre = int(plan.seq_lens[nd:].max())
-        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.err = guarded_empty((1,), torch.int32, device)
+        self.err.zero_()
 
     def slots(self):
         p = self.plan

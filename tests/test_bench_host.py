@@ -47,4 +47,26 @@ def test_reference_arm_json_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert "smollm2-135m" in cb["sample"] and "0 prefill queries" in cb["sample"]
-    assert d["config"]["workload"] == "smollm2-135m"
+    assert d["config"]["workload"] == "smollm2-135m" and "launch" not in d["config"]
+    assert cb["host_cores"] >= 1
+
+
+def test_decode_traffic_ratios_match_current_kernel_sources():
+    """Every DRAM-traffic ratio the benchmark reports was captured on the
+    decode kernel sources as they are now: a ratio recorded with another
+    source hash is stale (recapture it, or drop the entry)."""
+    h = bench.decode_source_hash()
+    for key, rec in bench.DECODE_TRAFFIC.items():
+        assert rec["source_sha256"] == h, (
+            f"traffic ratio for {key} was captured on decode sources {rec['source_sha256']}, "
+            f"now {h}")
+        assert 0.9 < rec["ratio"] < 2.0 and rec["capture"]
+
+
+def test_config_has_workload_keys_only():
+    """Both arms describe the workload with the same keys; how the GPU arm
+    launches its kernels is reported outside `config`."""
+    from workloads import draw_plan
+    cfg = bench.workload_config(draw_plan("llama2-70b-mixed"))
+    assert "launch" not in cfg
+    assert cfg["workload"] == bench.WORKLOAD_LABEL and cfg["layers_timed"] == 1

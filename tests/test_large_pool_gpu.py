@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_step import GpuStep, OracleStep, assert_close, f64
+from gpu_step import GpuStep, OracleStep, assert_close, f64, guarded_empty
 from workloads import make_tiny_layer, tiny_plan
 
 pytestmark = pytest.mark.gpu
@@ -37,8 +37,8 @@ def test_pool_beyond_4gib():
     off = BIG_BLOCKS - nb
     assert off * 16 * 8 * 128 * 2 > 2 ** 32
     shape = (BIG_BLOCKS, 16, 8, 128)
-    kb = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
-    vb = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    kb = guarded_empty(shape, torch.bfloat16)  # canary bands past the 5.4 GB pools
+    vb = guarded_empty(shape, torch.bfloat16)
     kb[off:] = kp0
     vb[off:] = vp0
     bt = (small.bt.long() + off).int()

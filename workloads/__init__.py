@@ -28,7 +28,12 @@ Recipe:
   * pool: every block handed to some sequence is filled with N(0, 1) values
     (all of its slots, including a last block's unused tail); blocks nobody
     holds are filled with ``fill`` (0 for timing, a large sentinel or NaN in
-    masking tests).
+    masking tests);
+  * timing-only layers (``make_layer_on_device``: the layers after the first
+    of a many-layer step, whose outputs nothing checks): the same shapes and
+    distribution, drawn by a ``torch.Generator`` on the GPU seeded with
+    ``7000 + 1000*config_id + layer`` (drawing gigabytes of pool on the host
+    would dominate the benchmark's run time).
 """
 from __future__ import annotations
 
@@ -38,7 +43,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-__all__ = ["Shape", "SHAPES", "CONFIG_IDS", "draw_plan", "make_layer", "Plan"]
+__all__ = ["Shape", "SHAPES", "CONFIG_IDS", "draw_plan", "make_layer", "make_layer_on_device", "Plan"]
 
 
 @dataclass(frozen=True)
@@ -294,3 +299,28 @@ def make_tiny_layer(plan: Plan, seed: int = 0, *, fill: float = 0.0, device="cpu
     if device != "cpu":
         out = {n: t.to(device) for n, t in out.items()}
     return out
+
+
+def make_layer_on_device(plan: Plan, layer: int, device):
+    """A timing-only layer drawn directly on ``device``: the shapes and
+    N(0, 1) values of ``make_layer`` (held blocks filled, the rest zero),
+    from a device generator seeded per (shape, layer)."""
+    sh = plan.shape
+    g = torch.Generator(device=device)
+    g.manual_seed(7000 + 1000 * CONFIG_IDS[sh.name] + layer)
+    T = plan.num_new_tokens
+    dt = sh.torch_dtype
+
+    def draw(*shape):
+        return torch.randn(*shape, generator=g, device=device).to(dt)
+
+    q = draw(T, sh.n_heads, sh.head_dim)
+    k = draw(T, sh.n_kv, sh.head_dim)
+    v = draw(T, sh.n_kv, sh.head_dim)
+    pool_shape = (sh.num_blocks, sh.block_size, sh.n_kv, sh.head_dim)
+    held = torch.from_numpy(plan.held_blocks).to(device)
+    k_pool = torch.zeros(pool_shape, dtype=dt, device=device)
+    v_pool = torch.zeros(pool_shape, dtype=dt, device=device)
+    k_pool[held] = draw(len(held), *pool_shape[1:])
+    v_pool[held] = draw(len(held), *pool_shape[1:])
+    return dict(q=q, k=k, v=v, k_pool=k_pool, v_pool=v_pool)
