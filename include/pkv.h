@@ -37,13 +37,18 @@
  *  Memory.  Every pointer argument except `pool` (a host struct) is DEVICE
  *  memory owned by the caller, contiguous and row-major.  Tensors read or
  *  written as 16-byte vectors (q, k, v, pools, out) must be 16-byte
- *  aligned.  The library allocates nothing, keeps no state between calls
- *  and never synchronises the device.
+ *  aligned.  The library never allocates device memory and never
+ *  synchronises the device.  The only state it keeps between calls is
+ *  host-side, per device: cached launch set-up (each kernel's shared-memory
+ *  opt-in and occupancy, the SM count), held in atomics; and, for
+ *  pkv_paged_attention_decode_noalloc alone, one fixed device array
+ *  compiled into the library and its looked-up address (see that entry).
  *
  *  Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *  default stream).  Every call only enqueues work on that stream and
  *  returns; results are visible to later work on the same stream.  Calls
- *  are thread-safe.
+ *  are thread-safe, except that pkv_paged_attention_decode_noalloc calls
+ *  whose kernels overlap on the GPU race on its shared array (see there).
  *
  *  Pool layout.  One pool per layer for K and one for V, each
  *  [num_blocks, block_size, n_kv, head_dim] of `dtype`.  Slot
@@ -236,7 +241,14 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t hea
  * points depend only on logical block positions, the lengths and max_ctas,
  * never on physical block ids, so the output is bit-identical under any
  * physical placement or sharing of blocks.  max_ctas = 1 computes every
- * sequence unsplit.
+ * sequence unsplit.  Small batches (max_ctas = 0, the longest sequence at
+ * most 64 blocks, and at most two waves of CTAs) are latency-bound rather
+ * than bandwidth-bound; for them each (sequence, KV-head group) is instead
+ * split over one thread-block cluster of up to 8 CTAs (about 4 blocks
+ * each, contiguous, split points fixed by the length alone), whose partial
+ * results are combined in distributed shared memory within the same
+ * launch.  Either way the split depends only on logical positions, and
+ * identical calls give identical bits.
  *
  *   q, out     [num_seqs, n_heads, head_dim] of pool->dtype
  *   scale      positive and finite (else PKV_ERR_RANGE)
@@ -337,9 +349,15 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * the split of the step's blocks over the decode grid (which CTA walks
  * which blocks) and leaves it in `workspace`; each layer's
  * pkv_paged_attention_decode_planned then reads that plan instead of
- * computing it, and reads its plan and first table entries before waiting
- * for the kernel launched just before it (programmatic dependent launch),
- * so that work overlaps the previous kernel's end.  The outputs are those
+ * computing it, and reads its plan, its first table entries and (bf16
+ * pools with head_dim 64 or 128) the K/V of its first blocks before
+ * waiting for the kernel launched just before it (programmatic dependent
+ * launch), so that work overlaps the previous kernel's end.  Those early
+ * reads never touch a sequence's last block, the only block a decode step
+ * writes: a kernel that can still be running when a planned call starts
+ * (one that lets its dependents launch early, as this library's decode
+ * kernels do) must not write any other block of the planned call's
+ * sequences.  Queries, outputs and every write wait for that kernel.  The outputs are those
  * of pkv_paged_attention_decode (k_new and v_new both NULL) or
  * pkv_paged_attention_decode_append (both given), bit for bit; with
  * shared_prefix_blocks > 0 they are those of
@@ -440,8 +458,11 @@ pkv_status pkv_paged_attention_prefill(const void* q, const int32_t* cu_q_lens,
  * Its scratch is one array of PKV_NOALLOC_SCRATCH_BYTES compiled into the
  * library; every GPU that loads the library holds it until the process
  * exits.  The first call on each device looks up the array's device
- * address (make that first call before any stream capture).  The call
- * itself allocates nothing.  Nothing in the array must start at zero.
+ * address (make that first call before any stream capture); the address is
+ * then cached for the life of the process.  cudaDeviceReset tears the
+ * module down and may reload the array elsewhere, so do not call this
+ * entry point on a device after resetting it.  The call itself allocates
+ * nothing.  Nothing in the array must start at zero.
  * Calls whose kernels overlap on the GPU (e.g. issued on two streams)
  * race on the shared array: issue them on one stream.  A batch needing
  * more scratch than the array holds returns PKV_ERR_WORKSPACE without

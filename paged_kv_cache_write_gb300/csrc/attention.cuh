@@ -658,6 +658,9 @@ struct DecodeParams {
   // 1 (main kernel): the plan is in the workspace from a finished plan-only
   // launch, so it and the tables are read before the dependency wait
   int planned;
+  // cluster decode: CTAs per (sequence, head group) cluster (0: stream-K
+  // path) and the byte offset of the partial results in shared memory
+  int cluster, part_off;
   float scale_log2;
 };
 
@@ -999,14 +1002,27 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
   Cursor cur;
   if (r0 < r1) cur.load(p, st);
   // planned call: the producer's first table entries are loaded before the
-  // wait (the plan's contract: lengths and tables unchanged since the plan)
-  int pre_id = 0;
+  // wait (the plan's contract: lengths and tables unchanged since the plan),
+  // and on the tile path its first blocks too: up to a ring's worth of the
+  // first segment, never the sequence's last block (the only block a decode
+  // step writes), so their bytes stream in while the preceding kernel ends
+  int pre_id = 0, early = 0;
   bool pre = false;
   if (p.planned) {
     if (warp == consumers && r0 < r1) {
       const int n0 = min(r1 - r0, cur.nblk - cur.j);
       pre_id = lane < n0 ? __ldg(p.bt + int64_t(cur.b) * p.W + p.prefix_blocks + cur.j + lane) : 0;
       pre = true;
+      if constexpr (MMA) {
+        const int lim = min(min(n0, 32), min(p.nstages, cur.nblk - 1 - cur.j));
+        for (; early < lim; ++early) {
+          const int blk = __shfl_sync(0xffffffffu, pre_id, early);
+          if (blk < 0 || blk >= p.num_blocks) break;  // the main loop reports it
+          if (lane == 0)  // stage `early` is unused yet: no wait
+            tile_fill(ring, static_cast<uint32_t>(early), tm_k, tm_v, blk * kBS,
+                      cur.grp * p.hg_size, p.err);
+        }
+      }
     }
     pdl_wait();
     if (p.prefix_blocks == 0)
@@ -1016,7 +1032,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
 
   if (warp == consumers) {
     // ------------------------------------------------------ producer
-    uint32_t it = 0;
+    uint32_t it = static_cast<uint32_t>(early);  // blocks already issued before the wait
+    int skip = early;
     bool ok = true;
     for (int u = r0; u < r1 && ok;) {
       const int n = min(r1 - u, cur.nblk - cur.j);
@@ -1026,7 +1043,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
         int id = pre ? pre_id : (jj + lane < n) ? __ldg(row + p.prefix_blocks + cur.j + jj + lane) : 0;
         pre = false;
         const int n_here = min(32, n - jj);
-        for (int k = 0; k < n_here; ++k) {
+        const int k0 = skip;
+        skip = 0;
+        for (int k = k0; k < n_here; ++k) {
           if (*ring.abort_flag) { ok = false; break; }
           const int blk = __shfl_sync(0xffffffffu, id, k);
           const int j = p.prefix_blocks + cur.j + jj + k;  // table index
@@ -1187,6 +1206,229 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) __maxnreg__(HD ==
 template <typename T, int HD, int MAXR>
 __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_rows_kernel(DecodeParams p) {
   decode_body<T, HD, MAXR, false>(nullptr, nullptr, p);
+}
+
+// ------------------------------------------------------- cluster decode
+//
+// Latency-bound batches (few sequences of at most a few hundred tokens,
+// where the stream-K split would leave each CTA a handful of blocks and the
+// merge launch would cost as much as the reads): one thread-block cluster
+// of C CTAs per (sequence, KV-head group).  CTA r walks blocks
+// [r n / C, (r + 1) n / C) of the sequence's n blocks (split points depend
+// only on the length and C, so placement and sharing of blocks change no
+// bit), leaves its normalised partial (output rows, max, exp-sum) in its
+// own shared memory, and after a cluster barrier the C CTAs combine the
+// partials through distributed shared memory, each CTA a slice of the
+// output elements, with log-sum-exp weights.  A second barrier keeps every
+// CTA's shared memory alive until its peers have read it.  Every thread of
+// the cluster reaches both barriers (waits in the loops are bounded; an
+// aborted CTA still leaves a partial).  Nothing goes through global
+// memory but the inputs and the output: no workspace, no merge launch.
+constexpr int kMaxCluster = 8;
+
+template <typename T, int HD, int MAXR, bool MMA>
+__device__ __forceinline__ void decode_cluster_body(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                                    const DecodeParams& p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using Rows = typename RowsOf<T, HD, MAXR, MMA>::type;
+  const int consumers = p.hg_size;
+  const int row_bytes = p.hg_size * HD * p.elem_bytes;
+  Ring ring = MMA ? make_tile_ring(smem, p.nstages, kBS * row_bytes)
+                  : make_ring(smem, p.nstages, row_bytes);
+  ring_init(ring, consumers);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = p.cluster;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int seg = static_cast<int>(blockIdx.x) / C;  // (sequence, head group)
+  const int b = seg / p.n_groups;
+  const int grp = seg - b * p.n_groups;
+  const int rows_per_group = p.hg_size * p.rep;
+  float* part_o = reinterpret_cast<float*>(smem + p.part_off);  // [rows_per_group][HD]
+  float* part_ml = part_o + rows_per_group * HD;                // [rows_per_group][2]
+
+  // a planned call checks the kept plan (written by a finished launch) before
+  // anything else; every CTA of the cluster reads the same record, so all of
+  // them leave here together, before any cluster barrier
+  if (p.planned && !plan_matches(p, p.grid)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(p.err, PKV_DEVERR_PLAN);
+    return;
+  }
+  if (!p.planned) pdl_wait();  // lengths and tables may come from the preceding kernel
+  pdl_launch_dependents();
+  if (!p.planned && blockIdx.x == 0 && threadIdx.x == 0)
+    p.total_units[1] = -1;  // a call planning for itself replaces any kept plan
+
+  const int L = used_len(p, b);
+  const int nblk = (L + kBS - 1) / kBS;
+  const int j0 = static_cast<int>(int64_t(rank) * nblk / C);
+  const int j1 = static_cast<int>(int64_t(rank + 1) * nblk / C);
+  if (!p.planned && rank == 0 && grp == 0 && threadIdx.x == 0) check_length(p, b);
+  const int64_t token_pitch = int64_t(p.n_kv) * HD * p.elem_bytes;
+  const int64_t head_off = int64_t(grp) * p.hg_size * HD * p.elem_bytes;
+  // append: the CTA holding the sequence's last block stores and uses the
+  // step's row (not for a length clamped from a bad value)
+  const bool append = p.k_new != nullptr && j1 == nblk && j1 > j0 && __ldg(p.seq_lens + b) == L;
+
+  if (warp == consumers) {
+    // ------------------------------------------------------ producer
+    // A planned call loads its first blocks before the kernel launched just
+    // before it has finished (up to a ring's worth, never the sequence's
+    // last block, the only one a decode step writes), then waits.
+    bool waited = !p.planned;
+    uint32_t it = 0;
+    bool ok = true;
+    const int32_t* row = p.bt + int64_t(b) * p.W;
+    for (int jj = j0; jj < j1 && ok; jj += 32) {
+      const int id = jj + lane < j1 ? __ldg(row + jj + lane) : 0;
+      const int n_here = min(32, j1 - jj);
+      for (int k = 0; k < n_here; ++k) {
+        const int j = jj + k;
+        if (!waited && (!MMA || it >= static_cast<uint32_t>(p.nstages) || j == nblk - 1)) {
+          pdl_wait();
+          waited = true;
+        }
+        if (*ring.abort_flag) { ok = false; break; }
+        const int blk = __shfl_sync(0xffffffffu, id, k);
+        int valid = min(kBS, L - j * kBS);
+        if (blk < 0 || blk >= p.num_blocks) {
+          if (lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
+          valid = 0;
+        }
+        const int64_t off = int64_t(valid > 0 ? blk : 0) * kBS * token_pitch + head_off;
+        const bool fresh = append && j == nblk - 1 && valid > 0;
+        const int new_row = fresh ? L - 1 - j * kBS : -1;
+        const int64_t new_off = int64_t(b) * p.n_kv * HD * p.elem_bytes + head_off;
+        bool filled;
+        if constexpr (MMA) {
+          filled = lane == 0 ? tile_fill(ring, it, tm_k, tm_v,
+                                         valid > 0 ? blk * kBS : p.num_blocks * kBS,
+                                         grp * p.hg_size, p.err)
+                             : true;
+          filled = __shfl_sync(0xffffffffu, filled, 0);
+        } else {
+          filled = ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err,
+                             new_row, p.k_new + new_off, p.v_new + new_off);
+        }
+        if (!filled) {
+          *ring.abort_flag = 1;
+          ok = false;
+          break;
+        }
+        ++it;
+        if (fresh) {  // the pool's copy of the step's row (this group's heads)
+          const int nvec = row_bytes / 16;
+          const int64_t dst = off + int64_t(new_row) * token_pitch;
+          for (int i = lane; i < 2 * nvec; i += 32) {
+            const bool is_v = i >= nvec;
+            const int64_t o = int64_t(is_v ? i - nvec : i) * 16;
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) +
+                                                                 new_off + o));
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(is_v ? p.v_pool : p.k_pool) + dst + o) = x;
+          }
+        }
+      }
+    }
+    if (!ok) ring_drain(ring, it);
+  } else if (warp < consumers) {
+    // ------------------------------------------------------ consumers
+    Rows rows;
+    if constexpr (!MMA) {
+      float* scratch = reinterpret_cast<float*>(ring.stages + p.nstages * ring.stage_bytes);
+      rows.bind(scratch + warp * RowsOf<T, HD, MAXR, MMA>::kScratch);
+    }
+    if (p.planned) pdl_wait();  // the queries may come from the preceding kernel
+    const T* q = static_cast<const T*>(p.q);
+    const int kv_head = grp * p.hg_size + warp;
+    const int head0 = kv_head * p.rep;
+    const int last = L - 1;
+    rows.begin(
+        [&](int r) -> const T* {
+          return r < p.rep ? q + (int64_t(b) * p.n_heads + head0 + r) * HD : nullptr;
+        },
+        [&](int) { return last; });
+    bool fresh = false;
+    uint32_t kn[2] = {0u, 0u}, vn[2] = {0u, 0u};
+    if constexpr (MMA) {
+      if (append) {
+        const int blk = __ldg(p.bt + int64_t(b) * p.W + nblk - 1);
+        fresh = blk >= 0 && blk < p.num_blocks;
+        if (fresh) new_row_piece<HD>(p.k_new, p.v_new, (int64_t(b) * p.n_kv + kv_head) * HD, kn, vn);
+      }
+    }
+    uint32_t it = 0;
+    for (int j = j0; j < j1; ++j, ++it) {
+      if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
+        *ring.abort_flag = 1;
+        break;
+      }
+      const int st = static_cast<int>(it % ring.nstages);
+      const int jpos = j * kBS;
+      if constexpr (MMA) {
+        uint8_t* kt = ring.k_tile(st);
+        uint8_t* vt = ring.v_tile(st);
+        const bool fix = j == nblk - 1 && (L - jpos < kBS || fresh);
+        if (fix) tile_fix<HD>(kt, vt, warp, L - jpos, fresh, kn, vn);
+        rows.block_sw(kt, vt, warp, jpos, p.scale_log2);
+        if (fix) fence_proxy_async_smem();
+      } else {
+        const int hoff = warp * HD * p.elem_bytes;
+        rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride, jpos,
+                   p.scale_log2);
+      }
+      ring_release(ring, it);
+    }
+    // this CTA's part (also after an abort, so the barrier below is reached)
+    rows.store_partial(
+        [&](int r) -> float* { return r < p.rep ? part_o + (warp * p.rep + r) * HD : nullptr; },
+        [&](int r) -> float* { return part_ml + (warp * p.rep + r) * 2; });
+  }
+
+  cluster_sync();  // every CTA's partial is in its shared memory
+  // CTA `rank` combines elements [rank E / C, (rank + 1) E / C) of the
+  // group's rows x head_dim outputs from the C partials
+  const int E = rows_per_group * HD;
+  const int e0 = rank * E / C, e1 = (rank + 1) * E / C;
+  T* out = static_cast<T*>(p.out) + (int64_t(b) * p.n_heads + int64_t(grp) * rows_per_group) * HD;
+  for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += static_cast<int>(blockDim.x)) {
+    const int r = e / HD;
+    float mc[kMaxCluster], lc[kMaxCluster];
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      mc[c] = -INFINITY;
+      lc[c] = 0.f;
+      if (c < C) {
+        const float2 ml = ld_cluster_f32x2(cluster_map(part_ml + r * 2, c));
+        mc[c] = ml.x;
+        lc[c] = ml.y;
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);  // a part that saw no key has no weight
+      }
+    }
+    float acc = 0.f, den = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      if (c < C && lc[c] > 0.f) {
+        const float w = fast_exp2(mc[c] - M) * lc[c];
+        den += w;
+        acc = fmaf(w, ld_cluster_f32(cluster_map(part_o + e, c)), acc);
+      }
+    }
+    out[e] = Elem<T>::from_f(den > 0.f ? acc * (1.f / den) : 0.f);
+  }
+  cluster_sync();  // the peers have read this CTA's partials
+}
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(decode_max_threads<T, HD>()) __maxnreg__(HD == 64 ? 112 : 224)
+    decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, DecodeParams p) {
+  decode_cluster_body<T, HD, 16, true>(&tm_k, &tm_v, p);
+}
+
+template <typename T, int HD, int MAXR>
+__global__ void __launch_bounds__(decode_max_threads<T, HD>())
+    decode_cluster_rows_kernel(DecodeParams p) {
+  decode_cluster_body<T, HD, MAXR, false>(nullptr, nullptr, p);
 }
 
 // Shared-prefix attention: the first prefix_blocks table entries are the
@@ -1719,8 +1961,31 @@ struct DecodeLaunch {
     else
       return decode_rows_kernel<T, HD, MAXR>;
   }
-  // Persistent grid: every SM filled with as many CTAs as fit, capped by max_ctas.
-  static cudaError_t grid(const AttnArgs& a, int hg, int* G, size_t* smem, int* nstages) {
+  static auto cluster_kernel() {
+    if constexpr (MMA)
+      return decode_cluster_kernel<T, HD>;
+    else
+      return decode_cluster_rows_kernel<T, HD, MAXR>;
+  }
+  // CTAs per cluster for the cluster path, or 0 for the stream-K path.  Only
+  // calls that leave the grid to the library (max_ctas 0) and share no
+  // prefix qualify, when the longest sequence is at most 64 blocks (each
+  // CTA then walks at most 8) and the clusters fit in two waves of the
+  // stream-K grid: batches too small to keep the machine streaming, whose
+  // time is latency (a block's round trip, the merge launch) rather than
+  // bytes.  About 4 blocks per CTA, at most 8 CTAs per cluster.
+  static int cluster_size(const AttnArgs& a, int hg, int wave) {
+    if (a.max_ctas != 0 || a.prefix_blocks != 0) return 0;
+    const int nmax = (min(a.max_seq_len, a.max_blocks_per_seq * kBS) + kBS - 1) / kBS;
+    if (nmax > 8 * kMaxCluster) return 0;
+    const int C = std::max(1, std::min(kMaxCluster, (nmax + 3) / 4));
+    const int64_t ctas = int64_t(a.num_seqs) * (a.pool.n_kv / hg) * C;
+    return ctas <= 2 * int64_t(wave) ? C : 0;
+  }
+  // Persistent grid: every SM filled with as many CTAs as fit, capped by
+  // max_ctas; *wave (optional) = the uncapped full wave.
+  static cudaError_t grid(const AttnArgs& a, int hg, int* G, size_t* smem, int* nstages,
+                          int* wave = nullptr) {
     *smem = smem_bytes(hg, a.pool.elem_bytes(), nstages);
     static KernelSetup setup;
     int per_sm = 0;
@@ -1729,6 +1994,7 @@ struct DecodeLaunch {
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     *G = sm_count() * per_sm;
+    if (wave) *wave = *G;
     if (a.max_ctas > 0 && a.max_ctas < *G) *G = a.max_ctas;
     // no more CTAs than the batch can have units (a small batch would
     // otherwise leave most ranges empty and its split groups spread thin)
@@ -1762,9 +2028,9 @@ struct DecodeLaunch {
     p.head_dim = HD;
     p.elem_bytes = pool.elem_bytes();
     p.scale_log2 = a.scale * kLog2e;
-    int G = 0;
+    int G = 0, wave = 0;
     size_t smem = 0;
-    cudaError_t e = grid(a, hg, &G, &smem, &p.nstages);
+    cudaError_t e = grid(a, hg, &G, &smem, &p.nstages, &wave);
     if (e != cudaSuccess) return e;
     if (G > 65535) return cudaErrorInvalidValue;  // split entries pack CTA indices in 16 bits
     p.grid = G;
@@ -1808,6 +2074,37 @@ struct DecodeLaunch {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    p.planned = a.decode_plan == kPlanned;
+    if (const int C = cluster_size(a, hg, wave); C > 0) {
+      // latency-bound batch: one cluster of C CTAs per (sequence, head
+      // group), partials combined in distributed shared memory
+      p.cluster = C;
+      p.part_off = static_cast<int>((smem + 15) / 16 * 16);
+      const size_t csmem = size_t(p.part_off) + size_t(hg) * p.rep * (HD + 2) * 4;
+      static KernelSetup cluster_setup;
+      e = kernel_setup(cluster_setup, cluster_kernel(), static_cast<int>(csmem), (hg + 1) * 32,
+                       nullptr);
+      if (e != cudaSuccess) return e;
+      cudaLaunchAttribute cattr[2];
+      cattr[0] = attr[0];
+      cattr[1].id = cudaLaunchAttributeClusterDimension;
+      cattr[1].val.clusterDim.x = static_cast<unsigned>(C);
+      cattr[1].val.clusterDim.y = 1;
+      cattr[1].val.clusterDim.z = 1;
+      cudaLaunchConfig_t ccfg = {};
+      ccfg.gridDim = dim3(static_cast<unsigned>(int64_t(p.B) * p.n_groups * C));
+      ccfg.blockDim = dim3((hg + 1) * 32);
+      ccfg.dynamicSmemBytes = csmem;
+      ccfg.stream = stream;
+      ccfg.attrs = cattr;
+      ccfg.numAttrs = 2;
+      if constexpr (MMA)
+        e = cudaLaunchKernelEx(&ccfg, decode_cluster_kernel<T, HD>, tm_k, tm_v, p);
+      else
+        e = cudaLaunchKernelEx(&ccfg, decode_cluster_rows_kernel<T, HD, MAXR>, p);
+      if (e != cudaSuccess) return e;
+      return cudaGetLastError();
+    }
     if (p.prefix_blocks > 0) {
       // the shared prefix: runs of its blocks, each read once per head group
       // for a chunk of sequences (same ring and shared memory as below)
@@ -1835,7 +2132,6 @@ struct DecodeLaunch {
     // small batches: every CTA scans the lengths in its ring stages (unless
     // the plan is already in the workspace)
     const size_t ring_bytes = size_t(p.nstages) * stage_bytes(hg, p.elem_bytes, MMA);
-    p.planned = a.decode_plan == kPlanned;
     p.plan_in_kernel = !p.planned && a.num_seqs <= kKernelPlanSeqs &&
                        size_t(a.num_seqs + 1 + 32) * 4 <= ring_bytes;
     if (!p.plan_in_kernel && !p.planned) {
