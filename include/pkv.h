@@ -59,8 +59,10 @@
  *
  *  Block tables.  int32 [num_seqs, max_blocks_per_seq]; row b lists the
  *  physical blocks of sequence b in logical order.  Entries at index
- *  >= ceil(seq_lens[b] / block_size) are never read (short rows may be
- *  padded with any value, e.g. a dummy block 0).  Several rows may name
+ *  >= ceil(seq_lens[b] / block_size) are never used as block ids (short
+ *  rows may be padded with any value, e.g. a dummy block 0; the decode
+ *  may load them along with the entries it uses, from within the
+ *  [num_seqs, max_blocks_per_seq] array).  Several rows may name
  *  the same block (shared prefix): it is read, never written, by attention.
  *
  *  Errors.  Argument checks run on the host before anything is enqueued;
@@ -468,7 +470,7 @@ pkv_status pkv_paged_attention_prefill(const void* q, const int32_t* cu_q_lens,
  * more scratch than the array holds returns PKV_ERR_WORKSPACE without
  * launching (a smaller max_ctas shrinks the need).
  */
-#define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define PKV_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 
 pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t num_seqs, int32_t n_heads,
                                               const void* k_pool, const void* v_pool,

@@ -532,10 +532,11 @@ __device__ __forceinline__ bool ring_fill(const Ring& r, uint32_t it, const uint
 // Producer side of a tile ring, one lane: wait for stage `it` to be free,
 // then load the K and V boxes at pool slot `slot` (a block's first token),
 // heads [head0, head0 + group) into it.  A slot past the pool's end reads
-// zeros.  Returns false if the wait timed out.
+// zeros.  `policy` (nonzero) is an L2 cache policy for the copied lines.
+// Returns false if the wait timed out.
 __device__ __forceinline__ bool tile_fill(const Ring& r, uint32_t it, const CUtensorMap* tm_k,
                                           const CUtensorMap* tm_v, int slot, int head0,
-                                          int32_t* err) {
+                                          int32_t* err, uint64_t policy = 0) {
   const int st = static_cast<int>(it % r.nstages);
   const uint32_t use = it / r.nstages;
   if (use > 0 && !mbar_wait(r.empty + st, (use - 1) & 1)) {
@@ -543,8 +544,13 @@ __device__ __forceinline__ bool tile_fill(const Ring& r, uint32_t it, const CUte
     return false;
   }
   mbar_arrive_expect_tx(r.full + st, static_cast<uint32_t>(r.stage_bytes));
-  tc::tma_load_4d(r.k_tile(st), tm_k, 0, slot, 0, head0, r.full + st);
-  tc::tma_load_4d(r.v_tile(st), tm_v, 0, slot, 0, head0, r.full + st);
+  if (policy != 0) {
+    tc::tma_load_4d_hint(r.k_tile(st), tm_k, 0, slot, 0, head0, r.full + st, policy);
+    tc::tma_load_4d_hint(r.v_tile(st), tm_v, 0, slot, 0, head0, r.full + st, policy);
+  } else {
+    tc::tma_load_4d(r.k_tile(st), tm_k, 0, slot, 0, head0, r.full + st);
+    tc::tma_load_4d(r.v_tile(st), tm_v, 0, slot, 0, head0, r.full + st);
+  }
   return true;
 }
 
@@ -896,27 +902,14 @@ struct Cursor {
 
 // Merge of split groups: out = sum_c w_c o_c / sum_c w_c over the CTAs c
 // that computed parts of one (sequence, head group), w_c = exp2(m_c - M) l_c.
-// One thread copies the parts' partial outputs (rows x head_dim fp32 each)
-// into shared memory with bulk copies, all in flight together, while the
-// CTA loads their max / sum pairs; parts are taken up to
-// merge_parts_per_round at a time with a running maximum, so any number
-// works.
+// Thread t owns J float4 pieces of the group's rows x head_dim outputs and
+// loads each part's pieces and the (max, exp-sum) of their rows straight
+// from L2 (the main kernel wrote them moments before and marks its K/V
+// stream to leave L2 first), 8 / J parts at a time with every load in
+// flight together, folding them in with a running maximum: any number of
+// parts in a few dependent round trips, no staging, no barrier.
 constexpr int kMergeThreads = 256;
-constexpr int kMergeMaxParts = 16;           // parts per round (one warp's ballot)
-// partial outputs staged per round; with the head this stays under 100 KB,
-// so a merge CTA fits on an SM beside a main-kernel CTA
-constexpr int kMergeSmemBudget = 96 * 1024;
-constexpr int kMergeVec = 8;  // float4 per thread: rows * head_dim <= 8192 = 256 x 8 x 4
-
-__host__ __device__ inline int merge_parts_per_round(int rows, int hd) {
-  const int n = kMergeSmemBudget / (rows * hd * 4);
-  return n < 1 ? 1 : (n > kMergeMaxParts ? kMergeMaxParts : n);
-}
-// Bytes of the merge CTA's shared memory before the staged partial outputs.
-__host__ __device__ inline int merge_head_bytes(int rows, int parts) {
-  const int b = 16 + (kMergeMaxParts + 1) * 4 + (2 * rows * parts + 3 * rows) * 4;
-  return (b + 127) / 128 * 128;
-}
+constexpr int kMergeMaxVec = 8;  // float4 per thread: rows * head_dim <= 8192 = 256 x 8 x 4
 
 // Largest decode CTA of an instantiation: one producer warp plus one warp
 // per KV head of the group (at most 8 heads, at most 1 KB of row data).
@@ -1014,13 +1007,14 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
       pre_id = lane < n0 ? __ldg(p.bt + int64_t(cur.b) * p.W + p.prefix_blocks + cur.j + lane) : 0;
       pre = true;
       if constexpr (MMA) {
+        const uint64_t pol = tc::l2_evict_first_policy();
         const int lim = min(min(n0, 32), min(p.nstages, cur.nblk - 1 - cur.j));
         for (; early < lim; ++early) {
           const int blk = __shfl_sync(0xffffffffu, pre_id, early);
           if (blk < 0 || blk >= p.num_blocks) break;  // the main loop reports it
           if (lane == 0)  // stage `early` is unused yet: no wait
             tile_fill(ring, static_cast<uint32_t>(early), tm_k, tm_v, blk * kBS,
-                      cur.grp * p.hg_size, p.err);
+                      cur.grp * p.hg_size, p.err, pol);
         }
       }
     }
@@ -1032,6 +1026,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
 
   if (warp == consumers) {
     // ------------------------------------------------------ producer
+    // each K/V block is read once per call: its lines leave L2 first
+    const uint64_t pol = MMA ? tc::l2_evict_first_policy() : 0;
     uint32_t it = static_cast<uint32_t>(early);  // blocks already issued before the wait
     int skip = early;
     bool ok = true;
@@ -1067,7 +1063,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
             // zeros past the pool's end); the consumers put the new row in
             filled = lane == 0 ? tile_fill(ring, it, tm_k, tm_v,
                                            valid > 0 ? blk * kBS : p.num_blocks * kBS,
-                                           cur.grp * p.hg_size, p.err)
+                                           cur.grp * p.hg_size, p.err, pol)
                                : true;
             filled = __shfl_sync(0xffffffffu, filled, 0);
           } else {
@@ -1246,19 +1242,30 @@ __device__ __forceinline__ void decode_cluster_body(const CUtensorMap* tm_k, con
   float* part_o = reinterpret_cast<float*>(smem + p.part_off);  // [rows_per_group][HD]
   float* part_ml = part_o + rows_per_group * HD;                // [rows_per_group][2]
 
-  // a planned call checks the kept plan (written by a finished launch) before
+  // A planned call checks the kept plan (written by a finished launch) before
   // anything else; every CTA of the cluster reads the same record, so all of
-  // them leave here together, before any cluster barrier
-  if (p.planned && !plan_matches(p, p.grid)) {
+  // them leave here together, before any cluster barrier.  Its lengths and
+  // tables are unchanged since the plan, so they are read in the same round
+  // trip; a call planning for itself reads them after the dependency wait.
+  if (!p.planned) pdl_wait();  // lengths and tables may come from the preceding kernel
+  const bool plan_ok = !p.planned || plan_matches(p, p.grid);
+  const int L = used_len(p, b);
+  // the producer holds the table row's first 64 entries (this path's
+  // sequences have at most 64 blocks; entries past the length are not used)
+  int ids[2] = {0, 0};
+  if (warp == consumers) {
+    const int32_t* trow = p.bt + int64_t(b) * p.W;
+    if (lane < p.W) ids[0] = __ldg(trow + lane);
+    if (lane + 32 < p.W) ids[1] = __ldg(trow + lane + 32);
+  }
+  if (!plan_ok) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(p.err, PKV_DEVERR_PLAN);
     return;
   }
-  if (!p.planned) pdl_wait();  // lengths and tables may come from the preceding kernel
   pdl_launch_dependents();
   if (!p.planned && blockIdx.x == 0 && threadIdx.x == 0)
     p.total_units[1] = -1;  // a call planning for itself replaces any kept plan
 
-  const int L = used_len(p, b);
   const int nblk = (L + kBS - 1) / kBS;
   const int j0 = static_cast<int>(int64_t(rank) * nblk / C);
   const int j1 = static_cast<int>(int64_t(rank + 1) * nblk / C);
@@ -1275,20 +1282,18 @@ __device__ __forceinline__ void decode_cluster_body(const CUtensorMap* tm_k, con
     // before it has finished (up to a ring's worth, never the sequence's
     // last block, the only one a decode step writes), then waits.
     bool waited = !p.planned;
+    const uint64_t pol = MMA ? tc::l2_evict_first_policy() : 0;  // K/V read once
     uint32_t it = 0;
     bool ok = true;
-    const int32_t* row = p.bt + int64_t(b) * p.W;
-    for (int jj = j0; jj < j1 && ok; jj += 32) {
-      const int id = jj + lane < j1 ? __ldg(row + jj + lane) : 0;
-      const int n_here = min(32, j1 - jj);
-      for (int k = 0; k < n_here; ++k) {
-        const int j = jj + k;
+    {
+      for (int j = j0; j < j1 && ok; ++j) {
+        const int jj = j & ~31, k = j & 31;  // the entry sits in lane k of ids[jj / 32]
         if (!waited && (!MMA || it >= static_cast<uint32_t>(p.nstages) || j == nblk - 1)) {
           pdl_wait();
           waited = true;
         }
         if (*ring.abort_flag) { ok = false; break; }
-        const int blk = __shfl_sync(0xffffffffu, id, k);
+        const int blk = __shfl_sync(0xffffffffu, ids[jj >> 5], k);
         int valid = min(kBS, L - j * kBS);
         if (blk < 0 || blk >= p.num_blocks) {
           if (lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
@@ -1302,7 +1307,7 @@ __device__ __forceinline__ void decode_cluster_body(const CUtensorMap* tm_k, con
         if constexpr (MMA) {
           filled = lane == 0 ? tile_fill(ring, it, tm_k, tm_v,
                                          valid > 0 ? blk * kBS : p.num_blocks * kBS,
-                                         grp * p.hg_size, p.err)
+                                         grp * p.hg_size, p.err, pol)
                              : true;
           filled = __shfl_sync(0xffffffffu, filled, 0);
         } else {
@@ -1391,26 +1396,28 @@ __device__ __forceinline__ void decode_cluster_body(const CUtensorMap* tm_k, con
   T* out = static_cast<T*>(p.out) + (int64_t(b) * p.n_heads + int64_t(grp) * rows_per_group) * HD;
   for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += static_cast<int>(blockDim.x)) {
     const int r = e / HD;
-    float mc[kMaxCluster], lc[kMaxCluster];
-    float M = -INFINITY;
+    float2 ml[kMaxCluster];
+    float oc[kMaxCluster];
 #pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) {
-      mc[c] = -INFINITY;
-      lc[c] = 0.f;
+    for (int c = 0; c < kMaxCluster; ++c) {  // every peer's values in one round trip
+      ml[c] = make_float2(-INFINITY, 0.f);
+      oc[c] = 0.f;
       if (c < C) {
-        const float2 ml = ld_cluster_f32x2(cluster_map(part_ml + r * 2, c));
-        mc[c] = ml.x;
-        lc[c] = ml.y;
-        if (ml.y > 0.f) M = fmaxf(M, ml.x);  // a part that saw no key has no weight
+        ml[c] = ld_cluster_f32x2(cluster_map(part_ml + r * 2, c));
+        oc[c] = ld_cluster_f32(cluster_map(part_o + e, c));
       }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c)
+      if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);  // a part that saw no key has no weight
     float acc = 0.f, den = 0.f;
 #pragma unroll
     for (int c = 0; c < kMaxCluster; ++c) {
-      if (c < C && lc[c] > 0.f) {
-        const float w = fast_exp2(mc[c] - M) * lc[c];
+      if (ml[c].y > 0.f) {
+        const float w = fast_exp2(ml[c].x - M) * ml[c].y;
         den += w;
-        acc = fmaf(w, ld_cluster_f32(cluster_map(part_o + e, c)), acc);
+        acc = fmaf(w, oc[c], acc);
       }
     }
     out[e] = Elem<T>::from_f(den > 0.f ? acc * (1.f / den) : 0.f);
@@ -1751,26 +1758,10 @@ inline int stages_for(int stage_bytes, int scratch_bytes, int target_bytes) {
 
 // Merge of the split groups, one CTA per main-kernel CTA: CTA c merges the
 // group main-kernel CTA c recorded, if any.  Launched as a programmatic
-// dependent of the main kernel.
-template <typename T, int HD>
+// dependent of the main kernel.  J = float4 pieces per thread.
+template <typename T, int HD, int J>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
-  extern __shared__ __align__(128) uint8_t merge_smem[];
-  const int t = threadIdx.x;
-  const int rows = p.hg_size * p.rep;
-  const int E = rows * HD;  // elements of one part
-  const int P = merge_parts_per_round(rows, HD);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(merge_smem);
-  int* slot_s = reinterpret_cast<int*>(merge_smem + 16);  // [kMergeMaxParts + 1]
-  float* m_s = reinterpret_cast<float*>(slot_s + kMergeMaxParts + 1);  // [rows][P]
-  float* w_s = m_s + rows * P;                                         // [rows][P]
-  float* M_s = w_s + rows * P;                                         // [rows]
-  float* den_s = M_s + rows;                                           // [rows]
-  float* alpha_s = den_s + rows;                                       // [rows]
-  float* o_s = reinterpret_cast<float*>(merge_smem + merge_head_bytes(rows, P));  // [P][E]
-  if (t == 0) {
-    mbar_init(bar, 1);
-    fence_barrier_init();
-  }
+  constexpr int NB = kMergeMaxVec / J;  // parts per batch
   pdl_launch_dependents();  // the next kernel's prologue may overlap this merge
   // the split group to merge: from the plan of a planned call (written by a
   // finished plan launch, so read before the wait: a CTA with nothing to
@@ -1784,112 +1775,95 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   pdl_wait();  // the main kernel's partials (and split entries)
   if (!p.planned) sp = __ldcg(p.splits + blockIdx.x);
   if (sp.x < 0) return;
+  const int t = threadIdx.x;
+  const int rows = p.hg_size * p.rep;
+  const int E = rows * HD;  // elements of one part
   const int grp = sp.y & 0xffff;
   const bool c0_tail = (sp.y & kSplitC0Tail) != 0;
   const bool dense = (sp.y & kSplitDense) != 0;
   const int U = dense ? 0 : __ldcg(p.total_units);  // only sparse grids look at range starts
   const int G = p.grid;
   const int c0 = sp.z & 0xffff, c1 = static_cast<int>(static_cast<uint32_t>(sp.z) >> 16);
-  float4 acc[kMergeVec];
+  float4 acc[J];
+  float M[J], den[J];
 #pragma unroll
-  for (int j = 0; j < kMergeVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int r = t; r < rows; r += kMergeThreads) {
-    M_s[r] = -INFINITY;
-    den_s[r] = 0.f;
+  for (int j = 0; j < J; ++j) {
+    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    M[j] = -INFINITY;
+    den[j] = 0.f;
   }
-  uint32_t phase = 0;
-  for (int cs = c0; cs <= c1; cs += P) {
-    __syncthreads();  // the previous round's reads of the staging area are done
-    if (t < 32) {     // slots of the parts of CTAs cs .. cs+P-1 whose range is not empty
-      const int c = cs + t;
-      bool has = t < P && c <= c1;
-      if (has && !dense) has = range_begin(c + 1, U, G) > range_begin(c, U, G);
-      const unsigned m = __ballot_sync(0xffffffffu, has);
-      // c0 holds the group's first units at the end of its range unless
-      // its range starts at the group (then they are its first segment)
-      if (has) slot_s[__popc(m & ((1u << t) - 1))] = (c == c0 && c0_tail) ? 2 * c + 1 : 2 * c;
-      if (t == 0) slot_s[kMergeMaxParts] = __popc(m);
-    }
-    __syncthreads();
-    const int np = slot_s[kMergeMaxParts];
-    if (np == 0) continue;
-    if (t == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np * E * 4));
-      for (int k = 0; k < np; ++k)
-        bulk_copy_g2s(o_s + k * E, p.ws_o + int64_t(slot_s[k]) * E, static_cast<uint32_t>(E * 4),
-                      bar);
-    }
-    for (int i = t; i < rows * np; i += kMergeThreads) {
-      const int r = i / np, k = i - r * np;
-      const int64_t prow = int64_t(slot_s[k]) * rows + r;
-      m_s[r * P + k] = __ldcg(p.ws_ml + prow * 2);
-      w_s[r * P + k] = __ldcg(p.ws_ml + prow * 2 + 1);
-    }
-    __syncthreads();
-    for (int r = t; r < rows; r += kMergeThreads) {
-      float cm = -INFINITY;
-      for (int k = 0; k < np; ++k) cm = fmaxf(cm, m_s[r * P + k]);
-      const float Mn = fmaxf(M_s[r], cm);  // finite: every part saw at least one key
-      const float alpha = fast_exp2(M_s[r] - Mn);
-      float den = den_s[r] * alpha;
-      for (int k = 0; k < np; ++k) {
-        const float w = fast_exp2(m_s[r * P + k] - Mn) * w_s[r * P + k];
-        w_s[r * P + k] = w;
-        den += w;
-      }
-      M_s[r] = Mn;
-      den_s[r] = den;
-      alpha_s[r] = alpha;
-    }
-    const bool ok = mbar_wait(bar, phase);
-    phase ^= 1u;
-    if (__syncthreads_or(!ok)) {  // copies did not land: report, let them finish, stop
-      if (t == 0) {
-        report(p.err, PKV_DEVERR_TIMEOUT);
-        mbar_wait(bar, phase ^ 1u);
-      }
-      return;
-    }
+  for (int cs = c0; cs <= c1; cs += NB) {
+    // the parts of CTAs cs .. cs + NB - 1 (those whose range is not empty);
+    // c0 holds the group's first units at the end of its range unless its
+    // range starts at the group (then they are its first segment)
+    int slot[NB];
+    bool has[NB];
 #pragma unroll
-    for (int j = 0; j < kMergeVec; ++j) {
+    for (int k = 0; k < NB; ++k) {
+      const int c = cs + k;
+      has[k] = c <= c1 && (dense || range_begin(c + 1, U, G) > range_begin(c, U, G));
+      slot[k] = (c == c0 && c0_tail) ? 2 * c + 1 : 2 * c;
+    }
+    float4 o[J][NB];
+    float2 ml[J][NB];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
       const int e = (t + j * kMergeThreads) * 4;
-      if (e < E) {
-        const int r = e / HD;
-        const float al = alpha_s[r];
-        float4 x = make_float4(acc[j].x * al, acc[j].y * al, acc[j].z * al, acc[j].w * al);
-        for (int k = 0; k < np; ++k) {
-          const float w = w_s[r * P + k];
-          const float4 o = *reinterpret_cast<const float4*>(o_s + k * E + e);
-          x.x = fmaf(w, o.x, x.x);
-          x.y = fmaf(w, o.y, x.y);
-          x.z = fmaf(w, o.z, x.z);
-          x.w = fmaf(w, o.w, x.w);
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        if (has[k] && e < E) {
+          o[j][k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + int64_t(slot[k]) * E + e));
+          ml[j][k] = __ldcg(reinterpret_cast<const float2*>(
+              p.ws_ml + (int64_t(slot[k]) * rows + e / HD) * 2));
+        } else {
+          o[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          ml[j][k] = make_float2(-INFINITY, 0.f);
         }
-        acc[j] = x;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        if (ml[j][k].y > 0.f) {  // a part that saw no key has no weight
+          const float Mn = fmaxf(M[j], ml[j][k].x);
+          const float a = fast_exp2(M[j] - Mn);
+          const float w = fast_exp2(ml[j][k].x - Mn) * ml[j][k].y;
+          acc[j] = make_float4(fmaf(w, o[j][k].x, acc[j].x * a), fmaf(w, o[j][k].y, acc[j].y * a),
+                               fmaf(w, o[j][k].z, acc[j].z * a), fmaf(w, o[j][k].w, acc[j].w * a));
+          den[j] = fmaf(den[j], a, w);
+          M[j] = Mn;
+        }
       }
     }
   }
-  __syncthreads();
   T* out = static_cast<T*>(p.out) + (int64_t(sp.x) * p.n_heads + grp * rows) * HD;
 #pragma unroll
-  for (int j = 0; j < kMergeVec; ++j) {
+  for (int j = 0; j < J; ++j) {
     const int e = (t + j * kMergeThreads) * 4;
     if (e < E) {
-      const float den = den_s[e / HD];
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      out[e + 0] = Elem<T>::from_f(acc[j].x * inv);
-      out[e + 1] = Elem<T>::from_f(acc[j].y * inv);
-      out[e + 2] = Elem<T>::from_f(acc[j].z * inv);
-      out[e + 3] = Elem<T>::from_f(acc[j].w * inv);
+      const float inv = den[j] > 0.f ? 1.f / den[j] : 0.f;
+      const float4 v = make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
+      if constexpr (std::is_same<T, float>::value) {
+        *reinterpret_cast<float4*>(out + e) = v;
+      } else {  // four bf16 in one 8-byte store
+        *reinterpret_cast<uint2*>(out + e) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+      }
     }
   }
 }
 
-// Shared memory of the merge kernel.
-inline size_t merge_smem_bytes(int rows, int hd) {
-  const int P = merge_parts_per_round(rows, hd);
-  return size_t(merge_head_bytes(rows, P)) + size_t(P) * rows * hd * 4;
+// Launch the merge with the fewest float4 pieces per thread that covers a
+// part of rows x HD elements (more parts per batch for small parts).
+template <typename T, int HD>
+cudaError_t launch_merge(cudaLaunchConfig_t cfg, const DecodeParams& p) {
+  const int pieces = (p.hg_size * p.rep * HD / 4 + kMergeThreads - 1) / kMergeThreads;
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  if (pieces <= 1) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, HD, 1>, p);
+  if (pieces <= 2) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, HD, 2>, p);
+  if (pieces <= 4) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, HD, 4>, p);
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, HD, 8>, p);
 }
 
 // Runs the shared prefix is cut into for the prefix kernel: enough CTAs
@@ -1946,13 +1920,25 @@ struct DecodeLaunch {
     const int row_bytes = hg * HD * elem_bytes;
     return tiles ? 2 * kBS * row_bytes : 2 * kBS * (row_bytes + 16);
   }
+  // Ring depth: the tile path keeps five 32 KB stages per CTA at one CTA
+  // per SM (160 KB in flight per SM; measured against 3, 4 and 6 stages on
+  // the 1B, 7B and 70B shapes, five was best or tied on each, and a deeper
+  // ring also holds more of a planned call's early loads); the CUDA-core
+  // path keeps about 110 KB.
   static size_t smem_bytes(int hg, int elem_bytes, int* nstages) {
     const int padded = stage_bytes(hg, elem_bytes, false);
     const size_t scratch = scratch_bytes(hg);
-    *nstages = stages_for(padded, static_cast<int>(scratch), 110 * 1024);
-    size_t bytes = kBarrierBytes + size_t(*nstages) * padded + scratch;
-    if (MMA)  // tile ring: 1024 bytes of alignment slack after the barriers
-      bytes = std::max(bytes, kBarrierBytes + 1024 + size_t(*nstages) * stage_bytes(hg, elem_bytes, true));
+    *nstages = stages_for(padded, static_cast<int>(scratch), (MMA ? 180 : 110) * 1024);
+    return smem_for(hg, elem_bytes, *nstages);
+  }
+  // Shared memory of a ring of `nstages` stages (plus the CUDA-core rows'
+  // scratch; the tile ring needs 1024 bytes of alignment slack after the
+  // barriers).
+  static size_t smem_for(int hg, int elem_bytes, int nstages) {
+    size_t bytes = kBarrierBytes + size_t(nstages) * stage_bytes(hg, elem_bytes, false) +
+                   scratch_bytes(hg);
+    if (MMA)
+      bytes = std::max(bytes, kBarrierBytes + 1024 + size_t(nstages) * stage_bytes(hg, elem_bytes, true));
     return bytes;
   }
   static auto main_kernel() {
@@ -2079,6 +2065,11 @@ struct DecodeLaunch {
       // latency-bound batch: one cluster of C CTAs per (sequence, head
       // group), partials combined in distributed shared memory
       p.cluster = C;
+      // a CTA walks at most ceil(blocks / C) <= 8 blocks: a ring that holds
+      // them all (at least 2 stages), so several CTAs fit on an SM
+      const int nmax = (min(a.max_seq_len, a.max_blocks_per_seq * kBS) + kBS - 1) / kBS;
+      p.nstages = std::max(2, std::min(p.nstages, (nmax + C - 1) / C));
+      smem = smem_for(hg, p.elem_bytes, p.nstages);
       p.part_off = static_cast<int>((smem + 15) / 16 * 16);
       const size_t csmem = size_t(p.part_off) + size_t(hg) * p.rep * (HD + 2) * 4;
       static KernelSetup cluster_setup;
@@ -2153,15 +2144,8 @@ struct DecodeLaunch {
       e = cudaLaunchKernelEx(&cfg, decode_rows_kernel<T, HD, MAXR>, p);
     if (e != cudaSuccess) return e;
     // split groups: one small CTA per main-kernel boundary, most exit at once
-    const size_t msmem = merge_smem_bytes(hg * p.rep, HD);
-    static KernelSetup merge_setup;
-    e = kernel_setup(merge_setup, decode_merge_kernel<T, HD>, static_cast<int>(msmem),
-                     kMergeThreads, nullptr);
-    if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(G);
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.dynamicSmemBytes = msmem;
-    e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, HD>, p);
+    e = launch_merge<T, HD>(cfg, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }

@@ -13,7 +13,7 @@
 // fixed array compiled into the library.
 //
 // The array is a file-scope __device__ variable of
-// PKV_NOALLOC_SCRATCH_BYTES (16 MiB).  Every GPU that loads the library
+// PKV_NOALLOC_SCRATCH_BYTES (8 MiB).  Every GPU that loads the library
 // holds one copy of it from module load until the process exits.  In host
 // code its name only stands in for the symbol; it is not a device address
 // (passing it to a kernel would fault, or silently use the wrong memory

@@ -36,6 +36,27 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// An L2 cache policy that evicts the lines it is applied to first: for
+// data streamed once (a decode call reads each K/V block once), so the
+// stream does not push out what the same call reads again soon (split
+// partials, queries, block tables).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// tma_load_4d with an L2 cache policy for the copied lines.
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* map, int x, int y,
+                                                 int z, int w, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar)),
+      "l"(policy)
+      : "memory");
+}
+
 // --------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile

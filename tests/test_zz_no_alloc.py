@@ -71,9 +71,10 @@ def test_noalloc_decode_matches_workspace_decode(name):
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
     """16 query heads per KV head at head_dim 128 need more split scratch
-    than the built-in array holds on a full grid (the batch has more units
-    than the grid has CTAs, so the grid is full): refused, nothing
-    launched; a smaller grid fits and matches the workspace entry point."""
+    than the built-in 8 MiB holds on a full grid (about 10 MB at one CTA
+    per SM on 152 SMs; the batch has more units than the grid has CTAs, so
+    the grid is full): refused, nothing launched; a 64-CTA grid fits and
+    matches the workspace entry point."""
     plan = tiny_plan([300, 9, 1000, 2000, 2000], [1] * 5, n_heads=64, n_kv=4, head_dim=128,
                      block_size=16, num_blocks=400, dtype="bf16", seed=5)
     layer = make_tiny_layer(plan, seed=5)
