@@ -71,13 +71,18 @@ PER_CONFIG = ("toy", "smollm2-135m", "llama-3.2-1b", "llama-7b", "llama2-70b-mix
 L2_BYTES = 126 * 2 ** 20
 # Sources of the decode kernels; the traffic ratios below are valid only for
 # the sources whose hash they carry.
-DECODE_SOURCES = ("attention.cuh", "device.cuh", "decode.cu", "decode_mma64.cu")
+DECODE_SOURCES = ("attention.cuh", "device.cuh", "tcgen05.cuh", "decode.cu", "decode_mma64.cu")
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic
 # byte of the fused write + decode call, from one ncu capture of the shape
 # named in "capture", keyed by (dtype, n_heads, n_kv, head_dim), valid for
 # the decode sources with the given hash only (a different hash reports
 # traffic null; tests/test_bench_host.py fails while a recorded hash is stale).
-DECODE_TRAFFIC: dict = {}
+DECODE_TRAFFIC: dict = {
+    ("bf16", 64, 8, 128): {"ratio": 1.0141, "source_sha256": "89f0995c637db2e0",
+                           "capture": "llama2-70b-decode64, decode + merge, 2 calls"},
+    ("bf16", 32, 8, 64): {"ratio": 1.0164, "source_sha256": "89f0995c637db2e0",
+                          "capture": "llama-3.2-1b (2 layers), decode + merge, 4 calls"},
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit -> name
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
