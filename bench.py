@@ -78,9 +78,9 @@ DECODE_SOURCES = ("attention.cuh", "device.cuh", "tcgen05.cuh", "decode.cu", "de
 # the decode sources with the given hash only (a different hash reports
 # traffic null; tests/test_bench_host.py fails while a recorded hash is stale).
 DECODE_TRAFFIC: dict = {
-    ("bf16", 64, 8, 128): {"ratio": 1.0141, "source_sha256": "89f0995c637db2e0",
+    ("bf16", 64, 8, 128): {"ratio": 1.0145, "source_sha256": "6590b8ac39a4cff9",
                            "capture": "llama2-70b-decode64, decode + merge, 2 calls"},
-    ("bf16", 32, 8, 64): {"ratio": 1.0164, "source_sha256": "89f0995c637db2e0",
+    ("bf16", 32, 8, 64): {"ratio": 1.0164, "source_sha256": "6590b8ac39a4cff9",
                           "capture": "llama-3.2-1b (2 layers), decode + merge, 4 calls"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -564,7 +564,7 @@ class DecodeCalls:
 
 
 def per_config_entry(torch, pkv, dev, stream, local, name, args, hbm, peak_src, layers=None,
-                     layers_cpu0=None, plan=None):
+                     layers_cpu0=None, plan=None, shared_prefix=False):
     """The decode call of one workload shape, as its step makes it: every
     layer's call (work split planned once when there are several layers,
     the step's K/V write fused in) replayed as one CUDA graph at least
@@ -581,7 +581,7 @@ def per_config_entry(torch, pkv, dev, stream, local, name, args, hbm, peak_src, 
         layers_cpu0 = make_layer(plan, 0)
         layers = [{n: t.to(dev) for n, t in layers_cpu0.items()}]
         layers += [make_layer_on_device(plan, li, dev) for li in range(1, n_layers)]
-    dc = DecodeCalls(pkv, torch, plan, layers, dev)
+    dc = DecodeCalls(pkv, torch, plan, layers, dev, shared_prefix=shared_prefix)
     acc = step_accounting(plan)
     per_layer_bytes = acc["decode_bytes"] + (acc["append_bytes"] if dc.fused else 0)
     replay_bytes = per_layer_bytes * len(layers)
@@ -607,7 +607,9 @@ def per_config_entry(torch, pkv, dev, stream, local, name, args, hbm, peak_src, 
         "layers_model": sh.layers, "decode_seqs": int(plan.n_decode),
         "call": ("decode_plan once per step + paged_attention_decode_planned with k_new/v_new "
                  "per layer" if dc.planned else
-                 "paged_attention_decode_append (work split planned inside the call)"),
+                 "paged_attention_decode_append (work split planned inside the call)")
+                + (f", shared prefix of {dc.P} blocks read once per chunk of sequences"
+                   if dc.P else ""),
         "algorithmic_bytes_per_layer": int(per_layer_bytes),
         "kv_bytes_per_layer": int(acc["decode_kv_bytes"]),
         "ms_per_layer": layer_ms, "replay_ms": s, "gbs": gbs, "peak": hbm,
@@ -887,6 +889,14 @@ def run_gb300(args, rank, world, local):
                 ent = per_config_entry(torch, pkv, dev, stream, local, name, args, hbm, src)
             per_config[name] = ent
             torch.cuda.empty_cache()
+    # ---- shared-prefix decode: 64 Llama-3.2-1B users behind one 1,024-token
+    # prompt, the prompt's blocks counted once in the algorithmic bytes
+    shared_prefix = None
+    if rank == 0 and not args.no_per_config and "llama-3.2-1b" in args.per_config.split(","):
+        shared_prefix = per_config_entry(torch, pkv, dev, stream, local,
+                                         "llama-3.2-1b-sharedprompt", args, hbm, src,
+                                         shared_prefix=True)
+        torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -990,6 +1000,7 @@ def run_gb300(args, rank, world, local):
         "prefill_tokens_per_s": pre_tok_s,
         "roofline": roof or pre_roof, "prefill_roofline": pre_roof,
         "per_config": per_config,
+        "decode_shared_prefix": shared_prefix,
         "cpu_baseline": cpu, "cpu_pages_method": pages_cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),

@@ -71,6 +71,14 @@ struct MmaRows {
   float o[HD / 8][4];
   float m[2], l[2];
   int last[2];
+  int slot[2];  // with several sequences' rows in the tile: the sequence of each row
+
+  // Rows r hold sequence r / rep (see block_sw's `only`).
+  __device__ __forceinline__ void set_row_slots(int rep) {
+    const int g = (threadIdx.x & 31) >> 2;
+    slot[0] = g / rep;
+    slot[1] = (g + 8) / rep;
+  }
 
   // q_row(r) -> pointer to row r's query (nullptr = inactive row),
   // last_key(r) -> last key position the row may see.
@@ -133,7 +141,7 @@ struct MmaRows {
     const uint8_t* kaddr = k_tile + ((mi >> 1) * 8 + ri) * stride + (mi & 1) * 16;
     const uint8_t* vaddr = v_tile + ((mi & 1) * 8 + ri) * stride + (mi >> 1) * 16;
     block_from([&](int kk) { return kaddr + kk * 32; }, [&](int dp) { return vaddr + dp * 32; },
-               j0, scale_log2);
+               j0, scale_log2, last);
   }
 
   // One 16-token block from TMA tiles in the 128-byte-swizzled layout: rows
@@ -141,17 +149,21 @@ struct MmaRows {
   // token t, dims [d, d + 64) of the group's head h; within a row the
   // 16-byte piece c sits at position c ^ (row % 8).  `head` is this warp's
   // head within the group.
+  // `only` >= 0: the block belongs to sequence `only` of the tile's rows
+  // (set_row_slots): the other rows see none of it.
   __device__ __forceinline__ void block_sw(const uint8_t* k_tile, const uint8_t* v_tile, int head,
-                                           int j0, float scale_log2) {
+                                           int j0, float scale_log2, int only = -1) {
     const int lane = threadIdx.x & 31;
     const int mi = lane >> 3, ri = lane & 7;
     const int hrow = head * (HD / 64) * kBS;
     const uint8_t* kaddr = k_tile + (hrow + (mi >> 1) * 8 + ri) * 128;
     const uint8_t* vaddr = v_tile + (hrow + (mi & 1) * 8 + ri) * 128;
     const int kx = (mi & 1) ^ ri, vx = (mi >> 1) ^ ri;
+    const int lim[2] = {only < 0 || slot[0] == only ? last[0] : -1,
+                        only < 0 || slot[1] == only ? last[1] : -1};
     block_from([&](int kk) { return kaddr + (kk >> 2) * (kBS * 128) + ((((kk & 3) * 2) ^ kx) << 4); },
                [&](int dp) { return vaddr + (dp >> 2) * (kBS * 128) + ((((dp & 3) * 2) ^ vx) << 4); },
-               j0, scale_log2);
+               j0, scale_log2, lim);
   }
 
   // kaddr(kk): this lane's ldmatrix row address for the K matrices of dims
@@ -159,7 +171,8 @@ struct MmaRows {
   // hi); vaddr(dp): the same for V, matrices tokens 0-7 | 8-15 (fast) x
   // dims lo | hi.
   template <typename KAddr, typename VAddr>
-  __device__ __forceinline__ void block_from(KAddr kaddr, VAddr vaddr, int j0, float scale_log2) {
+  __device__ __forceinline__ void block_from(KAddr kaddr, VAddr vaddr, int j0, float scale_log2,
+                                             const int (&lim)[2]) {
     const int lane = threadIdx.x & 31;
     const int c = lane & 3;
     float s[2][4];
@@ -182,7 +195,7 @@ struct MmaRows {
         const int h = e >> 1;
         const int pos = j0 + nt * 8 + 2 * c + (e & 1);
         const float x = s[nt][e] * scale_log2;
-        s[nt][e] = (pos <= last[h]) ? x : -INFINITY;
+        s[nt][e] = (pos <= lim[h]) ? x : -INFINITY;
         mx[h] = fmaxf(mx[h], s[nt][e]);
       }
     float alpha[2], mref[2];
@@ -664,9 +677,10 @@ struct DecodeParams {
   // 1 (main kernel): the plan is in the workspace from a finished plan-only
   // launch, so it and the tables are read before the dependency wait
   int planned;
-  // cluster decode: CTAs per (sequence, head group) cluster (0: stream-K
-  // path) and the byte offset of the partial results in shared memory
-  int cluster, part_off;
+  // cluster decode: CTAs per cluster (0: stream-K path), sequences per
+  // cluster (their rows per warp: cluster_seqs * rep), and the byte offset
+  // of the partial results in shared memory
+  int cluster, cluster_seqs, part_off;
   float scale_log2;
 };
 
@@ -1206,22 +1220,44 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) decode_rows_kerne
 
 // ------------------------------------------------------- cluster decode
 //
-// Latency-bound batches (few sequences of at most a few hundred tokens,
-// where the stream-K split would leave each CTA a handful of blocks and the
-// merge launch would cost as much as the reads): one thread-block cluster
-// of C CTAs per (sequence, KV-head group).  CTA r walks blocks
-// [r n / C, (r + 1) n / C) of the sequence's n blocks (split points depend
-// only on the length and C, so placement and sharing of blocks change no
+// Latency-bound batches (few, short sequences, where the stream-K split
+// would leave each CTA a handful of blocks and the merge launch would cost
+// as much as the reads) and shared prompt prefixes: one thread-block
+// cluster of C CTAs per chunk of `spc` sequences and KV-head group.  The
+// chunk's rows share one tensor-core tile (spc * rep <= 16 rows: row r is
+// query head r % rep of sequence r / rep).  The cluster's block list is
+// the shared prefix's blocks (every chunk row attends; keys past a row's
+// own length are masked), then, sequence by sequence, each sequence's
+// blocks after the prefix (only that sequence's rows attend): the prefix
+// is read once per chunk instead of once per sequence.  Without a prefix
+// and with one sequence per cluster this is plain split decode.  CTA r
+// walks list positions [r n / C, (r + 1) n / C) (split points depend only
+// on the lengths, C and spc, so placement and sharing of blocks change no
 // bit), leaves its normalised partial (output rows, max, exp-sum) in its
 // own shared memory, and after a cluster barrier the C CTAs combine the
 // partials through distributed shared memory, each CTA a slice of the
 // output elements, with log-sum-exp weights.  A second barrier keeps every
 // CTA's shared memory alive until its peers have read it.  Every thread of
 // the cluster reaches both barriers (waits in the loops are bounded; an
-// aborted CTA still leaves a partial).  Nothing goes through global
-// memory but the inputs and the output: no workspace, no merge launch.
+// aborted CTA still leaves a partial).  Nothing goes through global memory
+// but the inputs and the output: no workspace, no merge launch.
 constexpr int kMaxCluster = 8;
+constexpr int kMaxChunk = 16;  // sequences per cluster (tile rows at one query head per KV head)
 
+// Shared-memory bytes of the cluster kernel's partials and staged new rows
+// beyond its ring: spc * rep rows per consumer warp.  Kept small so that
+// the next call's CTAs fit beside the running ones (programmatic launch
+// lets them enter early and set up while this call finishes).
+inline size_t cluster_extra_bytes(int hg, int rep, int hd, int elem_bytes, int spc, bool append) {
+  const size_t rows = size_t(hg) * spc * rep;
+  return rows * hd * 4 + (rows * 2 * 4 + 15) / 16 * 16 +  // outputs; (max, sum) pairs, padded
+         (append ? size_t(spc) * 2 * hg * hd * elem_bytes : 0);  // staged step rows
+}
+
+// Plain split decode of latency-bound batches (no shared prefix): one
+// cluster per (sequence, KV-head group), as above with spc = 1; a leaner
+// body than the prefix one below (no list, no staging), so that the next
+// call's CTAs fit beside it and the set-up stays one round trip.
 template <typename T, int HD, int MAXR, bool MMA>
 __device__ __forceinline__ void decode_cluster_body(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                                     const DecodeParams& p) {
@@ -1425,6 +1461,359 @@ __device__ __forceinline__ void decode_cluster_body(const CUtensorMap* tm_k, con
   cluster_sync();  // the peers have read this CTA's partials
 }
 
+template <typename T, int HD, int MAXR, bool MMA>
+__device__ __forceinline__ void decode_cluster_prefix_body(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                                    const DecodeParams& p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using Rows = typename RowsOf<T, HD, MAXR, MMA>::type;
+  const int consumers = p.hg_size;
+  const int row_bytes = p.hg_size * HD * p.elem_bytes;  // the group's heads of one token
+  Ring ring = MMA ? make_tile_ring(smem, p.nstages, kBS * row_bytes)
+                  : make_ring(smem, p.nstages, row_bytes);
+  uint64_t* fresh_bar = reinterpret_cast<uint64_t*>(smem + 768);  // past the ring's barriers
+  if (threadIdx.x == 0) mbar_init(fresh_bar, 1);
+  ring_init(ring, consumers);  // (its barrier also publishes fresh_bar's init)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = p.cluster;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int seg = static_cast<int>(blockIdx.x) / C;  // (chunk of sequences, head group)
+  const int chunk = seg / p.n_groups;
+  const int grp = seg - chunk * p.n_groups;
+  const int spc = p.cluster_seqs;
+  const int s0 = chunk * spc;
+  const int ns = min(spc, p.B - s0);  // sequences of this chunk
+  const int P = p.prefix_blocks;
+  const bool plain = spc == 1 && P == 0;
+  const int PR = spc * p.rep;  // partial rows per consumer warp (<= R)
+  float* part_o = reinterpret_cast<float*>(smem + p.part_off);  // [consumers][PR][HD]
+  float* part_ml = part_o + consumers * PR * HD;                // [consumers][PR][2]
+  // staged step rows [spc][K|V][row_bytes]: bulk-copy destinations, so on a
+  // 16-byte boundary after the (max, sum) pairs
+  uint8_t* fresh = reinterpret_cast<uint8_t*>(part_ml) + (consumers * PR * 2 * 4 + 15) / 16 * 16;
+  __shared__ int len_s[kMaxChunk];      // used length of each chunk sequence
+  __shared__ int cum_s[kMaxChunk + 1];  // list position where each sequence's own blocks start
+  __shared__ int app_s[kMaxChunk];      // 1: the sequence's step row is appended (k_new given,
+                                        // a length not clamped, the token past the prefix)
+  __shared__ int fresh_s[kMaxChunk];    // set by the producer with the sequence's last tile:
+                                        // 1 if its step row goes into that tile
+
+  // A planned call checks the kept plan (written by a finished launch) before
+  // anything else; every CTA of the cluster reads the same record, so all of
+  // them leave here together, before any cluster barrier.  Its lengths and
+  // tables are unchanged since the plan, so they are read in the same round
+  // trip; a call planning for itself reads them after the dependency wait.
+  if (!p.planned) pdl_wait();  // lengths and tables may come from the preceding kernel
+  const bool plan_ok = !p.planned || plan_matches(p, p.grid);
+  if (threadIdx.x < kMaxChunk) {
+    const int t = threadIdx.x;
+    const int raw = t < ns ? __ldg(p.seq_lens + s0 + t) : 0;
+    const int L = raw < 0 ? 0 : (raw > p.max_len ? p.max_len : raw);  // as used_len
+    len_s[t] = L;
+    app_s[t] = p.k_new != nullptr && raw == L && L > P * kBS;
+    fresh_s[t] = 0;
+    // bad lengths (as check_length; a planned call's plan reported them),
+    // once, by the group-0 CTAs of rank 0
+    if (t < ns && !p.planned && grp == 0 && cluster_ctarank() == 0) {
+      if (raw < 0 || raw > p.max_seq_len) report(p.err, PKV_DEVERR_LENGTH);
+      else if (raw > p.W * kBS) report(p.err, PKV_DEVERR_TABLE_WIDTH);
+    }
+    // with append, a new token inside the shared prefix would land in a
+    // block other sequences read: not written, reported
+    if (t < ns && p.k_new != nullptr && P > 0 && L > 0 && L <= P * kBS && grp == 0 &&
+        cluster_ctarank() == 0)
+      report(p.err, PKV_DEVERR_PREFIX);
+  }
+  // plain split decode: the producer holds the table row's first 64 entries
+  // (this path's sequences have at most 64 blocks; entries past the length
+  // are not used), loaded with the length
+  int ids_pre[2] = {0, 0};
+  if (plain && warp == consumers) {
+    const int32_t* trow = p.bt + int64_t(s0) * p.W;
+    if (lane < p.W) ids_pre[0] = __ldg(trow + lane);
+    if (lane + 32 < p.W) ids_pre[1] = __ldg(trow + lane + 32);
+  }
+  __syncthreads();
+  if (!plan_ok) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(p.err, PKV_DEVERR_PLAN);
+    return;
+  }
+  pdl_launch_dependents();
+  if (!p.planned && blockIdx.x == 0 && threadIdx.x == 0)
+    p.total_units[1] = -1;  // a call planning for itself replaces any kept plan
+  // the list: prefix positions [0, Pe) (as far as any chunk sequence sees),
+  // then sequence s's own blocks from cum_s[s]
+  int vis = 0;  // positions of the prefix some chunk sequence sees
+  for (int s = 0; s < ns; ++s) vis = max(vis, min(len_s[s], P * kBS));
+  const int Pe = (vis + kBS - 1) / kBS;
+  if (threadIdx.x == 0) {
+    int c = Pe;
+    for (int s = 0; s < ns; ++s) {
+      cum_s[s] = c;
+      c += max(0, (len_s[s] + kBS - 1) / kBS - P);
+    }
+    cum_s[ns] = c;
+  }
+  __syncthreads();
+  const int n = cum_s[ns];
+  const int j0 = static_cast<int>(int64_t(rank) * n / C);
+  const int j1 = static_cast<int>(int64_t(rank + 1) * n / C);
+  const int64_t token_pitch = int64_t(p.n_kv) * HD * p.elem_bytes;
+  const int64_t head_off = int64_t(grp) * p.hg_size * HD * p.elem_bytes;
+  // list position -> (chunk sequence or -1 for the prefix, table index)
+  auto locate = [&](int t, int& sq, int& j) {
+    if (t < Pe) {
+      sq = -1;
+      j = t;
+    } else {
+      sq = 0;
+      while (sq + 1 < ns && cum_s[sq + 1] <= t) ++sq;
+      j = P + (t - cum_s[sq]);
+    }
+  };
+  // append: sequence s's step row is stored and used by the CTA holding its
+  // last block (a length clamped from a bad value, or a token inside the
+  // shared prefix, gets none)
+  auto appends = [&](int sq) { return app_s[sq] != 0; };
+
+  if (warp == consumers) {
+    // ------------------------------------------------------ producer
+    // A planned call loads its first blocks before the kernel launched just
+    // before it has finished (up to a ring's worth, never a sequence's last
+    // block, the only one a decode step writes), then waits.
+    bool waited = !p.planned;
+    const uint64_t pol = MMA ? tc::l2_evict_first_policy() : 0;  // K/V read once
+    // The step rows this CTA's tiles need (tile path, append), staged once
+    // for the consumers to patch into the tiles.  k_new / v_new may come
+    // from the preceding kernel: staged right after the dependency wait.
+    // (with one sequence per cluster the consumers load the row themselves)
+    const bool stage = MMA && p.k_new != nullptr && spc > 1;
+    auto stage_fresh = [&]() {
+      if (lane != 0) return;
+      uint32_t bytes = 0;
+      for (int sq = 0; sq < ns; ++sq) {
+        const int last_t = cum_s[sq + 1] - 1;
+        if (cum_s[sq + 1] > cum_s[sq] && last_t >= j0 && last_t < j1 && appends(sq)) bytes += 2 * row_bytes;
+      }
+      mbar_arrive_expect_tx(fresh_bar, bytes);
+      for (int sq = 0; sq < ns; ++sq) {
+        const int last_t = cum_s[sq + 1] - 1;
+        if (cum_s[sq + 1] > cum_s[sq] && last_t >= j0 && last_t < j1 && appends(sq)) {
+          const int64_t src = int64_t(s0 + sq) * p.n_kv * HD * p.elem_bytes + head_off;
+          bulk_copy_g2s(fresh + (2 * sq) * row_bytes, p.k_new + src, row_bytes, fresh_bar);
+          bulk_copy_g2s(fresh + (2 * sq + 1) * row_bytes, p.v_new + src, row_bytes, fresh_bar);
+        }
+      }
+    };
+    if (stage && waited) stage_fresh();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t0 = j0; t0 < j1 && ok; t0 += 32) {
+      int my_s = -1, my_j = 0, my_id = 0;
+      if (t0 + lane < j1) {
+        locate(t0 + lane, my_s, my_j);
+        if (!plain) my_id = __ldg(p.bt + int64_t(my_s < 0 ? 0 : s0 + my_s) * p.W + my_j);
+      }
+      const int n_here = min(32, j1 - t0);
+      for (int k = 0; k < n_here && ok; ++k) {
+        const int t = t0 + k;
+        const int sq = __shfl_sync(0xffffffffu, my_s, k);
+        const int j = __shfl_sync(0xffffffffu, my_j, k);
+        const int blk = plain ? __shfl_sync(0xffffffffu, ids_pre[t >> 5], t & 31)
+                              : __shfl_sync(0xffffffffu, my_id, k);
+        const int L = sq < 0 ? vis : len_s[sq];
+        const bool last_blk = sq >= 0 && t == cum_s[sq + 1] - 1;
+        if (!waited && (!MMA || it >= static_cast<uint32_t>(p.nstages) || last_blk)) {
+          pdl_wait();
+          waited = true;
+          if (stage) stage_fresh();
+        }
+        if (*ring.abort_flag) { ok = false; break; }
+        int valid = min(kBS, L - j * kBS);
+        if (blk < 0 || blk >= p.num_blocks) {
+          if (lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
+          valid = 0;
+        }
+        const int64_t off = int64_t(valid > 0 ? blk : 0) * kBS * token_pitch + head_off;
+        const bool fresh_row = last_blk && valid > 0 && appends(sq);
+        const int new_row = fresh_row ? L - 1 - j * kBS : -1;
+        // for the consumers, published by the tile's arrival (release / acquire)
+        if (last_blk && lane == 0) fresh_s[sq] = fresh_row ? 1 : 0;
+        const int64_t new_off = int64_t(s0 + (sq < 0 ? 0 : sq)) * p.n_kv * HD * p.elem_bytes + head_off;
+        bool filled;
+        if constexpr (MMA) {
+          // prefix blocks are read by every chunk's cluster: no evict-first
+          filled = lane == 0 ? tile_fill(ring, it, tm_k, tm_v,
+                                         valid > 0 ? blk * kBS : p.num_blocks * kBS,
+                                         grp * p.hg_size, p.err, sq < 0 ? 0 : pol)
+                             : true;
+          filled = __shfl_sync(0xffffffffu, filled, 0);
+        } else {
+          filled = ring_fill(ring, it, p.k_pool + off, p.v_pool + off, token_pitch, valid, p.err,
+                             new_row, p.k_new + new_off, p.v_new + new_off);
+        }
+        if (!filled) {
+          *ring.abort_flag = 1;
+          ok = false;
+          break;
+        }
+        ++it;
+        if (fresh_row) {  // the pool's copy of the step's row (this group's heads)
+          const int nvec = row_bytes / 16;
+          const int64_t dst = off + int64_t(new_row) * token_pitch;
+          for (int i = lane; i < 2 * nvec; i += 32) {
+            const bool is_v = i >= nvec;
+            const int64_t o = int64_t(is_v ? i - nvec : i) * 16;
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) +
+                                                                 new_off + o));
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(is_v ? p.v_pool : p.k_pool) + dst + o) = x;
+          }
+        }
+      }
+    }
+    if (!ok) ring_drain(ring, it);
+    if (stage) {
+      if (!waited) {  // every block was loaded early: stage now (nothing here needs it)
+        pdl_wait();
+        waited = true;
+        stage_fresh();
+      }
+      if (lane == 0) mbar_wait(fresh_bar, 0);  // staged rows land before the CTA can exit
+    }
+    // the prefix blocks this CTA read: every chunk sequence that reaches one
+    // must name it where row 0 does (checked off the loading path)
+    const int pe1 = min(j1, Pe);
+    for (int idx = lane; idx < ns * max(0, pe1 - j0); idx += 32) {
+      const int sq = idx / (pe1 - j0), j = j0 + idx - sq * (pe1 - j0);
+      if (len_s[sq] > j * kBS && __ldg(p.bt + int64_t(s0 + sq) * p.W + j) != __ldg(p.bt + j))
+        report(p.err, PKV_DEVERR_PREFIX);
+    }
+  } else if (warp < consumers) {
+    // ------------------------------------------------------ consumers
+    Rows rows;
+    if constexpr (MMA) rows.set_row_slots(p.rep);
+    if constexpr (!MMA) {
+      float* scratch = reinterpret_cast<float*>(ring.stages + p.nstages * ring.stage_bytes);
+      rows.bind(scratch + warp * RowsOf<T, HD, MAXR, MMA>::kScratch);
+    }
+    if (p.planned) pdl_wait();  // the queries may come from the preceding kernel
+    const T* q = static_cast<const T*>(p.q);
+    const int kv_head = grp * p.hg_size + warp;
+    const int head0 = kv_head * p.rep;
+    const int nrows = ns * p.rep;
+    rows.begin(
+        [&](int r) -> const T* {
+          return r < nrows ? q + (int64_t(s0 + r / p.rep) * p.n_heads + head0 + r % p.rep) * HD
+                           : nullptr;
+        },
+        [&](int r) { return len_s[r / p.rep] - 1; });
+    // one sequence per cluster: its step row, loaded with the queries when
+    // this CTA holds the sequence's last block (used if the producer finds
+    // that block's id valid)
+    uint32_t kn1[2] = {0u, 0u}, vn1[2] = {0u, 0u};
+    if constexpr (MMA) {
+      if (spc == 1 && app_s[0] && j1 == n && n > cum_s[0])
+        new_row_piece<HD>(p.k_new, p.v_new, (int64_t(s0) * p.n_kv + kv_head) * HD, kn1, vn1);
+    }
+    bool fresh_ready = false;
+    uint32_t it = 0;
+    for (int t = j0; t < j1; ++t, ++it) {
+      if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
+        *ring.abort_flag = 1;
+        break;
+      }
+      int sq, j;
+      locate(t, sq, j);
+      const int st = static_cast<int>(it % ring.nstages);
+      const int jpos = j * kBS;
+      if constexpr (MMA) {
+        uint8_t* kt = ring.k_tile(st);
+        uint8_t* vt = ring.v_tile(st);
+        const int L = sq < 0 ? vis : len_s[sq];
+        const bool last_blk = sq >= 0 && t == cum_s[sq + 1] - 1;
+        bool fresh_row = false;
+        uint32_t kn[2] = {0u, 0u}, vn[2] = {0u, 0u};
+        if (last_blk && appends(sq)) {
+          fresh_row = fresh_s[sq] != 0;  // the producer found a valid block id
+          if (fresh_row && spc == 1) {
+            kn[0] = kn1[0], kn[1] = kn1[1], vn[0] = vn1[0], vn[1] = vn1[1];
+          } else if (fresh_row) {
+            if (!fresh_ready && !mbar_wait(fresh_bar, 0)) {
+              if (lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
+              *ring.abort_flag = 1;
+              break;
+            }
+            fresh_ready = true;
+            const uint8_t* fk = fresh + (2 * sq) * row_bytes + warp * HD * 2 + lane * (HD / 16);
+            if constexpr (HD / 16 == 8) {
+              const uint2 a = *reinterpret_cast<const uint2*>(fk);
+              const uint2 c = *reinterpret_cast<const uint2*>(fk + row_bytes);
+              kn[0] = a.x, kn[1] = a.y, vn[0] = c.x, vn[1] = c.y;
+            } else {
+              kn[0] = *reinterpret_cast<const uint32_t*>(fk);
+              vn[0] = *reinterpret_cast<const uint32_t*>(fk + row_bytes);
+            }
+          }
+        }
+        const bool fix = (L - jpos < kBS) || fresh_row;
+        if (fix) tile_fix<HD>(kt, vt, warp, min(kBS, L - jpos), fresh_row, kn, vn);
+        rows.block_sw(kt, vt, warp, jpos, p.scale_log2, sq);
+        if (fix) fence_proxy_async_smem();
+      } else {
+        // plain split decode only (a shared prefix takes the tile path)
+        const int hoff = warp * HD * p.elem_bytes;
+        rows.block(ring.k_tile(st) + hoff, ring.v_tile(st) + hoff, ring.row_stride, jpos,
+                   p.scale_log2);
+      }
+      ring_release(ring, it);
+    }
+    // this CTA's part (also after an abort, so the barrier below is reached)
+    rows.store_partial(
+        [&](int r) -> float* { return r < nrows ? part_o + (warp * PR + r) * HD : nullptr; },
+        [&](int r) -> float* { return part_ml + (warp * PR + r) * 2; });
+  }
+
+  cluster_sync();  // every CTA's partial is in its shared memory
+  // CTA `rank` combines elements [rank E / C, (rank + 1) E / C) of the
+  // chunk's active rows x head_dim outputs (warp-major) from the C partials
+  const int nrows = ns * p.rep;
+  const int E = consumers * nrows * HD;
+  const int e0 = static_cast<int>(int64_t(rank) * E / C), e1 = static_cast<int>(int64_t(rank + 1) * E / C);
+  T* out = static_cast<T*>(p.out);
+  for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += static_cast<int>(blockDim.x)) {
+    const int w = e / (nrows * HD);
+    const int rem = e - w * nrows * HD;
+    const int r = rem / HD, d = rem - (rem / HD) * HD;
+    const int prow = w * PR + r;
+    float2 ml[kMaxCluster];
+    float oc[kMaxCluster];
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {  // every peer's values in one round trip
+      ml[c] = make_float2(-INFINITY, 0.f);
+      oc[c] = 0.f;
+      if (c < C) {
+        ml[c] = ld_cluster_f32x2(cluster_map(part_ml + prow * 2, c));
+        oc[c] = ld_cluster_f32(cluster_map(part_o + prow * HD + d, c));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c)
+      if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);  // a part that saw no key has no weight
+    float acc = 0.f, den = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      if (ml[c].y > 0.f) {
+        const float wgt = fast_exp2(ml[c].x - M) * ml[c].y;
+        den += wgt;
+        acc = fmaf(wgt, oc[c], acc);
+      }
+    }
+    const int64_t orow = int64_t(s0 + r / p.rep) * p.n_heads + (grp * p.hg_size + w) * p.rep + r % p.rep;
+    out[orow * HD + d] = Elem<T>::from_f(den > 0.f ? acc * (1.f / den) : 0.f);
+  }
+  cluster_sync();  // the peers have read this CTA's partials
+}
+
 template <typename T, int HD>
 __global__ void __launch_bounds__(decode_max_threads<T, HD>()) __maxnreg__(HD == 64 ? 112 : 224)
     decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -1436,6 +1825,13 @@ template <typename T, int HD, int MAXR>
 __global__ void __launch_bounds__(decode_max_threads<T, HD>())
     decode_cluster_rows_kernel(DecodeParams p) {
   decode_cluster_body<T, HD, MAXR, false>(nullptr, nullptr, p);
+}
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(decode_max_threads<T, HD>()) __maxnreg__(HD == 64 ? 112 : 224)
+    decode_cluster_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                 const __grid_constant__ CUtensorMap tm_v, DecodeParams p) {
+  decode_cluster_prefix_body<T, HD, 16, true>(&tm_k, &tm_v, p);
 }
 
 // Shared-prefix attention: the first prefix_blocks table entries are the
@@ -1953,20 +2349,95 @@ struct DecodeLaunch {
     else
       return decode_cluster_rows_kernel<T, HD, MAXR>;
   }
-  // CTAs per cluster for the cluster path, or 0 for the stream-K path.  Only
-  // calls that leave the grid to the library (max_ctas 0) and share no
-  // prefix qualify, when the longest sequence is at most 64 blocks (each
-  // CTA then walks at most 8) and the clusters fit in two waves of the
-  // stream-K grid: batches too small to keep the machine streaming, whose
-  // time is latency (a block's round trip, the merge launch) rather than
-  // bytes.  About 4 blocks per CTA, at most 8 CTAs per cluster.
-  static int cluster_size(const AttnArgs& a, int hg, int wave) {
-    if (a.max_ctas != 0 || a.prefix_blocks != 0) return 0;
+  // the shared-prefix cluster kernel (tile path only; the CUDA-core path
+  // never selects it)
+  static auto cluster_prefix_kernel() {
+    if constexpr (MMA)
+      return decode_cluster_prefix_kernel<T, HD>;
+    else
+      return decode_cluster_rows_kernel<T, HD, MAXR>;  // unused
+  }
+  // Shape of the cluster path for a call (C = 0: the stream-K path).  Only
+  // calls that leave the grid to the library (max_ctas 0) qualify.
+  //  * No shared prefix: one sequence per cluster, when the longest
+  //    sequence is at most 64 blocks and the clusters fit in two waves of
+  //    the stream-K grid: batches too small to keep the machine streaming,
+  //    whose time is latency (a block's round trip, the merge launch)
+  //    rather than bytes.  About 4 blocks per CTA, at most 8 CTAs.
+  //  * A shared prefix (tile path): the prefix is read once per chunk of
+  //    spc sequences; spc (up to a tile's 16 rows) and C are chosen for the
+  //    fewest blocks on the busiest CTA times the waves of clusters.
+  // The ring holds a CTA's blocks (2 to nstages_max stages).
+  struct ClusterShape {
+    int C = 0, spc = 1, stages = 0;
+    size_t smem = 0;
+  };
+  // The cluster kernel is opted into nearly the most dynamic shared memory
+  // a CTA may have (227 KB, less 1 KB for its static shared variables), once
+  // per device; each launch uses what its shape needs.
+  static constexpr int kClusterSmemMax = 226 * 1024;
+  static cudaError_t cluster_kernel_setup(bool prefix, int threads) {
+    static KernelSetup setup, prefix_setup;
+    return prefix ? kernel_setup(prefix_setup, cluster_prefix_kernel(), kClusterSmemMax, threads,
+                                 nullptr)
+                  : kernel_setup(setup, cluster_kernel(), kClusterSmemMax, threads, nullptr);
+  }
+  static ClusterShape cluster_shape(const AttnArgs& a, int hg, int wave, int nstages_max) {
+    ClusterShape best;
+    if (a.max_ctas != 0) return best;
+    const int P = a.prefix_blocks;
+    if (P > 0 && !MMA) return best;
     const int nmax = (min(a.max_seq_len, a.max_blocks_per_seq * kBS) + kBS - 1) / kBS;
-    if (nmax > 8 * kMaxCluster) return 0;
-    const int C = std::max(1, std::min(kMaxCluster, (nmax + 3) / 4));
-    const int64_t ctas = int64_t(a.num_seqs) * (a.pool.n_kv / hg) * C;
-    return ctas <= 2 * int64_t(wave) ? C : 0;
+    const int rep = a.n_heads / a.pool.n_kv;
+    const int groups = a.pool.n_kv / hg;
+    const int eb = a.pool.elem_bytes();
+    const bool staged = MMA && a.k_new != nullptr && P > 0;  // the prefix kernel stages step rows
+    const int threads = (hg + 1) * 32;
+    auto shape_for = [&](int C, int spc, int per) {
+      ClusterShape c;
+      c.C = C;
+      c.spc = spc;
+      c.stages = std::max(2, std::min(nstages_max, per));
+      for (;; --c.stages) {
+        c.smem = (smem_for(hg, eb, c.stages) + 15) / 16 * 16 +
+                 cluster_extra_bytes(hg, rep, HD, eb, spc, staged);
+        if (c.smem <= 220 * 1024 || c.stages == 2) break;
+      }
+      return c;
+    };
+    if (P == 0) {
+      if (nmax > 8 * kMaxCluster) return best;
+      const int C = std::max(1, std::min(kMaxCluster, (nmax + 3) / 4));
+      const int64_t ctas = int64_t(a.num_seqs) * groups * C;
+      if (ctas > 2 * int64_t(wave)) return best;
+      return shape_for(C, 1, (nmax + C - 1) / C);
+    }
+    // shared prefix: every (spc, C), costed as the busiest CTA's blocks
+    // times the waves of clusters the device holds at once
+    static ClusterOccupancy occ;
+    if (cluster_kernel_setup(true, threads) != cudaSuccess) {
+      cudaGetLastError();
+      return best;
+    }
+    int64_t best_cost = -1;
+    for (int spc = 1; spc <= std::min(kRowsPerWarp / rep, kMaxChunk); ++spc) {
+      const int64_t clusters = int64_t((a.num_seqs + spc - 1) / spc) * groups;
+      const int list = P + spc * std::max(0, nmax - P);
+      for (int C = 1; C <= kMaxCluster; ++C) {
+        const int per = (list + C - 1) / C;
+        const ClusterShape c = shape_for(C, spc, per);
+        if (c.smem > kClusterSmemMax) continue;
+        const int at_once = max_active_clusters(occ, cluster_prefix_kernel(), C,
+                                                static_cast<int>(c.smem), threads);
+        if (at_once <= 0) continue;
+        const int64_t cost = (clusters + at_once - 1) / at_once * per;
+        if (best_cost < 0 || cost < best_cost) {
+          best_cost = cost;
+          best = c;
+        }
+      }
+    }
+    return best;
   }
   // Persistent grid: every SM filled with as many CTAs as fit, capped by
   // max_ctas; *wave (optional) = the uncapped full wave.
@@ -2061,20 +2532,16 @@ struct DecodeLaunch {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     p.planned = a.decode_plan == kPlanned;
-    if (const int C = cluster_size(a, hg, wave); C > 0) {
-      // latency-bound batch: one cluster of C CTAs per (sequence, head
-      // group), partials combined in distributed shared memory
+    if (const ClusterShape cs = cluster_shape(a, hg, wave, p.nstages); cs.C > 0) {
+      // latency-bound batch, or a shared prefix: one cluster of C CTAs per
+      // (chunk of spc sequences, head group), partials combined in
+      // distributed shared memory
+      const int C = cs.C;
       p.cluster = C;
-      // a CTA walks at most ceil(blocks / C) <= 8 blocks: a ring that holds
-      // them all (at least 2 stages), so several CTAs fit on an SM
-      const int nmax = (min(a.max_seq_len, a.max_blocks_per_seq * kBS) + kBS - 1) / kBS;
-      p.nstages = std::max(2, std::min(p.nstages, (nmax + C - 1) / C));
-      smem = smem_for(hg, p.elem_bytes, p.nstages);
-      p.part_off = static_cast<int>((smem + 15) / 16 * 16);
-      const size_t csmem = size_t(p.part_off) + size_t(hg) * p.rep * (HD + 2) * 4;
-      static KernelSetup cluster_setup;
-      e = kernel_setup(cluster_setup, cluster_kernel(), static_cast<int>(csmem), (hg + 1) * 32,
-                       nullptr);
+      p.cluster_seqs = cs.spc;
+      p.nstages = cs.stages;
+      p.part_off = static_cast<int>((smem_for(hg, p.elem_bytes, cs.stages) + 15) / 16 * 16);
+      e = cluster_kernel_setup(p.prefix_blocks > 0, (hg + 1) * 32);
       if (e != cudaSuccess) return e;
       cudaLaunchAttribute cattr[2];
       cattr[0] = attr[0];
@@ -2083,16 +2550,21 @@ struct DecodeLaunch {
       cattr[1].val.clusterDim.y = 1;
       cattr[1].val.clusterDim.z = 1;
       cudaLaunchConfig_t ccfg = {};
-      ccfg.gridDim = dim3(static_cast<unsigned>(int64_t(p.B) * p.n_groups * C));
+      const int64_t chunks = (int64_t(p.B) + cs.spc - 1) / cs.spc;
+      ccfg.gridDim = dim3(static_cast<unsigned>(chunks * p.n_groups * C));
       ccfg.blockDim = dim3((hg + 1) * 32);
-      ccfg.dynamicSmemBytes = csmem;
+      ccfg.dynamicSmemBytes = cs.smem;
       ccfg.stream = stream;
       ccfg.attrs = cattr;
       ccfg.numAttrs = 2;
-      if constexpr (MMA)
-        e = cudaLaunchKernelEx(&ccfg, decode_cluster_kernel<T, HD>, tm_k, tm_v, p);
-      else
+      if constexpr (MMA) {
+        if (p.prefix_blocks > 0)
+          e = cudaLaunchKernelEx(&ccfg, decode_cluster_prefix_kernel<T, HD>, tm_k, tm_v, p);
+        else
+          e = cudaLaunchKernelEx(&ccfg, decode_cluster_kernel<T, HD>, tm_k, tm_v, p);
+      } else {
         e = cudaLaunchKernelEx(&ccfg, decode_cluster_rows_kernel<T, HD, MAXR>, p);
+      }
       if (e != cudaSuccess) return e;
       return cudaGetLastError();
     }

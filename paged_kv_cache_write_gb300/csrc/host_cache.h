@@ -48,6 +48,66 @@ cudaError_t kernel_setup(KernelSetup& ks, Kern kern, int smem, int threads, int*
   return cudaSuccess;
 }
 
+// Clusters of C CTAs (threads each, smem bytes of dynamic shared memory)
+// of `kern` that the current device can hold at once, from the runtime's
+// occupancy query, cached per device and shape (the kernel's dynamic
+// shared-memory opt-in must be set first).  0 on error.
+struct ClusterOccupancy {
+  static constexpr int kSlots = 256;
+  std::atomic<uint64_t> entry[kMaxCachedDevices][kSlots];
+  ClusterOccupancy() {
+    for (auto& d : entry)
+      for (auto& e : d) e.store(0);
+  }
+};
+
+template <typename Kern>
+int max_active_clusters(ClusterOccupancy& co, Kern kern, int C, int smem, int threads) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  // key: C (5 bits), smem / 16 (15 bits), threads / 32 (6 bits); value + 1 in 20 bits
+  const uint64_t key = (uint64_t(C) << 21) | (uint64_t(smem / 16) << 6) | uint64_t(threads / 32);
+  // open addressing: probe up to 16 slots from the key's hash
+  const int h = static_cast<int>((key * 0x9E3779B97F4A7C15ull) >> 56);
+  if (dev < kMaxCachedDevices) {
+    for (int i = 0; i < 16; ++i) {
+      const uint64_t v = co.entry[dev][(h + i) & (ClusterOccupancy::kSlots - 1)].load(
+          std::memory_order_acquire);
+      if (v == 0) break;
+      if ((v >> 20) == key) return int(v & 0xfffff) - 1;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (n > 0xffffe) n = 0xffffe;
+  if (dev < kMaxCachedDevices) {
+    for (int i = 0; i < 16; ++i) {  // first free slot (racing writers may store it twice)
+      uint64_t expect = 0;
+      if (co.entry[dev][(h + i) & (ClusterOccupancy::kSlots - 1)].compare_exchange_strong(
+              expect, (key << 20) | uint64_t(n + 1)))
+        break;
+    }
+  }
+  return n;
+}
+
 // SMs of the current device, looked up once per device (devices past
 // kMaxCachedDevices are asked every time).  Entries are atomics, so threads
 // calling on different devices neither race nor see each other's count.
