@@ -125,3 +125,60 @@ def test_shared_prefix_large_batch():
     torch.cuda.synchronize()
     assert int(g.err.item()) == 0
     assert_close(f64(out)[rows], ref[rows], "bf16", "B=3000")
+
+
+APPEND_SHAPES = [(9, 3, 64, "bf16"), (32, 8, 64, "bf16"), (64, 8, 128, "bf16"), (16, 1, 64, "bf16")]
+
+
+@pytest.mark.parametrize("shape", APPEND_SHAPES, ids=[f"{h}x{k}x{d}" for h, k, d, _ in APPEND_SHAPES])
+@pytest.mark.parametrize("P", [1, 3])
+def test_shared_prefix_planned_append_edges(shape, P):
+    """Planned shared-prefix decode with the step's K/V fused in, lengths
+    inside, at and past the prefix, on whichever kernel the shape selects: a
+    token that would land in a shared block is
+    reported (PKV_DEVERR_PREFIX) and not written; otherwise outputs and
+    pools equal pkv_kv_write of the other sequences' rows followed by the
+    planned call without k_new, bit for bit, and match the oracle."""
+    import oracle
+    from gpu_step import guarded_copy, guarded_empty
+    H, K, D, dt = shape
+    lens = [0, 5, 16 * P, 16 * P + 1, 40 + 16 * P, 100, 260, 33, 16 * P - 3, 500]
+    plan = _plan_with_prefix(lens, P, H, K, D, dt, seed=7 * P + D)
+    layer = make_tiny_layer(plan, seed=P + H)
+    g = GpuStep(plan, layer)
+    nd, t, sh = g.nd, g.t, g.sh
+    past = [b for b in range(nd) if lens[b] > 16 * P]
+    slots = np.full(nd, -1, dtype=np.int64)
+    for b in past:
+        slots[b] = oracle.slot_of(plan.block_tables[b], lens[b] - 1, 16)
+    k_new, v_new = t["k"][:nd].contiguous(), t["v"][:nd].contiguous()
+    kp1, vp1 = guarded_copy(t["k_pool"]), guarded_copy(t["v_pool"])
+    kp2, vp2 = guarded_copy(t["k_pool"]), guarded_copy(t["v_pool"])
+    ws = guarded_empty((pkv.decode_shared_prefix_workspace_bytes(nd, H, D, g.max_dec, P),),
+                       torch.uint8)
+    ws.zero_()
+    err1 = guarded_empty((1,), torch.int32)
+    err1.zero_()
+    err2 = guarded_empty((1,), torch.int32)
+    err2.zero_()
+    pkv.decode_plan(t["k_pool"], g.seq_lens[:nd], H, g.bt.shape[1], g.max_dec, workspace=ws,
+                    shared_prefix_blocks=P, err=err1)
+    pkv.kv_write(k_new, v_new, torch.from_numpy(slots).cuda(), kp1, vp1, err=err1)
+    ref = pkv.paged_attention_decode_planned(t["q"][:nd], kp1, vp1, g.bt[:nd], g.seq_lens[:nd],
+                                             sh.scale, g.max_dec, workspace=ws,
+                                             shared_prefix_blocks=P, err=err1)
+    out = pkv.paged_attention_decode_planned(t["q"][:nd], kp2, vp2, g.bt[:nd], g.seq_lens[:nd],
+                                             sh.scale, g.max_dec, workspace=ws, k_new=k_new,
+                                             v_new=v_new, shared_prefix_blocks=P, err=err2)
+    torch.cuda.synchronize()
+    assert int(err1.item()) == 0
+    assert int(err2.item()) == PKV_DEVERR_PREFIX  # lengths 5, 16P, 16P - 3 (0 has no token)
+    # a reported row's output is unspecified; every other row is compared
+    rows = torch.tensor(past, device="cuda")
+    assert torch.equal(out[rows].view(torch.int16), ref[rows].view(torch.int16))
+    assert torch.equal(kp2.view(torch.int16), kp1.view(torch.int16))
+    assert torch.equal(vp2.view(torch.int16), vp1.view(torch.int16))
+    o = OracleStep(plan, layer)
+    o.kp, o.vp = oracle.kv_write(o.raw["k"][:nd], o.raw["v"][:nd], slots, o.raw["k_pool"],
+                                 o.raw["v_pool"])
+    assert_close(f64(out)[past], o.decode(rows=past)[past], dt, f"P={P}")
