@@ -186,24 +186,26 @@ struct MmaRows {
       mma_bf16_16816(s[0], qa[kk], kb[0], kb[1]);
       mma_bf16_16816(s[1], qa[kk], kb[2], kb[3]);
     }
-    // scale, causal / length mask, online softmax
-    float mx[2] = {-INFINITY, -INFINITY};
+    // causal / length mask: only a block that crosses some row's last key
+    // (warp-uniform test) masks element by element
+    const int first_cut = min(lim[0], lim[1]);
+    if (!__all_sync(0xffffffffu, j0 + kBS - 1 <= first_cut)) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h = e >> 1;
-        const int pos = j0 + nt * 8 + 2 * c + (e & 1);
-        const float x = s[nt][e] * scale_log2;
-        s[nt][e] = (pos <= lim[h]) ? x : -INFINITY;
-        mx[h] = fmaxf(mx[h], s[nt][e]);
-      }
+        for (int e = 0; e < 4; ++e)
+          if (j0 + nt * 8 + 2 * c + (e & 1) > lim[e >> 1]) s[nt][e] = -INFINITY;
+    }
+    // online softmax in log2 units: the raw maximum times the (positive)
+    // scale is the maximum of the scaled scores
+    float mx[2] = {fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])),
+                   fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]))};
     float alpha[2], mref[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
       mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-      const float mn = fmaxf(m[h], mx[h]);
+      const float mn = fmaxf(m[h], mx[h] * scale_log2);
       mref[h] = (mn == -INFINITY) ? 0.f : mn;  // a row with nothing visible yet
       alpha[h] = fast_exp2(m[h] - mref[h]);
       m[h] = mn;
@@ -214,8 +216,8 @@ struct MmaRows {
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float p0 = fast_exp2(s[nt][2 * h] - mref[h]);
-        const float p1 = fast_exp2(s[nt][2 * h + 1] - mref[h]);
+        const float p0 = fast_exp2(fmaf(s[nt][2 * h], scale_log2, -mref[h]));
+        const float p1 = fast_exp2(fmaf(s[nt][2 * h + 1], scale_log2, -mref[h]));
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         const float2 pr = __bfloat1622float2(pb);
         rs[h] += pr.x + pr.y;  // the sum uses the same rounded weights as P V
@@ -223,12 +225,16 @@ struct MmaRows {
       }
 #pragma unroll
     for (int h = 0; h < 2; ++h) l[h] = l[h] * alpha[h] + rs[h];
+    // the outputs are rescaled only when some row's maximum moved (alpha 1
+    // elsewhere: skipping the product changes no bit)
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-    for (int i = 0; i < HD / 8; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[0];
-      o[i][2] *= alpha[1];
-      o[i][3] *= alpha[1];
+      for (int i = 0; i < HD / 8; ++i) {
+        o[i][0] *= alpha[0];
+        o[i][1] *= alpha[0];
+        o[i][2] *= alpha[1];
+        o[i][3] *= alpha[1];
+      }
     }
     // O += P V: matrices (tokens 0-7 | 8-15) x (dims lo | hi), transposed.
 #pragma unroll
@@ -626,13 +632,19 @@ __device__ __forceinline__ void ring_drain(const Ring& r, uint32_t issued) {
     mbar_wait(r.full + (it % r.nstages), (it / r.nstages) & 1);
 }
 
+// Consumer side: wait for stage `it`'s tile.  False if the producer gave up
+// (abort flag, looked at only while the tile is not there yet) or the wait
+// timed out (reported).
 __device__ __forceinline__ bool ring_wait_full(const Ring& r, uint32_t it, int32_t* err) {
   const int st = static_cast<int>(it % r.nstages);
-  if (!mbar_wait(r.full + st, (it / r.nstages) & 1)) {
-    if ((threadIdx.x & 31) == 0) report(err, PKV_DEVERR_TIMEOUT);
-    return false;
+  const uint32_t parity = (it / r.nstages) & 1;
+  if (mbar_try_wait(r.full + st, parity)) return true;
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    if (*r.abort_flag) return false;
+    if (mbar_try_wait(r.full + st, parity)) return true;
   }
-  return true;
+  if ((threadIdx.x & 31) == 0) report(err, PKV_DEVERR_TIMEOUT);
+  return false;
 }
 
 __device__ __forceinline__ void ring_release(const Ring& r, uint32_t it) {
@@ -681,6 +693,18 @@ struct DecodeParams {
   // cluster (their rows per warp: cluster_seqs * rep), and the byte offset
   // of the partial results in shared memory
   int cluster, cluster_seqs, part_off;
+  // wide shared-prefix pass: consumer warps (16-row tiles) per CTA, and 1
+  // if each prefix tile is read by one cluster only (its lines may leave L2
+  // first)
+  int wide_mt, wide_evict;
+  // fused shared prefix (stream-K kernel): CTAs [0, prompt_items) first
+  // attend item c = ((chunk * n_kv) + KV head) * prompt_runs + run: run
+  // `run` (prompt_bpr blocks of row 0's table) for the prompt_seqs
+  // sequences of `chunk`, consumer warp w carrying the rows of sequences
+  // w * (16 / rep) ..; each leaves a partial per row in run slot `run`.
+  // Every group after the prefix then leaves a partial too (a whole one in
+  // run slot prompt_runs) and the prefix merge kernel combines them.
+  int prompt_items, prompt_runs, prompt_bpr, prompt_seqs;
   float scale_log2;
 };
 
@@ -874,7 +898,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     // CTA merges, so those calls' merge CTAs can read it before they wait
     if (p.plan_only) p.splits[c] = sp;
   }
-  if (p.plan_only) {  // kept for the calls that use the plan (empty sequences)
+  if (p.plan_only || p.prompt_items > 0) {  // kept for later calls / the prefix merge
     if (in_smem)
       for (int b = tid; b <= p.B; b += blockDim.x) p.cu_units[b] = cu[b];
   } else if (p.prefix_blocks == 0) {  // with a prefix, the prefix kernel writes them
@@ -934,7 +958,7 @@ constexpr int decode_max_threads() {
 
 // The decode body; tm_k / tm_v are the pools' tile maps (tensor-core path)
 // or null (CUDA-core path).
-template <typename T, int HD, int MAXR, bool MMA>
+template <typename T, int HD, int MAXR, bool MMA, bool PROMPT = false>
 __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                             const DecodeParams& p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -944,7 +968,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
   // tensor-core path: whole-block TMA tiles; CUDA-core path: a copy per row
   Ring ring = MMA ? make_tile_ring(smem, p.nstages, kBS * row_bytes)
                   : make_ring(smem, p.nstages, row_bytes);
-  ring_init(ring, consumers);
+  if (PROMPT && threadIdx.x == 0) mbar_init(reinterpret_cast<uint64_t*>(smem + 768), 1);  // pbar
+  ring_init(ring, consumers);  // (its barrier also publishes pbar's init)
   // inputs written by the preceding kernel (the plan, when there is one);
   // a planned call waits after reading its plan and first table entries
   if (!p.planned) pdl_wait();
@@ -1013,6 +1038,68 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
   // and on the tile path its first blocks too: up to a ring's worth of the
   // first segment, never the sequence's last block (the only block a decode
   // step writes), so their bytes stream in while the preceding kernel ends
+  // fused shared prefix: this CTA's prompt item (item_nb blocks of one KV
+  // head), held in its own buffer after the ring and attended by the
+  // prompt warps (warps consumers + 1 ..) while the consumers stream the
+  // blocks after the prefix
+  [[maybe_unused]] int item_run = 0, item_head = 0, item_s0 = 0, item_j0 = 0, item_nb = 0;
+  [[maybe_unused]] uint8_t* pbuf = ring.stages + p.nstages * ring.stage_bytes;  // K tiles, then V tiles
+  [[maybe_unused]] uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + 768);   // past the ring's barriers
+  if constexpr (PROMPT) {
+    if (static_cast<int>(blockIdx.x) < p.prompt_items) {
+      const int c = blockIdx.x;
+      item_run = c % p.prompt_runs;
+      item_head = (c / p.prompt_runs) % p.n_kv;
+      item_s0 = c / (p.prompt_runs * p.n_kv) * p.prompt_seqs;
+      item_j0 = item_run * p.prompt_bpr;
+      item_nb = max(0, min(p.prompt_bpr, p.prefix_blocks - item_j0));
+      // The prefix blocks are never written by a decode step, so their
+      // loads go out before the dependency wait.  One head of a block is 16
+      // rows of HD * 2 bytes a token pitch apart: 16-byte copies by every
+      // producer lane (the TMA engine moves such short rows slowly), into
+      // the 128-byte-swizzled tile layout, published on pbar once landed.
+      if (warp == consumers) {
+        const int id = lane < item_nb ? __ldg(p.bt + item_j0 + lane) : 0;  // row 0's table
+        constexpr int kChunks = kBS * HD * 2 / 16;  // 16-byte pieces of one head of a block
+        const int64_t pitch = int64_t(p.n_kv) * HD * 2;
+        for (int i = 0; i < item_nb; ++i) {
+          const int b_id = __shfl_sync(0xffffffffu, id, i);
+          const bool bad = b_id < 0 || b_id >= p.num_blocks;
+          if (bad && lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
+          const int64_t off = int64_t(bad ? 0 : b_id) * kBS * pitch + int64_t(item_head) * HD * 2;
+          uint8_t* kt = pbuf + i * (kBS * HD * 2);
+          uint8_t* vt = pbuf + (p.prompt_bpr + i) * (kBS * HD * 2);
+          for (int x = lane; x < kChunks; x += 32) {
+            // piece x: token t, 16-byte column cx of the head's row
+            const int t = x / (HD / 8), cx = x - t * (HD / 8);
+            const int row = (cx >> 3) * kBS + t;  // (64-dim half, token)
+            const int dst = row * 128 + (((cx & 7) ^ (row & 7)) << 4);
+            const int64_t src = off + int64_t(t) * pitch + cx * 16;
+            if (bad) {  // as the zeros a bad id reads elsewhere
+              *reinterpret_cast<uint4*>(kt + dst) = make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(vt + dst) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+              cp_async_16(kt + dst, p.k_pool + src);
+              cp_async_16(vt + dst, p.v_pool + src);
+            }
+          }
+        }
+      }
+    }
+  }
+  // the prompt buffer is published once its copies have landed: after the
+  // first blocks after the prefix are requested (planned call) or at once
+  // (the dependency wait came first)
+  [[maybe_unused]] auto publish_prompt = [&]() {
+    if constexpr (PROMPT) {
+      if (item_nb > 0 && warp == consumers) {
+        cp_async_wait_all();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pbar);
+      }
+    }
+  };
+  if (!p.planned) publish_prompt();
   int pre_id = 0, early = 0;
   bool pre = false;
   if (p.planned) {
@@ -1032,6 +1119,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
         }
       }
     }
+    publish_prompt();
     pdl_wait();
     if (p.prefix_blocks == 0)
       zero_empty<T, HD>(p, blockIdx.x, G,
@@ -1137,7 +1225,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
             return r < p.rep ? q + (int64_t(b) * p.n_heads + head0 + r) * HD : nullptr;
           },
           [&](int) { return last; });
-      if (p.prefix_blocks > 0 && cur.j == 0) {
+      if (!PROMPT && p.prefix_blocks > 0 && cur.j == 0) {
         // the group's first walked block: continue from the shared prefix
         const int64_t prow = int64_t(p.prefix_seed_run) * p.B * p.n_heads +
                              int64_t(b) * p.n_heads + head0;
@@ -1157,7 +1245,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
         }
       }
       for (int k = 0; k < n; ++k) {
-        if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
+        if (!ring_wait_full(ring, it, p.err)) {
           *ring.abort_flag = 1;
           ok = false;
           break;
@@ -1184,7 +1272,13 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
       }
       if (!ok) break;
       const bool whole = (cur.j == 0) && (n == cur.nblk);
-      if (whole) {
+      if (PROMPT && whole) {
+        // fused shared prefix: the prefix merge kernel adds the prompt runs
+        const int64_t prow = int64_t(p.prompt_runs) * p.B * p.n_heads + int64_t(b) * p.n_heads + head0;
+        rows.store_partial(
+            [&](int r) -> float* { return r < p.rep ? p.pre_o + (prow + r) * HD : nullptr; },
+            [&](int r) -> float* { return p.pre_ml + (prow + r) * 2; });
+      } else if (whole) {
         rows.store([&](int r) -> T* {
           return r < p.rep ? out + (int64_t(b) * p.n_heads + head0 + r) * HD : nullptr;
         });
@@ -1199,6 +1293,58 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
       u += n;
       cur.advance(p, n);
     }
+  } else if (PROMPT && warp > consumers && warp <= consumers + p.wide_mt && item_nb > 0) {
+    // ------------------------------------------------------ prompt warps
+    // warp consumers + 1 + w carries sequences item_s0 + w spm .. (row r:
+    // query head r % rep of the KV head item_head); keys past a row's own
+    // length are masked, and V rows past every chunk sequence's reach
+    // (which may hold anything) are zeroed by each reading warp alike
+    // before its P V
+    if constexpr (PROMPT) {
+      const int w = warp - consumers - 1;
+      const int spm = kMaxRep / p.rep;
+      const int pre_len = p.prefix_blocks * kBS;
+      const int nseq = min(p.prompt_seqs, p.B - item_s0);
+      int vis = 0;
+      for (int t = lane; t < nseq; t += 32) vis = max(vis, min(used_len(p, item_s0 + t), pre_len));
+      vis = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(vis)));
+      const int sw = item_s0 + w * spm;  // this warp's first sequence
+      const int nrow = min(spm, max(0, p.B - sw)) * p.rep;
+      if (nrow > 0) {
+        const T* q = static_cast<const T*>(p.q);
+        Rows rows;
+        rows.begin(
+            [&](int r) -> const T* {
+              return r < nrow ? q + (int64_t(sw + r / p.rep) * p.n_heads + item_head * p.rep + r % p.rep) * HD
+                              : nullptr;
+            },
+            [&](int r) { return min(used_len(p, sw + r / p.rep), pre_len) - 1; });
+        if (!mbar_wait(pbar, 0)) {
+          if (lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
+        } else {
+          const uint32_t none[2] = {0u, 0u};
+          for (int i = 0; i < item_nb; ++i) {
+            const int jpos = (item_j0 + i) * kBS;
+            if (jpos >= vis) break;  // no chunk sequence reaches it
+            uint8_t* kt = pbuf + i * (kBS * HD * 2);
+            uint8_t* vt = pbuf + (p.prompt_bpr + i) * (kBS * HD * 2);
+            if (vis - jpos < kBS) tile_fix<HD>(kt, vt, 0, vis - jpos, false, none, none);
+            rows.block_sw(kt, vt, 0, jpos, p.scale_log2);
+          }
+        }
+        const int64_t prow = int64_t(item_run) * p.B * p.n_heads;
+        rows.store_partial(
+            [&](int r) -> float* {
+              return r < nrow ? p.pre_o + (prow + int64_t(sw + r / p.rep) * p.n_heads +
+                                           item_head * p.rep + r % p.rep) * HD
+                              : nullptr;
+            },
+            [&](int r) -> float* {
+              return p.pre_ml + (prow + int64_t(sw + r / p.rep) * p.n_heads + item_head * p.rep +
+                                 r % p.rep) * 2;
+            });
+      }
+    }
   }
 }
 
@@ -1210,6 +1356,36 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) __maxnreg__(HD ==
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   DecodeParams p) {
   decode_body<T, HD, 16, true>(&tm_k, &tm_v, p);
+}
+
+// Tensor-core path with a shared prefix attended in the same launch: in
+// the first prompt_items CTAs a second set of warps (wide_mt prompt warps)
+// takes one run of the prefix for a chunk of sequences at one KV head
+// while the consumers walk the CTA's range of the blocks after the prefix;
+// all results are partials for decode_prefix_merge_kernel.
+// Warps of the fused shared-prefix CTA: the consumers (one per KV head of
+// the group, hg), the producer and up to hg prompt warps, within what the
+// register file gives each of the four schedulers (at most 16 warps at 112
+// registers for head_dim 64, 12 at 168 for head_dim 128).
+template <int HD>
+constexpr int fused_max_warps() {
+  return HD == 64 ? 16 : 12;
+}
+inline int fused_prompt_warps(int hg, int max_warps) { return std::max(0, std::min(hg, max_warps - hg - 1)); }
+
+template <typename T, int HD>
+constexpr int fused_max_threads() {
+  return (decode_max_threads<T, HD>() / 32 +
+          (decode_max_threads<T, HD>() / 32 - 1 < fused_max_warps<HD>() - decode_max_threads<T, HD>() / 32
+               ? decode_max_threads<T, HD>() / 32 - 1
+               : fused_max_warps<HD>() - decode_max_threads<T, HD>() / 32)) * 32;
+}
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(fused_max_threads<T, HD>()) __maxnreg__(HD == 64 ? 112 : 224)
+    decode_fused_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
+                               const __grid_constant__ CUtensorMap tm_v, DecodeParams p) {
+  decode_body<T, HD, 16, true, true>(&tm_k, &tm_v, p);
 }
 
 // CUDA-core path: a bulk copy per token row into a padded ring.
@@ -1398,7 +1574,7 @@ __device__ __forceinline__ void decode_cluster_body(const CUtensorMap* tm_k, con
     }
     uint32_t it = 0;
     for (int j = j0; j < j1; ++j, ++it) {
-      if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
+      if (!ring_wait_full(ring, it, p.err)) {
         *ring.abort_flag = 1;
         break;
       }
@@ -1717,7 +1893,7 @@ __device__ __forceinline__ void decode_cluster_prefix_body(const CUtensorMap* tm
     bool fresh_ready = false;
     uint32_t it = 0;
     for (int t = j0; t < j1; ++t, ++it) {
-      if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
+      if (!ring_wait_full(ring, it, p.err)) {
         *ring.abort_flag = 1;
         break;
       }
@@ -1834,6 +2010,218 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>()) __maxnreg__(HD ==
   decode_cluster_prefix_body<T, HD, 16, true>(&tm_k, &tm_v, p);
 }
 
+// ------------------------------------------------- wide shared prefix
+//
+// A long prompt common to many sequences: every sequence's rows attend to
+// all of its blocks, so each block is read once per KV head for a chunk of
+// up to 16 tiles of rows (64 sequences at 4 query heads per KV head)
+// instead of once per tile.  One cluster of K CTAs per (KV head, chunk of
+// sequences); CTA r walks run r of the prefix, blocks [r P / K, (r+1) P / K)
+// of row 0's table, one KV head per TMA tile (16 tokens x head_dim), each
+// tile used by every consumer warp.  Warp w carries the rows of sequences
+// s0 + w spm .. s0 + (w+1) spm - 1 (spm = 16 / rep; row i = query head
+// i % rep of sequence i / rep), keys past a row's own length masked.  After
+// a cluster barrier the K partials of each row are combined through
+// distributed shared memory, each CTA a slice of the rows x head_dim
+// elements: a sequence that ends inside the prefix gets its output, any
+// other sequence a normalised partial (output, max, exp-sum) in run slot
+// prefix_seed_run, from which the main kernel goes on over its own blocks.
+// A second barrier keeps each CTA's partials alive until its peers have
+// read them.
+constexpr int kWideMaxSeqs = 256;  // sequences of one chunk: 16 tiles x 16 rows at one head
+
+template <int HD>
+constexpr int wide_max_warps() {
+  return HD == 64 ? 16 : 8;  // 112 / 224 registers per thread: 544 / 288 threads per CTA
+}
+
+template <typename T, int HD>
+__global__ void __launch_bounds__((wide_max_warps<HD>() + 1) * 32) __maxnreg__(HD == 64 ? 112 : 224)
+    decode_prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
+                              const __grid_constant__ CUtensorMap tm_v, DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int len_s[kWideMaxSeqs];  // used length of each chunk sequence
+  __shared__ int vis_s;                // prefix positions some chunk sequence sees
+  const int mt = p.wide_mt;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.cluster;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int seg = static_cast<int>(blockIdx.x) / K;  // (chunk of sequences, KV head)
+  const int head = seg % p.n_kv;
+  const int s0 = (seg / p.n_kv) * p.cluster_seqs;
+  const int ns = min(p.cluster_seqs, p.B - s0);
+  const int spm = kMaxRep / p.rep;  // sequences per warp
+  const int P = p.prefix_blocks;
+  const int pre_len = P * kBS;
+  const int j0 = static_cast<int>(int64_t(rank) * P / K);
+  const int jr = static_cast<int>(int64_t(rank + 1) * P / K);  // this CTA's run: [j0, jr)
+  float* part_o = reinterpret_cast<float*>(smem + p.part_off);  // [mt][16][HD]
+  float* part_ml = part_o + mt * 16 * HD;                        // [mt][16][2]
+
+  // A planned call reads its plan record, the lengths and the run's table
+  // entries (unchanged since the plan) before the dependency wait, all in
+  // one round trip; every CTA of the cluster sees the same record, so all
+  // leave together on a mismatch.
+  if (!p.planned) pdl_wait();
+  int id0 = 0;  // producer: the first 32 table entries of the run (row 0's)
+  if (warp == mt && j0 + lane < jr) id0 = __ldg(p.bt + j0 + lane);
+  const bool plan_ok = !p.planned || plan_matches(p, p.grid);
+  int my_vis = 0;
+  for (int t = threadIdx.x; t < ns; t += blockDim.x) {
+    const int L = used_len(p, s0 + t);
+    len_s[t] = L;
+    my_vis = max(my_vis, min(L, pre_len));
+  }
+  if (threadIdx.x == 0) vis_s = 0;
+  Ring ring = make_tile_ring(smem, p.nstages, kBS * HD * 2);  // one head: 16 tokens x HD bf16
+  ring_init(ring, mt);  // (its barrier publishes vis_s = 0 and the lengths)
+  my_vis = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(my_vis)));
+  if (lane == 0 && my_vis > 0) atomicMax(&vis_s, my_vis);
+  __syncthreads();
+  if (!plan_ok) return;  // reported by the main kernel
+  const int vis = vis_s;
+  const int j1 = min(jr, (vis + kBS - 1) / kBS);
+
+  if (warp == mt) {
+    // ------------------------------------------------------ producer
+    // The prefix blocks are never written by a decode step (a token that
+    // would land in one is refused), so a planned call loads them before
+    // the preceding kernel has finished.
+    const uint64_t pol = p.wide_evict ? tc::l2_evict_first_policy() : 0;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int jb = j0; jb < j1 && ok; jb += 32) {
+      const int id = jb == j0 ? id0 : jb + lane < j1 ? __ldg(p.bt + jb + lane) : 0;  // row 0's table
+      for (int k = 0; k < min(32, j1 - jb); ++k) {
+        if (*ring.abort_flag) { ok = false; break; }
+        const int blk = __shfl_sync(0xffffffffu, id, k);
+        const bool bad = blk < 0 || blk >= p.num_blocks;
+        if (bad && lane == 0) report(p.err, PKV_DEVERR_BLOCK_ID);
+        // a bad id reads the zeros past the pool's end
+        bool filled = lane == 0 ? tile_fill(ring, it, &tm_k, &tm_v, bad ? p.num_blocks * kBS : blk * kBS,
+                                            head, p.err, pol)
+                                : true;
+        filled = __shfl_sync(0xffffffffu, filled, 0);
+        if (!filled) {
+          *ring.abort_flag = 1;
+          ok = false;
+          break;
+        }
+        ++it;
+      }
+    }
+    if (!ok) ring_drain(ring, it);
+    // every chunk sequence that reaches one of this run's blocks must name
+    // it where row 0 does (checked once, by the head-0 clusters)
+    if (head == 0 && j1 > j0) {
+      const int nj = j1 - j0;
+      for (int idx = lane; idx < ns * nj; idx += 32) {
+        const int t = idx / nj, j = j0 + idx - t * nj;
+        if (len_s[t] > j * kBS && __ldg(p.bt + int64_t(s0 + t) * p.W + j) != __ldg(p.bt + j))
+          report(p.err, PKV_DEVERR_PREFIX);
+      }
+    }
+  } else if (warp < mt) {
+    // ------------------------------------------------------ consumers
+    if (p.planned) pdl_wait();  // the queries may come from the preceding kernel
+    MmaRows<HD> rows;
+    const int sw = warp * spm;  // this warp's first chunk sequence
+    const T* q = static_cast<const T*>(p.q);
+    rows.begin(
+        [&](int r) -> const T* {
+          const int t = sw + r / p.rep;
+          return r < spm * p.rep && t < ns
+                     ? q + (int64_t(s0 + t) * p.n_heads + head * p.rep + r % p.rep) * HD
+                     : nullptr;
+        },
+        [&](int r) { return min(len_s[sw + r / p.rep], pre_len) - 1; });
+    const bool active = sw < ns;
+    const uint32_t none[2] = {0u, 0u};
+    uint32_t it = 0;
+    for (int j = j0; j < j1; ++j, ++it) {
+      // every warp takes every tile (the stage is free once all have)
+      if (!ring_wait_full(ring, it, p.err)) {
+        *ring.abort_flag = 1;
+        break;
+      }
+      const int st = static_cast<int>(it % ring.nstages);
+      if (active) {
+        // slots past every chunk sequence's reach may hold anything: each
+        // reading warp zeroes those V rows itself (the others write the
+        // same zeros) before its P V
+        const bool fix = vis - j * kBS < kBS;
+        if (fix) tile_fix<HD>(ring.k_tile(st), ring.v_tile(st), 0, vis - j * kBS, false, none, none);
+        rows.block_sw(ring.k_tile(st), ring.v_tile(st), 0, j * kBS, p.scale_log2);
+        if (fix) fence_proxy_async_smem();  // before the stage's next TMA writes
+      }
+      ring_release(ring, it);
+    }
+    rows.store_partial([&](int r) -> float* { return part_o + (warp * 16 + r) * HD; },
+                       [&](int r) -> float* { return part_ml + (warp * 16 + r) * 2; });
+  }
+  pdl_launch_dependents();  // after this CTA's wait: the main kernel may be scheduled
+
+  cluster_sync();  // every CTA's partial is in its shared memory
+  // CTA `rank` combines pieces [rank E / K, (rank + 1) E / K) of four
+  // elements of the chunk's rows x head_dim (row i: query head i % rep of
+  // sequence i / rep), every peer's values loaded in one round trip
+  constexpr int V4 = HD / 4;
+  const int E = ns * p.rep * V4;
+  const int e0 = static_cast<int>(int64_t(rank) * E / K);
+  const int e1 = static_cast<int>(int64_t(rank + 1) * E / K);
+  T* out = static_cast<T*>(p.out);
+  const int64_t seed = int64_t(p.prefix_seed_run) * p.B * p.n_heads;
+  for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += static_cast<int>(blockDim.x)) {
+    const int i = e / V4, d = (e - (e / V4) * V4) * 4;
+    const int t = i / p.rep, r = i - (i / p.rep) * p.rep;
+    const int prow = (t / spm) * 16 + (t - (t / spm) * spm) * p.rep + r;
+    float2 ml[kMaxCluster];
+    float4 oc[kMaxCluster];
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      ml[c] = make_float2(-INFINITY, 0.f);
+      oc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < K) {
+        ml[c] = ld_cluster_f32x2(cluster_map(part_ml + prow * 2, c));
+        oc[c] = ld_cluster_f32x4(cluster_map(part_o + prow * HD + d, c));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c)
+      if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);  // a run that saw no key has no weight
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      if (ml[c].y > 0.f) {
+        const float w = fast_exp2(ml[c].x - M) * ml[c].y;
+        den += w;
+        acc = make_float4(fmaf(w, oc[c].x, acc.x), fmaf(w, oc[c].y, acc.y), fmaf(w, oc[c].z, acc.z),
+                          fmaf(w, oc[c].w, acc.w));
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const float4 v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    const int L = len_s[t];
+    const int64_t orow = int64_t(s0 + t) * p.n_heads + head * p.rep + r;
+    if (L <= pre_len) {
+      T* o = out + orow * HD + d;
+      o[0] = Elem<T>::from_f(v.x);
+      o[1] = Elem<T>::from_f(v.y);
+      o[2] = Elem<T>::from_f(v.z);
+      o[3] = Elem<T>::from_f(v.w);
+      // with append, this sequence's token would belong in a shared block
+      // (other sequences read it): not written, reported
+      if (p.k_new != nullptr && L > 0 && head == 0 && r == 0 && d == 0) report(p.err, PKV_DEVERR_PREFIX);
+    } else {
+      *reinterpret_cast<float4*>(p.pre_o + (seed + orow) * HD + d) = v;
+      if (d == 0) *reinterpret_cast<float2*>(p.pre_ml + (seed + orow) * 2) = make_float2(M, den);
+    }
+  }
+  cluster_sync();  // the peers have read this CTA's partials
+}
+
 // Shared-prefix attention: the first prefix_blocks table entries are the
 // same blocks for every sequence (a common prompt), so they are read once
 // for a whole chunk of sequences instead of once per sequence.  The prefix
@@ -1934,7 +2322,7 @@ __global__ void __launch_bounds__(decode_max_threads<T, HD>())
              [&](int r) { return active(r) ? min(used_len(p, seq_of(r)), pre_len) - 1 : -1; });
   const int hoff = warp * HD * p.elem_bytes;
   for (uint32_t it = 0; it < static_cast<uint32_t>(j1 - j0); ++it) {
-    if (*ring.abort_flag || !ring_wait_full(ring, it, p.err)) {
+    if (!ring_wait_full(ring, it, p.err)) {
       *ring.abort_flag = 1;
       return;
     }
@@ -2113,7 +2501,7 @@ __global__ void __launch_bounds__(288) prefill_kernel(PrefillParams p) {
     // this warp's last visible key (its rows beyond it are masked anyway)
     const int my_last = L - c + min(c, qw + p.queries_per_warp) - 1;
     for (int k = 0; k < n_blocks; ++k) {
-      if (*ring.abort_flag || !ring_wait_full(ring, k, p.err)) {
+      if (!ring_wait_full(ring, k, p.err)) {
         *ring.abort_flag = 1;
         return;
       }
@@ -2246,6 +2634,122 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
         *reinterpret_cast<uint2*>(out + e) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
       }
     }
+  }
+}
+
+// Merge of the fused shared-prefix call: per (sequence, KV-head group),
+// the prompt runs' partials of the group's rows (run slots 0 ..
+// prompt_runs - 1) and, for a sequence that goes past the prefix, the
+// partial(s) of its own blocks (run slot prompt_runs when one CTA walked
+// them all, else the split parts of the CTAs whose ranges hold them), with
+// log-sum-exp weights.  One thread per four outputs, kPrefixMergeThreads
+// per CTA (a group's rows take one or more CTAs); the runs' loads and the
+// plan numbers go out together, then the parts' loads.  It also reports a
+// table that leaves row 0's prefix blocks where the sequence reaches them,
+// and with append a sequence whose new token would land in a shared block.
+constexpr int kPrefixMergeThreads = 128;
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(kPrefixMergeThreads) decode_prefix_merge_kernel(DecodeParams p) {
+  pdl_launch_dependents();
+  if (p.planned && !plan_matches(p, p.grid)) return;  // reported by the main kernel
+  const int rows = p.hg_size * p.rep;
+  const int slices = (rows * HD / 4 + kPrefixMergeThreads - 1) / kPrefixMergeThreads;
+  const int gs = static_cast<int>(blockIdx.x) / slices;
+  const int slice = static_cast<int>(blockIdx.x) - gs * slices;
+  const int b = gs / p.n_groups, grp = gs - (gs / p.n_groups) * p.n_groups;
+  const int t = threadIdx.x;
+  const int L = used_len(p, b);  // lengths and tables are inputs: read before the wait
+  const int P = p.prefix_blocks;
+  if (grp == 0 && slice == 0) {
+    const int reach = min(P, (L + kBS - 1) / kBS);
+    for (int j = t; j < reach; j += kPrefixMergeThreads)
+      if (__ldg(p.bt + int64_t(b) * p.W + j) != __ldg(p.bt + j)) report(p.err, PKV_DEVERR_PREFIX);
+    if (t == 0 && p.k_new != nullptr && L > 0 && L <= P * kBS) report(p.err, PKV_DEVERR_PREFIX);
+  }
+  const int E = rows * HD;
+  const int e = (slice * kPrefixMergeThreads + t) * 4;  // this thread's four outputs
+  if (e >= E) return;
+  const int nblk = walked_blocks(p, L);
+  const int64_t row = int64_t(b) * p.n_heads + grp * rows + e / HD;  // output row
+  const int d = e % HD;
+  const int64_t run_rows = int64_t(p.B) * p.n_heads;
+  pdl_wait();  // the main kernel's partials
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float M = -INFINITY, den = 0.f;
+  auto fold = [&](float4 o, float2 ml) {
+    if (ml.y > 0.f) {  // a part that saw no key has no weight
+      const float Mn = fmaxf(M, ml.x);
+      const float a = fast_exp2(M - Mn);
+      const float w = fast_exp2(ml.x - Mn) * ml.y;
+      acc = make_float4(fmaf(w, o.x, acc.x * a), fmaf(w, o.y, acc.y * a), fmaf(w, o.z, acc.z * a),
+                        fmaf(w, o.w, acc.w * a));
+      den = fmaf(den, a, w);
+      M = Mn;
+    }
+  };
+  // round 1: every prompt run's piece, and where the group's own blocks went
+  float4 po[kMaxPrefixRuns];
+  float2 pml[kMaxPrefixRuns];
+#pragma unroll
+  for (int k = 0; k < kMaxPrefixRuns; ++k) {
+    if (k < p.prompt_runs) {
+      po[k] = __ldcg(reinterpret_cast<const float4*>(p.pre_o + (k * run_rows + row) * HD + d));
+      pml[k] = __ldcg(reinterpret_cast<const float2*>(p.pre_ml + (k * run_rows + row) * 2));
+    } else {
+      po[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      pml[k] = make_float2(-INFINITY, 0.f);
+    }
+  }
+  const int G = p.grid;
+  const int U = nblk > 0 ? __ldcg(p.total_units) : 0;
+  const int u0 = nblk > 0 ? __ldcg(p.cu_units + b) + grp * nblk : 0;
+#pragma unroll
+  for (int k = 0; k < kMaxPrefixRuns; ++k) fold(po[k], pml[k]);
+  if (nblk > 0) {
+    auto owner = [&](int u) {  // largest c with range_begin(c) <= u
+      int lo = 0, hi = G;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (range_begin(mid, U, G) <= u) lo = mid; else hi = mid;
+      }
+      return lo;
+    };
+    const int c0 = owner(u0), c1 = owner(u0 + nblk - 1);
+    if (c0 == c1) {  // one CTA walked them all
+      const int64_t wrow = int64_t(p.prompt_runs) * run_rows + row;
+      fold(__ldcg(reinterpret_cast<const float4*>(p.pre_o + wrow * HD + d)),
+           __ldcg(reinterpret_cast<const float2*>(p.pre_ml + wrow * 2)));
+    } else {
+      // round 2: the split parts, kParts CTAs' at a time
+      constexpr int kParts = 8;
+      const int first_slot = range_begin(c0, U, G) == u0 ? 2 * c0 : 2 * c0 + 1;
+      const int pr = e / HD;  // row within the group
+      for (int cs = c0; cs <= c1; cs += kParts) {
+        float4 o[kParts];
+        float2 ml[kParts];
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) {
+          const int c = cs + k;
+          const bool has = c <= c1 && (c == c0 || range_begin(c + 1, U, G) > range_begin(c, U, G));
+          const int slot = c == c0 ? first_slot : 2 * c;
+          o[k] = has ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + int64_t(slot) * E + e))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+          ml[k] = has ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (int64_t(slot) * rows + pr) * 2))
+                      : make_float2(-INFINITY, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) fold(o[k], ml[k]);
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const float4 v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  T* out = static_cast<T*>(p.out) + row * HD + d;
+  if constexpr (std::is_same<T, float>::value) {
+    *reinterpret_cast<float4*>(out) = v;
+  } else {  // four bf16 in one 8-byte store
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
   }
 }
 
@@ -2439,6 +2943,118 @@ struct DecodeLaunch {
     }
     return best;
   }
+  // Shape of the wide shared-prefix pass (K = 0: not used): K CTAs per
+  // cluster (runs of the prefix), mt consumer warps of 16 rows, `seqs`
+  // sequences per chunk, `chunks` chunks, a ring of `stages` one-head tiles.
+  // Chosen (tile path, grid left to the library) when the prefix bytes it
+  // saves against the cluster path (which reads the prefix once per chunk
+  // of at most a tile's rows) exceed about what its two extra launches and
+  // its partials cost, 16 MB of reads; K for the fewest prefix blocks per
+  // CTA times the waves of clusters the device holds at once.
+  struct WideShape {
+    int K = 0, mt = 0, seqs = 0, chunks = 0, stages = 0;
+    size_t part_off = 0, smem = 0;
+  };
+  static constexpr int kWideSmemMax = 200 * 1024;
+  static cudaError_t wide_setup(int threads) {
+    static KernelSetup setup;
+    return kernel_setup(setup, decode_prefix_wide_kernel<T, HD>, kWideSmemMax, threads, nullptr);
+  }
+  static WideShape wide_shape(const AttnArgs& a, const ClusterShape& cs) {
+    WideShape w;
+    if constexpr (MMA) {
+      const int P = a.prefix_blocks;
+      if (a.max_ctas != 0 || P == 0 || a.num_seqs <= 0) return w;
+      const int rep = a.n_heads / a.pool.n_kv;
+      const int spm = kMaxRep / rep;
+      const int mt_max = std::min(wide_max_warps<HD>(), (a.num_seqs + spm - 1) / spm);
+      const int64_t prefix_bytes = int64_t(P) * kBS * a.pool.n_kv * HD * 2 * 2;
+      const int64_t cluster_reads =
+          (a.num_seqs + (cs.C > 0 ? cs.spc : spm) - 1) / (cs.C > 0 ? cs.spc : spm);
+      const int64_t min_reads = (a.num_seqs + mt_max * spm - 1) / (mt_max * spm);
+      if ((cluster_reads - min_reads) * prefix_bytes < (int64_t(16) << 20)) return w;
+      static ClusterOccupancy occ;
+      const int sms = sm_count();
+      double best = -1.0;
+      // candidates: 16-row tiles per CTA (mt_max, half, quarter) x runs;
+      // cost = waves x blocks per CTA x a block's time on one SM for mt
+      // warps (measured: 4, 2 and 1 warps per scheduler take about 218,
+      // 301 and 450 cycles per warp-block) x CTAs sharing an SM
+      for (int mt = mt_max; mt >= 1; mt = mt > 1 ? std::max(1, mt / 2) : 0) {
+        const int threads = (mt + 1) * 32;
+        if (wide_setup(threads) != cudaSuccess) {
+          cudaGetLastError();
+          return WideShape{};
+        }
+        const int seqs = mt * spm;
+        const int chunks = (a.num_seqs + seqs - 1) / seqs;
+        const int per_sched = (mt + 3) / 4;
+        const double warp_block = per_sched >= 4 ? 218.0 : per_sched == 3 ? 250.0 : per_sched == 2 ? 301.0 : 450.0;
+        const double cta_block = warp_block * per_sched;
+        const int64_t clusters = int64_t(chunks) * a.pool.n_kv;
+        for (int K = 1; K <= std::min(kMaxCluster, P); ++K) {
+          const int per = (P + K - 1) / K;
+          const int stages = std::max(2, std::min(16, per));
+          const size_t part_off =
+              (kBarrierBytes + 1024 + size_t(stages) * 2 * kBS * HD * 2 + 15) / 16 * 16;
+          const size_t smem = part_off + size_t(mt) * 16 * (HD + 2) * 4;
+          if (smem > size_t(kWideSmemMax)) continue;
+          const int at_once = max_active_clusters(occ, decode_prefix_wide_kernel<T, HD>, K,
+                                                  static_cast<int>(smem), threads);
+          if (at_once <= 0) continue;
+          const int64_t waves = (clusters + at_once - 1) / at_once;
+          const int64_t in_wave = std::min<int64_t>(clusters, at_once) * K;
+          const double cost = double(waves) * per * cta_block *
+                              std::max(1.0, double(in_wave) / std::max(1, sms));
+          if (best < 0 || cost < best) {
+            best = cost;
+            w.K = K, w.mt = mt, w.seqs = seqs, w.chunks = chunks, w.stages = stages;
+            w.part_off = part_off, w.smem = smem;
+          }
+        }
+        if (mt == 1) break;
+      }
+    }
+    return w;
+  }
+  // Shape of the fused shared-prefix call (R = 0: not used): the tile path
+  // with the grid left to the library, when the prefix bytes it saves
+  // against the cluster path exceed 16 MB of reads.  A chunk is the rows of
+  // one tile per consumer warp (hg * 16 / rep sequences); the prefix is cut
+  // into R runs of bpr blocks so that every (chunk, KV head, run) item has
+  // its own CTA, a run fits in the ring beside at least one stage of the
+  // blocks after the prefix (hg one-head blocks per stage) and R run slots
+  // plus one fit in the workspace's prefix partials (max_runs + 1 slots).
+  struct FusedShape {
+    int R = 0, bpr = 0, seqs = 0, chunks = 0, pw = 0;
+    size_t smem = 0;
+  };
+  static FusedShape fused_shape(const AttnArgs& a, const ClusterShape& cs, int hg, int G,
+                                int nstages, int max_runs) {
+    FusedShape f;
+    const int P = a.prefix_blocks;
+    if (!MMA || a.max_ctas != 0 || P == 0 || a.num_seqs <= 0) return f;
+    const int rep = a.n_heads / a.pool.n_kv;
+    const int spm = kMaxRep / rep;
+    const int pw = fused_prompt_warps(hg, fused_max_warps<HD>());
+    if (pw < 1) return f;
+    const int seqs = pw * spm;
+    const int chunks = (a.num_seqs + seqs - 1) / seqs;
+    const int64_t prefix_bytes = int64_t(P) * kBS * a.pool.n_kv * HD * 2 * 2;
+    const int64_t cluster_reads =
+        (a.num_seqs + (cs.C > 0 ? cs.spc : spm) - 1) / (cs.C > 0 ? cs.spc : spm);
+    if ((cluster_reads - chunks) * prefix_bytes < (int64_t(16) << 20)) return f;
+    const int64_t per_run = int64_t(a.pool.n_kv) * chunks;
+    int R = static_cast<int>(std::min<int64_t>({int64_t(max_runs), G / per_run, int64_t(P)}));
+    if (R < 1) return f;
+    const int bpr = (P + R - 1) / R;
+    R = (P + bpr - 1) / bpr;
+    // the ring, then the run's K and V tiles (one head each)
+    const size_t smem = smem_for(hg, a.pool.elem_bytes(), nstages) + size_t(bpr) * 2 * kBS * HD * 2;
+    if (bpr > 32 || smem > size_t(kClusterSmemMax)) return f;
+    f.R = R, f.bpr = bpr, f.seqs = seqs, f.chunks = chunks, f.smem = smem, f.pw = pw;
+    return f;
+  }
   // Persistent grid: every SM filled with as many CTAs as fit, capped by
   // max_ctas; *wave (optional) = the uncapped full wave.
   static cudaError_t grid(const AttnArgs& a, int hg, int* G, size_t* smem, int* nstages,
@@ -2532,7 +3148,49 @@ struct DecodeLaunch {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     p.planned = a.decode_plan == kPlanned;
-    if (const ClusterShape cs = cluster_shape(a, hg, wave, p.nstages); cs.C > 0) {
+    const ClusterShape cs = cluster_shape(a, hg, wave, p.nstages);
+    const FusedShape fused = p.prefix_blocks > 0
+                                 ? fused_shape(a, cs, hg, G, p.nstages, p.prefix_chunks)
+                                 : FusedShape{};
+    if (fused.R > 0) {
+      // a long prefix shared by many sequences: one launch attends both the
+      // prefix (runs x chunks x KV heads, one per CTA) and each sequence's
+      // own blocks (stream-K), the prefix merge combines them
+      if constexpr (MMA) {
+        p.prompt_runs = fused.R;
+        p.prompt_bpr = fused.bpr;
+        p.prompt_seqs = fused.seqs;
+        p.prompt_items = fused.R * pool.n_kv * fused.chunks;
+        p.wide_mt = fused.pw;
+        p.plan_in_kernel = 0;
+        if (!p.planned) {
+          decode_plan_kernel<T, HD><<<1, 1024, 0, stream>>>(p);
+          if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        static KernelSetup fused_setup;
+        e = kernel_setup(fused_setup, decode_fused_prefix_kernel<T, HD>, static_cast<int>(fused.smem),
+                         (hg + 1 + fused.pw) * 32, nullptr);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t fcfg = {};
+        fcfg.gridDim = dim3(G);
+        fcfg.blockDim = dim3((hg + 1 + fused.pw) * 32);
+        fcfg.dynamicSmemBytes = fused.smem;
+        fcfg.stream = stream;
+        fcfg.attrs = attr;
+        fcfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&fcfg, decode_fused_prefix_kernel<T, HD>, tm_k, tm_v, p);
+        if (e != cudaSuccess) return e;
+        const int slices = (hg * p.rep * HD / 4 + kPrefixMergeThreads - 1) / kPrefixMergeThreads;
+        fcfg.gridDim = dim3(static_cast<unsigned>(int64_t(p.B) * p.n_groups * slices));
+        fcfg.blockDim = dim3(kPrefixMergeThreads);
+        fcfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&fcfg, decode_prefix_merge_kernel<T, HD>, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+      }
+    }
+    const WideShape wide = p.prefix_blocks > 0 ? wide_shape(a, cs) : WideShape{};
+    if (cs.C > 0 && wide.K == 0) {
       // latency-bound batch, or a shared prefix: one cluster of C CTAs per
       // (chunk of spc sequences, head group), partials combined in
       // distributed shared memory
@@ -2568,7 +3226,44 @@ struct DecodeLaunch {
       if (e != cudaSuccess) return e;
       return cudaGetLastError();
     }
-    if (p.prefix_blocks > 0) {
+    if (wide.K > 0) {
+      // a long prefix shared by many sequences: one pass per KV head and
+      // chunk of up to 16 tiles of rows, its runs combined in the cluster;
+      // the seed is run slot 0
+      if constexpr (MMA) {
+        DecodeParams pw = p;
+        pw.cluster = wide.K;
+        pw.cluster_seqs = wide.seqs;
+        pw.wide_mt = wide.mt;
+        pw.wide_evict = wide.chunks == 1;
+        pw.nstages = wide.stages;
+        pw.part_off = static_cast<int>(wide.part_off);
+        pw.prefix_seed_run = 0;
+        CUtensorMap wk{}, wv{};
+        const uint64_t dims[4] = {64, uint64_t(pool.num_blocks) * kBS, HD / 64, uint64_t(pool.n_kv)};
+        const uint64_t strides[3] = {uint64_t(pool.n_kv) * HD * 2, 128, uint64_t(HD) * 2};
+        const uint32_t box[4] = {64, kBS, HD / 64, 1};
+        if (!encode_bf16_sw128(&wk, a.k_pool, 4, dims, strides, box) ||
+            !encode_bf16_sw128(&wv, a.v_pool, 4, dims, strides, box))
+          return cudaErrorInvalidValue;
+        cudaLaunchAttribute wattr[2];
+        wattr[0] = attr[0];
+        wattr[1].id = cudaLaunchAttributeClusterDimension;
+        wattr[1].val.clusterDim.x = static_cast<unsigned>(wide.K);
+        wattr[1].val.clusterDim.y = 1;
+        wattr[1].val.clusterDim.z = 1;
+        cudaLaunchConfig_t wcfg = {};
+        wcfg.gridDim = dim3(static_cast<unsigned>(int64_t(wide.chunks) * pool.n_kv * wide.K));
+        wcfg.blockDim = dim3((wide.mt + 1) * 32);
+        wcfg.dynamicSmemBytes = wide.smem;
+        wcfg.stream = stream;
+        wcfg.attrs = wattr;
+        wcfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&wcfg, decode_prefix_wide_kernel<T, HD>, wk, wv, pw);
+        if (e != cudaSuccess) return e;
+        p.prefix_seed_run = 0;
+      }
+    } else if (p.prefix_blocks > 0) {
       // the shared prefix: runs of its blocks, each read once per head group
       // for a chunk of sequences (same ring and shared memory as below)
       static KernelSetup prefix_setup;

@@ -182,3 +182,124 @@ def test_shared_prefix_planned_append_edges(shape, P):
     o.kp, o.vp = oracle.kv_write(o.raw["k"][:nd], o.raw["v"][:nd], slots, o.raw["k_pool"],
                                  o.raw["v_pool"])
     assert_close(f64(out)[past], o.decode(rows=past)[past], dt, f"P={P}")
+
+
+# Long prompts shared by many sequences take the wide prefix pass (one read
+# of the prompt per KV head for up to 16 tiles of rows); these shapes are
+# past its threshold.  (n_heads, n_kv, head_dim, batch, prefix blocks)
+WIDE = [(32, 8, 64, 256, 32), (64, 8, 128, 100, 40), (9, 3, 64, 200, 64), (16, 16, 64, 300, 24)]
+
+
+def _wide_lens(rng, B, P):
+    pre = 16 * P
+    lens = rng.integers(pre + 1, pre + 300, size=B)
+    # inside, at the end of and just past the prompt; empty
+    lens[:8] = [0, 1, pre - 17, pre - 1, pre, pre + 1, pre + 15, pre + 16]
+    return rng.permutation(lens).tolist()
+
+
+@pytest.mark.parametrize("shape", WIDE, ids=[f"{h}x{k}x{d}-B{b}-P{p}" for h, k, d, b, p in WIDE])
+def test_shared_prefix_wide_pass(shape):
+    """Every row against the oracle and the plain decode."""
+    H, K, D, B, P = shape
+    rng = np.random.default_rng(H + B)
+    lens = _wide_lens(rng, B, P)
+    nb = P + sum(max(0, (l + 15) // 16 - P) for l in lens) + 8
+    plan = _plan_with_prefix(lens, P, H, K, D, "bf16", seed=B, num_blocks=nb)
+    layer = make_tiny_layer(plan, seed=P, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.kp, o.vp = o.raw["k_pool"], o.raw["v_pool"]
+    shared = _prefix_decode(g, P)
+    plain = g.decode()
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert_close(f64(shared), o.decode(), "bf16", f"wide {shape}")
+    assert_close(f64(shared), f64(plain), "bf16", "vs plain decode")
+
+
+def test_shared_prefix_wide_pass_reports_foreign_tables():
+    """A row whose table leaves the prompt where its length reaches is
+    reported; rows that stop before the differing entry are not."""
+    H, K, D, B, P = 32, 8, 64, 256, 32
+    rng = np.random.default_rng(5)
+    lens = rng.integers(16 * P + 1, 16 * P + 200, size=B).tolist()
+    lens[7] = 16 * 10  # stops before block 10
+    nb = P + sum(max(0, (l + 15) // 16 - P) for l in lens) + 8
+    plan = _plan_with_prefix(lens, P, H, K, D, "bf16", seed=6, num_blocks=nb)
+    layer = make_tiny_layer(plan, seed=6)
+    plan.block_tables[7, 10] = plan.block_tables[7, 11]  # beyond its length: not reported
+    g = GpuStep(plan, layer)
+    _prefix_decode(g, P)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    plan.block_tables[200, 20] = plan.block_tables[200, P]  # inside its length
+    g = GpuStep(plan, layer)
+    _prefix_decode(g, P)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) & PKV_DEVERR_PREFIX
+
+
+@pytest.mark.parametrize("shape", WIDE[:2], ids=[f"{h}x{k}x{d}" for h, k, d, _, _ in WIDE[:2]])
+def test_shared_prefix_wide_pass_planned_append(shape):
+    """Planned, with the step's K/V fused in: bit-identical to pkv_kv_write
+    of the rows past the prompt followed by the planned call without k_new;
+    rows ending inside the prompt reported and not written."""
+    import oracle
+    from gpu_step import guarded_copy, guarded_empty
+    H, K, D, B, P = shape
+    rng = np.random.default_rng(D + B)
+    lens = _wide_lens(rng, B, P)
+    nb = P + sum(max(0, (l + 15) // 16 - P) for l in lens) + 8
+    plan = _plan_with_prefix(lens, P, H, K, D, "bf16", seed=D, num_blocks=nb)
+    layer = make_tiny_layer(plan, seed=D)
+    g = GpuStep(plan, layer)
+    nd, t, sh = g.nd, g.t, g.sh
+    past = [b for b in range(nd) if lens[b] > 16 * P]
+    slots = np.full(nd, -1, dtype=np.int64)
+    for b in past:
+        slots[b] = oracle.slot_of(plan.block_tables[b], lens[b] - 1, 16)
+    k_new, v_new = t["k"][:nd].contiguous(), t["v"][:nd].contiguous()
+    kp1, vp1 = guarded_copy(t["k_pool"]), guarded_copy(t["v_pool"])
+    kp2, vp2 = guarded_copy(t["k_pool"]), guarded_copy(t["v_pool"])
+    ws = guarded_empty((pkv.decode_shared_prefix_workspace_bytes(nd, H, D, g.max_dec, P),),
+                       torch.uint8)
+    ws.zero_()
+    errs = [guarded_empty((1,), torch.int32) for _ in range(2)]
+    for e in errs:
+        e.zero_()
+    pkv.decode_plan(t["k_pool"], g.seq_lens[:nd], H, g.bt.shape[1], g.max_dec, workspace=ws,
+                    shared_prefix_blocks=P, err=errs[0])
+    pkv.kv_write(k_new, v_new, torch.from_numpy(slots).cuda(), kp1, vp1, err=errs[0])
+    ref = pkv.paged_attention_decode_planned(t["q"][:nd], kp1, vp1, g.bt[:nd], g.seq_lens[:nd],
+                                             sh.scale, g.max_dec, workspace=ws,
+                                             shared_prefix_blocks=P, err=errs[0])
+    out = pkv.paged_attention_decode_planned(t["q"][:nd], kp2, vp2, g.bt[:nd], g.seq_lens[:nd],
+                                             sh.scale, g.max_dec, workspace=ws, k_new=k_new,
+                                             v_new=v_new, shared_prefix_blocks=P, err=errs[1])
+    torch.cuda.synchronize()
+    assert int(errs[0].item()) == 0
+    assert int(errs[1].item()) == PKV_DEVERR_PREFIX
+    rows = torch.tensor(past, device="cuda")
+    assert torch.equal(out[rows].view(torch.int16), ref[rows].view(torch.int16))
+    assert torch.equal(kp2.view(torch.int16), kp1.view(torch.int16))
+    assert torch.equal(vp2.view(torch.int16), vp1.view(torch.int16))
+    o = OracleStep(plan, layer)
+    o.kp, o.vp = oracle.kv_write(o.raw["k"][:nd], o.raw["v"][:nd], slots, o.raw["k_pool"],
+                                 o.raw["v_pool"])
+    assert_close(f64(out)[past], o.decode(rows=past)[past], "bf16", f"wide append {shape}")
+
+
+def test_shared_prefix_wide_pass_short_rows_nan_slots():
+    """No sequence reaches the end of the prompt: its last slots hold NaN,
+    which no output may see."""
+    H, K, D, B, P = 32, 8, 64, 256, 32
+    rng = np.random.default_rng(9)
+    lens = rng.integers(0, 16 * P - 5, size=B).tolist()
+    plan = _plan_with_prefix(lens, P, H, K, D, "bf16", seed=9, num_blocks=P + 8)
+    layer = make_tiny_layer(plan, seed=9, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.kp, o.vp = o.raw["k_pool"], o.raw["v_pool"]
+    out = _prefix_decode(g, P)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert_close(f64(out), o.decode(), "bf16", "short rows")
