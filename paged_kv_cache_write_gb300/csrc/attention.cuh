@@ -705,6 +705,10 @@ struct DecodeParams {
   // Every group after the prefix then leaves a partial too (a whole one in
   // run slot prompt_runs) and the prefix merge kernel combines them.
   int prompt_items, prompt_runs, prompt_bpr, prompt_seqs;
+  // fused shared prefix, per (sequence, KV-head group), from the plan: the
+  // first and last CTA whose ranges hold the group's blocks after the
+  // prefix and the first CTA's partial slot (c0 = -1: none)
+  int4* gparts;
   float scale_log2;
 };
 
@@ -897,6 +901,29 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     // a plan kept for later calls also fixes which split group each merge
     // CTA merges, so those calls' merge CTAs can read it before they wait
     if (p.plan_only) p.splits[c] = sp;
+  }
+  if (p.prompt_items > 0) {
+    // fused shared prefix: where each (sequence, group)'s blocks after the
+    // prefix went, for the prefix merge
+    auto owner = [&](int u) {  // largest c with range_begin(c) <= u
+      int lo = 0, hi = p.grid;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (range_begin(mid, U, p.grid) <= u) lo = mid; else hi = mid;
+      }
+      return lo;
+    };
+    for (int i = tid; i < p.B * p.n_groups; i += blockDim.x) {
+      const int b = i / p.n_groups, grp = i - (i / p.n_groups) * p.n_groups;
+      const int nblk = (cu[b + 1] - cu[b]) / p.n_groups;
+      int4 gp = make_int4(-1, -1, 0, 0);
+      if (nblk > 0) {
+        const int u0 = cu[b] + grp * nblk;
+        const int c0 = owner(u0);
+        gp = make_int4(c0, owner(u0 + nblk - 1), range_begin(c0, U, p.grid) == u0 ? 2 * c0 : 2 * c0 + 1, 0);
+      }
+      p.gparts[i] = gp;
+    }
   }
   if (p.plan_only || p.prompt_items > 0) {  // kept for later calls / the prefix merge
     if (in_smem)
@@ -2643,8 +2670,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
 // partial(s) of its own blocks (run slot prompt_runs when one CTA walked
 // them all, else the split parts of the CTAs whose ranges hold them), with
 // log-sum-exp weights.  One thread per four outputs, kPrefixMergeThreads
-// per CTA (a group's rows take one or more CTAs); the runs' loads and the
-// plan numbers go out together, then the parts' loads.  It also reports a
+// per CTA (a group's rows take one or more CTAs); where the parts are comes
+// from the plan, so all loads go out together.  It also reports a
 // table that leaves row 0's prefix blocks where the sequence reaches them,
 // and with append a sequence whose new token would land in a shared block.
 constexpr int kPrefixMergeThreads = 128;
@@ -2670,11 +2697,18 @@ __global__ void __launch_bounds__(kPrefixMergeThreads) decode_prefix_merge_kerne
   const int E = rows * HD;
   const int e = (slice * kPrefixMergeThreads + t) * 4;  // this thread's four outputs
   if (e >= E) return;
-  const int nblk = walked_blocks(p, L);
   const int64_t row = int64_t(b) * p.n_heads + grp * rows + e / HD;  // output row
   const int d = e % HD;
   const int64_t run_rows = int64_t(p.B) * p.n_heads;
+  // where the group's own blocks went: part of a plan kept for this call
+  // (read before the wait), else written by the preceding plan launch
+  int4 gp = p.planned ? __ldcg(p.gparts + gs) : make_int4(-1, -1, 0, 0);
+  int U = p.planned ? __ldcg(p.total_units) : 0;
   pdl_wait();  // the main kernel's partials
+  if (!p.planned) {
+    gp = __ldcg(p.gparts + gs);
+    U = __ldcg(p.total_units);
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float M = -INFINITY, den = 0.f;
   auto fold = [&](float4 o, float2 ml) {
@@ -2688,7 +2722,10 @@ __global__ void __launch_bounds__(kPrefixMergeThreads) decode_prefix_merge_kerne
       M = Mn;
     }
   };
-  // round 1: every prompt run's piece, and where the group's own blocks went
+  // every load goes out before the first is used: each prompt run's piece,
+  // then the part of the group's own blocks (one CTA walked them all: run
+  // slot prompt_runs) or the first kParts split parts (an empty range's
+  // slot is skipped)
   float4 po[kMaxPrefixRuns];
   float2 pml[kMaxPrefixRuns];
 #pragma unroll
@@ -2701,47 +2738,48 @@ __global__ void __launch_bounds__(kPrefixMergeThreads) decode_prefix_merge_kerne
       pml[k] = make_float2(-INFINITY, 0.f);
     }
   }
+  constexpr int kParts = 8;
   const int G = p.grid;
-  const int U = nblk > 0 ? __ldcg(p.total_units) : 0;
-  const int u0 = nblk > 0 ? __ldcg(p.cu_units + b) + grp * nblk : 0;
+  const int pr = e / HD;  // row within the group
+  const int c0 = gp.x, c1 = gp.y;
+  auto load_parts = [&](int cs, float4 (&o)[kParts], float2 (&ml)[kParts]) {
 #pragma unroll
-  for (int k = 0; k < kMaxPrefixRuns; ++k) fold(po[k], pml[k]);
-  if (nblk > 0) {
-    auto owner = [&](int u) {  // largest c with range_begin(c) <= u
-      int lo = 0, hi = G;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (range_begin(mid, U, G) <= u) lo = mid; else hi = mid;
+    for (int k = 0; k < kParts; ++k) {
+      const int c = cs + k;
+      bool has = c0 >= 0 && c <= c1;
+      int64_t orow = 0, mrow = 0;
+      const float* ob = p.ws_o;
+      const float* mb = p.ws_ml;
+      if (has && c0 == c1) {  // the whole part, in run slot prompt_runs
+        orow = (int64_t(p.prompt_runs) * run_rows + row) * HD + d;
+        mrow = (int64_t(p.prompt_runs) * run_rows + row) * 2;
+        ob = p.pre_o;
+        mb = p.pre_ml;
+      } else if (has) {
+        has = c == c0 || range_begin(c + 1, U, G) > range_begin(c, U, G);
+        const int slot = c == c0 ? gp.z : 2 * c;
+        orow = int64_t(slot) * E + e;
+        mrow = (int64_t(slot) * rows + pr) * 2;
       }
-      return lo;
-    };
-    const int c0 = owner(u0), c1 = owner(u0 + nblk - 1);
-    if (c0 == c1) {  // one CTA walked them all
-      const int64_t wrow = int64_t(p.prompt_runs) * run_rows + row;
-      fold(__ldcg(reinterpret_cast<const float4*>(p.pre_o + wrow * HD + d)),
-           __ldcg(reinterpret_cast<const float2*>(p.pre_ml + wrow * 2)));
-    } else {
-      // round 2: the split parts, kParts CTAs' at a time
-      constexpr int kParts = 8;
-      const int first_slot = range_begin(c0, U, G) == u0 ? 2 * c0 : 2 * c0 + 1;
-      const int pr = e / HD;  // row within the group
-      for (int cs = c0; cs <= c1; cs += kParts) {
-        float4 o[kParts];
-        float2 ml[kParts];
-#pragma unroll
-        for (int k = 0; k < kParts; ++k) {
-          const int c = cs + k;
-          const bool has = c <= c1 && (c == c0 || range_begin(c + 1, U, G) > range_begin(c, U, G));
-          const int slot = c == c0 ? first_slot : 2 * c;
-          o[k] = has ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + int64_t(slot) * E + e))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-          ml[k] = has ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (int64_t(slot) * rows + pr) * 2))
-                      : make_float2(-INFINITY, 0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < kParts; ++k) fold(o[k], ml[k]);
-      }
+      o[k] = has ? __ldcg(reinterpret_cast<const float4*>(ob + orow)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      ml[k] = has ? __ldcg(reinterpret_cast<const float2*>(mb + mrow)) : make_float2(-INFINITY, 0.f);
     }
+  };
+  {
+    float4 o[kParts];
+    float2 ml[kParts];
+    load_parts(c0, o, ml);
+#pragma unroll
+    for (int k = 0; k < kMaxPrefixRuns; ++k) fold(po[k], pml[k]);
+#pragma unroll
+    for (int k = 0; k < kParts; ++k) fold(o[k], ml[k]);
+  }
+  for (int cs = c0 + kParts; c0 >= 0 && cs <= c1; cs += kParts) {  // long split groups
+    float4 o[kParts];
+    float2 ml[kParts];
+    load_parts(cs, o, ml);
+#pragma unroll
+    for (int k = 0; k < kParts; ++k) fold(o[k], ml[k]);
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   const float4 v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -2791,10 +2829,12 @@ inline int prefix_runs(int num_seqs, int n_groups, int seqs_per_cta, int prefix_
 // [runs][B][n_heads][HD] and max/sum [runs][B][n_heads][2]; each region
 // 256-byte aligned.
 struct DecodeWs {
-  size_t cu, starts, splits, total_units, ml, o, pre_o, pre_ml, total;
+  size_t cu, starts, splits, total_units, ml, o, pre_o, pre_ml, gparts, total;
   // prefix_heads: runs x n_heads with a shared prefix (its partials
-  // follow), else 0
-  DecodeWs(int num_seqs, size_t G, size_t rows_per_group, int head_dim, int prefix_heads = 0) {
+  // follow), else 0; prefix_groups: KV-head groups per sequence with a
+  // shared prefix (where each group's parts are, for the prefix merge)
+  DecodeWs(int num_seqs, size_t G, size_t rows_per_group, int head_dim, int prefix_heads = 0,
+           int prefix_groups = 0) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     cu = 0;
     starts = up(size_t(num_seqs + 1) * 4);
@@ -2804,7 +2844,8 @@ struct DecodeWs {
     o = ml + up(2 * G * rows_per_group * 2 * 4);
     pre_o = o + up(2 * G * rows_per_group * size_t(head_dim) * 4);
     pre_ml = pre_o + up(size_t(num_seqs) * prefix_heads * head_dim * 4);
-    total = pre_ml + size_t(num_seqs) * prefix_heads * 2 * 4;
+    gparts = pre_ml + up(size_t(num_seqs) * prefix_heads * 2 * 4);
+    total = gparts + size_t(num_seqs) * prefix_groups * 16;
   }
 };
 
@@ -3019,7 +3060,8 @@ struct DecodeLaunch {
   }
   // Shape of the fused shared-prefix call (R = 0: not used): the tile path
   // with the grid left to the library, when the prefix bytes it saves
-  // against the cluster path exceed 16 MB of reads.  A chunk is the rows of
+  // against the cluster path exceed 16 MB of reads (a function of the
+  // sizes only, so that a plan and the calls using it agree).  A chunk is the rows of
   // one tile per consumer warp (hg * 16 / rep sequences); the prefix is cut
   // into R runs of bpr blocks so that every (chunk, KV head, run) item has
   // its own CTA, a run fits in the ring beside at least one stage of the
@@ -3029,8 +3071,7 @@ struct DecodeLaunch {
     int R = 0, bpr = 0, seqs = 0, chunks = 0, pw = 0;
     size_t smem = 0;
   };
-  static FusedShape fused_shape(const AttnArgs& a, const ClusterShape& cs, int hg, int G,
-                                int nstages, int max_runs) {
+  static FusedShape fused_shape(const AttnArgs& a, int hg, int G, int nstages, int max_runs) {
     FusedShape f;
     const int P = a.prefix_blocks;
     if (!MMA || a.max_ctas != 0 || P == 0 || a.num_seqs <= 0) return f;
@@ -3040,9 +3081,10 @@ struct DecodeLaunch {
     if (pw < 1) return f;
     const int seqs = pw * spm;
     const int chunks = (a.num_seqs + seqs - 1) / seqs;
+    // (the cluster path reads the prefix once per chunk of at most a tile's
+    // spm sequences; the plan and every call using it decide alike)
     const int64_t prefix_bytes = int64_t(P) * kBS * a.pool.n_kv * HD * 2 * 2;
-    const int64_t cluster_reads =
-        (a.num_seqs + (cs.C > 0 ? cs.spc : spm) - 1) / (cs.C > 0 ? cs.spc : spm);
+    const int64_t cluster_reads = (a.num_seqs + spm - 1) / spm;
     if ((cluster_reads - chunks) * prefix_bytes < (int64_t(16) << 20)) return f;
     const int64_t per_run = int64_t(a.pool.n_kv) * chunks;
     int R = static_cast<int>(std::min<int64_t>({int64_t(max_runs), G / per_run, int64_t(P)}));
@@ -3114,7 +3156,7 @@ struct DecodeLaunch {
                                     &p.prefix_bpc);
     p.prefix_seed_run = p.prefix_chunks;
     const DecodeWs L(a.num_seqs, G, size_t(hg) * p.rep, HD,
-                     prefix_slots(p.prefix_chunks) * a.n_heads);
+                     prefix_slots(p.prefix_chunks) * a.n_heads, p.prefix_blocks > 0 ? p.n_groups : 0);
     if (L.total > a.workspace_bytes) return cudaErrorInvalidValue;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     p.cu_units = reinterpret_cast<int32_t*>(ws + L.cu);
@@ -3125,6 +3167,20 @@ struct DecodeLaunch {
     p.ws_o = reinterpret_cast<float*>(ws + L.o);
     p.pre_o = reinterpret_cast<float*>(ws + L.pre_o);
     p.pre_ml = reinterpret_cast<float*>(ws + L.pre_ml);
+    p.gparts = reinterpret_cast<int4*>(ws + L.gparts);
+    // the launch shape (a plan made for later calls records what the fused
+    // shared-prefix merge needs)
+    const ClusterShape cs = cluster_shape(a, hg, wave, p.nstages);
+    const FusedShape fused = p.prefix_blocks > 0
+                                 ? fused_shape(a, hg, G, p.nstages, p.prefix_chunks)
+                                 : FusedShape{};
+    if (fused.R > 0) {
+      p.prompt_runs = fused.R;
+      p.prompt_bpr = fused.bpr;
+      p.prompt_seqs = fused.seqs;
+      p.prompt_items = fused.R * pool.n_kv * fused.chunks;
+      p.wide_mt = fused.pw;
+    }
     if (a.decode_plan == kPlanOnly) {  // the plan alone, kept in the workspace
       p.plan_only = 1;
       p.out = nullptr;
@@ -3148,20 +3204,11 @@ struct DecodeLaunch {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     p.planned = a.decode_plan == kPlanned;
-    const ClusterShape cs = cluster_shape(a, hg, wave, p.nstages);
-    const FusedShape fused = p.prefix_blocks > 0
-                                 ? fused_shape(a, cs, hg, G, p.nstages, p.prefix_chunks)
-                                 : FusedShape{};
     if (fused.R > 0) {
       // a long prefix shared by many sequences: one launch attends both the
       // prefix (runs x chunks x KV heads, one per CTA) and each sequence's
       // own blocks (stream-K), the prefix merge combines them
       if constexpr (MMA) {
-        p.prompt_runs = fused.R;
-        p.prompt_bpr = fused.bpr;
-        p.prompt_seqs = fused.seqs;
-        p.prompt_items = fused.R * pool.n_kv * fused.chunks;
-        p.wide_mt = fused.pw;
         p.plan_in_kernel = 0;
         if (!p.planned) {
           decode_plan_kernel<T, HD><<<1, 1024, 0, stream>>>(p);
@@ -3331,7 +3378,7 @@ size_t decode_exact_workspace(const AttnArgs& a, int hg) {
                        DecodeLaunch<T, HD, MAXR, MMA>::kRowsPerWarp / (a.n_heads / a.pool.n_kv),
                        a.prefix_blocks, &bpc);
   return DecodeWs(a.num_seqs, G, size_t(hg) * (a.n_heads / a.pool.n_kv), HD,
-                  prefix_slots(runs) * a.n_heads)
+                  prefix_slots(runs) * a.n_heads, a.prefix_blocks > 0 ? a.pool.n_kv / hg : 0)
       .total;
 }
 

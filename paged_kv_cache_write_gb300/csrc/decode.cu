@@ -16,11 +16,13 @@ bool decode_supported(const PoolShape& pool, int32_t n_heads) {
 // Upper bound of the decode workspace over every grid this device can run.
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t n_heads, int32_t head_dim, int32_t, int32_t,
                               int32_t shared_prefix_blocks) {
-  // rows per head group <= n_heads; at most 16 resident CTAs per SM
+  // rows per head group <= n_heads, head groups <= n_heads; at most 16
+  // resident CTAs per SM
   return DecodeWs(num_seqs, size_t(sm_count()) * 16, size_t(n_heads), head_dim,
                   shared_prefix_blocks > 0
                       ? prefix_slots(max_prefix_runs(num_seqs, shared_prefix_blocks)) * n_heads
-                      : 0)
+                      : 0,
+                  shared_prefix_blocks > 0 ? n_heads : 0)
       .total;
 }
 

@@ -303,3 +303,82 @@ def test_shared_prefix_wide_pass_short_rows_nan_slots():
     torch.cuda.synchronize()
     assert int(g.err.item()) == 0
     assert_close(f64(out), o.decode(), "bf16", "short rows")
+
+
+# Shapes that take the fused launch (prompt runs beside each sequence's own
+# blocks, then the prefix merge): (n_heads, n_kv, head_dim, batch, prefix blocks)
+FUSED = [(32, 8, 64, 64, 64), (16, 8, 64, 120, 48)]
+
+
+@pytest.mark.parametrize("shape", FUSED, ids=[f"{h}x{k}x{d}-B{b}-P{p}" for h, k, d, b, p in FUSED])
+def test_shared_prefix_fused_launch(shape):
+    """Lengths inside, at and past the prompt, NaN in unused slots: every
+    row against the oracle; the planned call with the step's K/V fused in
+    against pkv_kv_write + the planned call, bit for bit."""
+    import oracle
+    from gpu_step import guarded_copy, guarded_empty
+    H, K, D, B, P = shape
+    rng = np.random.default_rng(B + P)
+    lens = _wide_lens(rng, B, P)
+    nb = P + sum(max(0, (l + 15) // 16 - P) for l in lens) + 8
+    plan = _plan_with_prefix(lens, P, H, K, D, "bf16", seed=P, num_blocks=nb)
+    layer = make_tiny_layer(plan, seed=B, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.kp, o.vp = o.raw["k_pool"], o.raw["v_pool"]
+    out = _prefix_decode(g, P)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert_close(f64(out), o.decode(), "bf16", f"fused {shape}")
+
+    nd, t, sh = g.nd, g.t, g.sh
+    past = [b for b in range(nd) if lens[b] > 16 * P]
+    slots = np.full(nd, -1, dtype=np.int64)
+    for b in past:
+        slots[b] = oracle.slot_of(plan.block_tables[b], lens[b] - 1, 16)
+    k_new, v_new = t["k"][:nd].contiguous(), t["v"][:nd].contiguous()
+    kp1, vp1 = guarded_copy(t["k_pool"]), guarded_copy(t["v_pool"])
+    kp2, vp2 = guarded_copy(t["k_pool"]), guarded_copy(t["v_pool"])
+    ws = guarded_empty((pkv.decode_shared_prefix_workspace_bytes(nd, H, D, g.max_dec, P),),
+                       torch.uint8)
+    ws.zero_()
+    errs = [guarded_empty((1,), torch.int32) for _ in range(2)]
+    for e in errs:
+        e.zero_()
+    pkv.decode_plan(t["k_pool"], g.seq_lens[:nd], H, g.bt.shape[1], g.max_dec, workspace=ws,
+                    shared_prefix_blocks=P, err=errs[0])
+    pkv.kv_write(k_new, v_new, torch.from_numpy(slots).cuda(), kp1, vp1, err=errs[0])
+    ref = pkv.paged_attention_decode_planned(t["q"][:nd], kp1, vp1, g.bt[:nd], g.seq_lens[:nd],
+                                             sh.scale, g.max_dec, workspace=ws,
+                                             shared_prefix_blocks=P, err=errs[0])
+    app = pkv.paged_attention_decode_planned(t["q"][:nd], kp2, vp2, g.bt[:nd], g.seq_lens[:nd],
+                                             sh.scale, g.max_dec, workspace=ws, k_new=k_new,
+                                             v_new=v_new, shared_prefix_blocks=P, err=errs[1])
+    torch.cuda.synchronize()
+    assert int(errs[0].item()) == 0
+    assert int(errs[1].item()) == PKV_DEVERR_PREFIX
+    rows = torch.tensor(past, device="cuda")
+    assert torch.equal(app[rows].view(torch.int16), ref[rows].view(torch.int16))
+    assert torch.equal(kp2.view(torch.int16), kp1.view(torch.int16))
+    assert torch.equal(vp2.view(torch.int16), vp1.view(torch.int16))
+    # the planned call without k_new on unchanged pools is the unplanned one
+    # up to the order of its sums: against the oracle on the written pools
+    o.kp, o.vp = oracle.kv_write(o.raw["k"][:nd], o.raw["v"][:nd], slots, o.raw["k_pool"],
+                                 o.raw["v_pool"])
+    assert_close(f64(app)[past], o.decode(rows=past)[past], "bf16", f"fused append {shape}")
+
+
+def test_shared_prefix_fused_launch_short_rows():
+    """The fused shape with every sequence ending inside the prompt (and
+    NaN in the prompt's unreached slots): outputs from the prompt runs
+    alone."""
+    H, K, D, B, P = FUSED[0]
+    rng = np.random.default_rng(11)
+    lens = rng.integers(0, 16 * P - 40, size=B).tolist()
+    plan = _plan_with_prefix(lens, P, H, K, D, "bf16", seed=11, num_blocks=P + 8)
+    layer = make_tiny_layer(plan, seed=11, fill=float("nan"))
+    g, o = GpuStep(plan, layer), OracleStep(plan, layer)
+    o.kp, o.vp = o.raw["k_pool"], o.raw["v_pool"]
+    out = _prefix_decode(g, P)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert_close(f64(out), o.decode(), "bf16", "fused short rows")
