@@ -276,13 +276,15 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n
  * gathering per user reads the shared prefix blocks once per user; a kernel
  * that reads blocks in place should read them once.  The caller declares
  * that the first shared_prefix_blocks entries of every row of
- * block_tables are the same blocks (row 0's entries are used).  Each KV
- * head's prefix keys are read once for all sequences and every sequence's
- * query rows attend over the prefix tokens they can see (min(seq_lens[b],
- * shared_prefix_blocks * bs)) in runs of the prefix blocks, several
- * sequences' rows sharing each tensor-core tile; the blocks after the
- * prefix are walked as in pkv_paged_attention_decode, continuing each
- * sequence's softmax from its combined prefix runs.  The output is the same attention as
+ * block_tables are the same blocks (row 0's entries are used).  The
+ * prefix keys are read once per chunk of sequences (as many as the
+ * library's shape for the call holds: up to 16 tiles of query rows) and
+ * every sequence's query rows attend over the prefix tokens they can see
+ * (min(seq_lens[b], shared_prefix_blocks * bs)) in runs of the prefix
+ * blocks, several sequences' rows sharing each tensor-core tile; the
+ * blocks after the prefix are walked as in pkv_paged_attention_decode and
+ * each sequence's runs and own parts are combined with log-sum-exp
+ * weights.  The output is the same attention as
  * pkv_paged_attention_decode (within the dtype's tolerance; not bit-equal:
  * the sums are taken in another order).  A row whose first entries differ
  * from row 0's, where the sequence reaches them, is reported as
@@ -291,7 +293,8 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t num_seqs, int32_t n
  *   shared_prefix_blocks  0 .. max_blocks_per_seq (else PKV_ERR_RANGE)
  *   workspace   at least pkv_decode_shared_prefix_workspace_bytes(...)
  *               (the decode workspace plus up to 16 prefix partials per
- *               query row, at most 1,024 per query head)
+ *               query row, at most 1,024 per query head, and 16 bytes
+ *               per sequence and query head)
  *   everything else as for pkv_paged_attention_decode
  */
 size_t pkv_decode_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t n_heads,
