@@ -369,7 +369,8 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * pkv_paged_attention_decode_shared_prefix (preceded, when k_new and v_new
  * are given, by pkv_kv_write of each sequence's new token at its last
  * slot; the prefix runs and their combine are launched by each planned
- * call; the plan covers the blocks after the prefix), bit for bit.
+ * call; the plan covers the blocks after the prefix and, for the fused
+ * launch, where each sequence's parts are), bit for bit.
  *
  * Contract: the planned calls pass the same num_seqs, n_heads, pool shape,
  * max_blocks_per_seq, seq_lens (pointer and contents), max_seq_len and
@@ -382,7 +383,7 @@ pkv_status pkv_paged_attention_decode_append(const void* q, const void* k_new, c
  * differs from its plan's reports PKV_DEVERR_PLAN, stores no k_new / v_new
  * row and writes no output that depends on the plan (with a shared prefix,
  * the rows of sequences that end inside the prefix, which the plan does
- * not cover, are still written); so does one whose workspace was never
+ * not cover, may still be written); so does one whose workspace was never
  * planned or was last used by a call that plans for itself
  * (pkv_paged_attention_decode and the like).
  *
