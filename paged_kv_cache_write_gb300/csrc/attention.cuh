@@ -693,17 +693,18 @@ struct DecodeParams {
   // cluster (their rows per warp: cluster_seqs * rep), and the byte offset
   // of the partial results in shared memory
   int cluster, cluster_seqs, part_off;
-  // wide shared-prefix pass: consumer warps (16-row tiles) per CTA, and 1
-  // if each prefix tile is read by one cluster only (its lines may leave L2
-  // first)
+  // warps of 16 query rows that attend a shared prefix: the consumer warps
+  // of the wide pass, the prompt warps of the fused launch; and (wide pass)
+  // 1 if each prefix tile is read by one cluster only (its lines may leave
+  // L2 first)
   int wide_mt, wide_evict;
-  // fused shared prefix (stream-K kernel): CTAs [0, prompt_items) first
-  // attend item c = ((chunk * n_kv) + KV head) * prompt_runs + run: run
+  // fused shared prefix (stream-K kernel): CTA c < prompt_items also
+  // attends item c = ((chunk * n_kv) + KV head) * prompt_runs + run: run
   // `run` (prompt_bpr blocks of row 0's table) for the prompt_seqs
-  // sequences of `chunk`, consumer warp w carrying the rows of sequences
+  // sequences of `chunk`, prompt warp w carrying the rows of sequences
   // w * (16 / rep) ..; each leaves a partial per row in run slot `run`.
-  // Every group after the prefix then leaves a partial too (a whole one in
-  // run slot prompt_runs) and the prefix merge kernel combines them.
+  // Every group's blocks after the prefix leave partials too (a whole one
+  // in run slot prompt_runs) and the prefix merge kernel combines them.
   int prompt_items, prompt_runs, prompt_bpr, prompt_seqs;
   // fused shared prefix, per (sequence, KV-head group), from the plan: the
   // first and last CTA whose ranges hold the group's blocks after the
