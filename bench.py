@@ -82,6 +82,8 @@ DECODE_TRAFFIC: dict = {
                            "capture": "llama2-70b-decode64, decode + merge, 2 calls"},
     ("bf16", 32, 8, 64): {"ratio": 1.0168, "source_sha256": "a94aaa662fc93776",
                           "capture": "llama-3.2-1b (2 layers), decode + merge, 4 calls"},
+    ("bf16", 32, 32, 128): {"ratio": 1.0014, "source_sha256": "a94aaa662fc93776",
+                            "capture": "llama-7b (2 layers), decode + merge, 4-5 calls"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit -> name
