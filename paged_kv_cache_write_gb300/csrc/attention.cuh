@@ -70,8 +70,9 @@ struct MmaRows {
   uint32_t qa[HD / 16][4];
   float o[HD / 8][4];
   float m[2], l[2];
-  int last[2];
+  int last[2];  // kNoQuery: the row has no query (it computes garbage, never stored)
   int slot[2];  // with several sequences' rows in the tile: the sequence of each row
+  static constexpr int kNoQuery = INT_MIN;
 
   // Rows r hold sequence r / rep (see block_sw's `only`).
   __device__ __forceinline__ void set_row_slots(int rep) {
@@ -89,7 +90,7 @@ struct MmaRows {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const __nv_bfloat16* qp = q_row(g + 8 * h);
-      last[h] = qp ? last_key(g + 8 * h) : -1;
+      last[h] = qp ? last_key(g + 8 * h) : kNoQuery;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
         uint32_t lo = 0, hi = 0;
@@ -186,9 +187,10 @@ struct MmaRows {
       mma_bf16_16816(s[0], qa[kk], kb[0], kb[1]);
       mma_bf16_16816(s[1], qa[kk], kb[2], kb[3]);
     }
-    // causal / length mask: only a block that crosses some row's last key
-    // (warp-uniform test) masks element by element
-    const int first_cut = min(lim[0], lim[1]);
+    // causal / length mask: only a block that crosses some live row's last
+    // key (warp-uniform test) masks element by element
+    const int first_cut = min(last[0] == kNoQuery ? INT_MAX : lim[0],
+                              last[1] == kNoQuery ? INT_MAX : lim[1]);
     if (!__all_sync(0xffffffffu, j0 + kBS - 1 <= first_cut)) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -225,9 +227,10 @@ struct MmaRows {
       }
 #pragma unroll
     for (int h = 0; h < 2; ++h) l[h] = l[h] * alpha[h] + rs[h];
-    // the outputs are rescaled only when some row's maximum moved (alpha 1
-    // elsewhere: skipping the product changes no bit)
-    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+    // the outputs are rescaled only when some live row's maximum moved
+    // (alpha 1 elsewhere: skipping the product changes no bit)
+    if (__any_sync(0xffffffffu, (last[0] != kNoQuery && alpha[0] != 1.f) ||
+                                    (last[1] != kNoQuery && alpha[1] != 1.f))) {
 #pragma unroll
       for (int i = 0; i < HD / 8; ++i) {
         o[i][0] *= alpha[0];
