@@ -78,11 +78,11 @@ DECODE_SOURCES = ("attention.cuh", "device.cuh", "tcgen05.cuh", "decode.cu", "de
 # the decode sources with the given hash only (a different hash reports
 # traffic null; tests/test_bench_host.py fails while a recorded hash is stale).
 DECODE_TRAFFIC: dict = {
-    ("bf16", 64, 8, 128): {"ratio": 1.0138, "source_sha256": "08b2171c43481cd0",
+    ("bf16", 64, 8, 128): {"ratio": 1.0141, "source_sha256": "63ed210e029b166d",
                            "capture": "llama2-70b-decode64, decode + merge, 2 calls"},
-    ("bf16", 32, 8, 64): {"ratio": 1.0165, "source_sha256": "08b2171c43481cd0",
+    ("bf16", 32, 8, 64): {"ratio": 1.0164, "source_sha256": "63ed210e029b166d",
                           "capture": "llama-3.2-1b (2 layers), decode + merge, 4 calls"},
-    ("bf16", 32, 32, 128): {"ratio": 1.0014, "source_sha256": "08b2171c43481cd0",
+    ("bf16", 32, 32, 128): {"ratio": 1.0013, "source_sha256": "63ed210e029b166d",
                             "capture": "llama-7b (2 layers), decode + merge, 4-5 calls"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

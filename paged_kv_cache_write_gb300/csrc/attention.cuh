@@ -1086,9 +1086,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
       item_nb = max(0, min(p.prompt_bpr, p.prefix_blocks - item_j0));
       // The prefix blocks are never written by a decode step, so their
       // loads go out before the dependency wait.  One head of a block is 16
-      // rows of HD * 2 bytes a token pitch apart: 16-byte copies by every
-      // producer lane (the TMA engine moves such short rows slowly), into
-      // the 128-byte-swizzled tile layout, published on pbar once landed.
+      // rows of HD * 2 bytes a token pitch apart, only 2-4 KB: the whole
+      // run is requested at once (16-byte copies by every producer lane,
+      // into the 128-byte-swizzled tile layout) so that enough bytes are in
+      // flight, and published on pbar once landed.
       if (warp == consumers) {
         const int id = lane < item_nb ? __ldg(p.bt + item_j0 + lane) : 0;  // row 0's table
         constexpr int kChunks = kBS * HD * 2 / 16;  // 16-byte pieces of one head of a block
