@@ -13,6 +13,7 @@ from workloads import draw_plan, make_layer, make_tiny_layer, tiny_plan
 pytestmark = pytest.mark.gpu
 
 PKV_DEVERR_PREFIX = 32
+PKV_DEVERR_BLOCK_ID = 1
 
 
 def _prefix_decode(g, P, max_ctas=0):
@@ -382,3 +383,22 @@ def test_shared_prefix_fused_launch_short_rows():
     torch.cuda.synchronize()
     assert int(g.err.item()) == 0
     assert_close(f64(out), o.decode(), "bf16", "fused short rows")
+
+
+@pytest.mark.parametrize("shape", [FUSED[0], WIDE[0]], ids=["fused", "wide"])
+def test_shared_prefix_bad_prompt_block_reported(shape):
+    """A prompt block id past the pool (the same in every table, so the
+    prefix stays common) is reported as PKV_DEVERR_BLOCK_ID and read as
+    zeros: no fault, no stray write (canary bands), finite outputs."""
+    H, K, D, B, P = shape
+    rng = np.random.default_rng(17)
+    lens = _wide_lens(rng, B, P)
+    nb = P + sum(max(0, (l + 15) // 16 - P) for l in lens) + 8
+    plan = _plan_with_prefix(lens, P, H, K, D, "bf16", seed=17, num_blocks=nb)
+    plan.block_tables[:, P // 2] = nb + 3  # every row: past the pool's end
+    layer = make_tiny_layer(plan, seed=17)
+    g = GpuStep(plan, layer)
+    out = _prefix_decode(g, P)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) & PKV_DEVERR_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
