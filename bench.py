@@ -38,8 +38,8 @@ Reported (one JSON line from rank 0):
              at least 50 graph replays, with its error against the oracle
   cpu_baseline  the float64 CPU oracle on a bounded sample of the workload
 
---impl reference times the CPU oracle (the reference implementation of
-this build) on the same workload and metric.
+--impl reference times the float64 CPU oracle, the reference arm, on the
+same workload and metric.
 """
 from __future__ import annotations
 
